@@ -1,0 +1,229 @@
+/*
+ * kvp.h -- C ABI of the paged, prefix-shared KV pool and its attention kernels
+ * (GB300 / sm_103a).
+ *
+ * Conventions for every entry point:
+ *   - returns KVP_OK (0) or a negative KVP_ERR_* code; out-parameters are
+ *     written only on success and state is left unchanged on failure;
+ *   - "device" pointers are CUDA global memory on the current device, owned by
+ *     the caller; "host" pointers are ordinary host memory owned by the caller;
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream);
+ *     device work is enqueued on it and the call returns without synchronising,
+ *     except where a function says it synchronises;
+ *   - bf16 tensors are IEEE bfloat16 bit patterns, 16-byte aligned;
+ *   - a pool handle is not thread-safe: serialise calls on one pool.
+ *
+ * Layouts (row-major, innermost last):
+ *   K pool, V pool   [L][NB][Hkv][bs][d]  bf16   (one (block, kv head) tile is
+ *                                                  a contiguous bs*d run)
+ *   block tables     [S][MB] int32, entries past a sequence's blocks ignored
+ *   decode q, out    [L][S][Hq][d] bf16;   lse [L][S][Hq] fp32, natural log
+ *   verify q, out    [L][B*n][Hq][d] bf16; lse [L][B*n][Hq] fp32
+ *   appended k, v    [L][ntok][Hkv][d] bf16
+ * Query head h reads kv head h / (Hq / Hkv).
+ */
+#ifndef KVP_H
+#define KVP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    KVP_OK = 0,
+    KVP_ERR_INVALID = -1, /* bad argument, unknown sequence, capacity exceeded */
+    KVP_ERR_OOM = -2,     /* no free block or sequence slot                   */
+    KVP_ERR_STATE = -3,   /* operation not possible in the object's state     */
+    KVP_ERR_CUDA = -4,    /* a CUDA runtime call failed                        */
+    KVP_ERR_DEVICE = -5   /* a kernel's own bounds check tripped (see below)  */
+};
+
+/* Device error word bits (kvp_device_error). */
+enum {
+    KVP_DEVERR_BLOCK_ID = 1,    /* a block table entry outside [0, NB): that tile read as 0 */
+    KVP_DEVERR_TREE_PARENT = 2  /* a parent pointer not in [-1, i): treated as a root       */
+};
+
+/* ------------------------------------------------------------------ pool */
+
+/*
+ * A block-paged KV pool: NB blocks of bs token slots per layer, shared by many
+ * sequences through per-sequence block tables with per-block refcounts.
+ * Paper: "Dendrite: O(1) fork latency agent-native inference engine", section
+ * details (16-token paged blocks; tree-shaped KV cache with reference
+ * counting); "Trellis: RadixAttention", section "RadixAttention in Trellis"
+ * (a session holds an ordered list of block ids into one shared pool).
+ */
+typedef struct kvp_pool kvp_pool;
+
+typedef struct {
+    int32_t num_layers;         /* L   */
+    int32_t num_blocks;         /* NB  */
+    int32_t block_size;         /* bs, tokens per block (16 and 32 are the pages' sizes) */
+    int32_t num_kv_heads;       /* Hkv */
+    int32_t head_dim;           /* d, a multiple of 8 */
+    int32_t max_seqs;           /* sequence ids are 0 .. max_seqs-1, lowest free id first */
+    int32_t max_blocks_per_seq; /* MB, block table capacity */
+    uint64_t alloc_seed;        /* free-list order: splitmix64-driven Fisher-Yates
+                                   shuffle of [0, NB); 0 = identity order */
+} kvp_pool_desc;
+
+/* Create a pool over caller-owned device storage k_storage / v_storage, each
+ * [L][NB][Hkv][bs][d] bf16.  Both may be NULL for a bookkeeping-only pool, in
+ * which case seq_append / seq_append_batch return KVP_ERR_STATE (use
+ * seq_reserve).  The pool never allocates or frees KV storage. */
+int kv_pool_create(const kvp_pool_desc *desc, void *k_storage, void *v_storage, kvp_pool **out);
+int kv_pool_destroy(kvp_pool *pool);
+
+/* New empty sequence ("allocate_sequence" in Dendrite's API example). */
+int seq_alloc(kvp_pool *pool, int32_t *seq_out);
+
+/* Copy-on-write fork ("fork_sequence(parent)?" in Dendrite's API example):
+ * the child gets a copy of the parent's block table and every block's
+ * refcount goes up by one.  No KV bytes move and no device work is issued;
+ * cost is O(number of blocks) host integer work, independent of KV size. */
+int seq_fork(kvp_pool *pool, int32_t parent, int32_t *child_out);
+
+/* Release a sequence: every block's refcount drops by one and blocks that
+ * reach zero go back to the free list, last table entry first ("SGLang
+ * RadixAttention", reference-counting section: referenced blocks are never
+ * reclaimed). */
+int seq_free(kvp_pool *pool, int32_t seq);
+
+/* Append ntok tokens' K and V (device, [L][ntok][Hkv][d] bf16 each) to a
+ * sequence.  Copy-on-write ("Dendrite", section details: data is shared until
+ * modified and copied only on write): if the last block is partially filled
+ * and other live sequences also hold it, the sequence first gets a fresh
+ * block with the used slots copied on the device; a full last block just
+ * gets a new block; a block held only by this sequence is written in place.
+ * Enqueues at most one kernel.  k and v must stay valid until it has run. */
+int seq_append(kvp_pool *pool, int32_t seq, const void *k, const void *v, int32_t ntok,
+               void *stream);
+
+/* Append to several distinct sequences in one launch: ntoks[i] tokens to
+ * seqs[i] (host arrays), processed in order with the semantics of seq_append;
+ * k, v: device [L][sum ntoks][Hkv][d], sequence-major.  All or nothing: if the
+ * pool cannot hold every append, nothing changes and KVP_ERR_OOM returns. */
+int seq_append_batch(kvp_pool *pool, int32_t nseq, const int32_t *seqs, const int32_t *ntoks,
+                     const void *k, const void *v, void *stream);
+
+/* Bookkeeping half of seq_append with no device work: reserves slots for ntok
+ * tokens and reports where they go.  slots_out (host, ntok entries, may be
+ * NULL) receives block*bs + slot per token; cow_out (host, 3 entries, may be
+ * NULL) receives {source block, copy block, used slots} or {-1, -1, 0} when no
+ * copy-on-write happened.  The caller is then responsible for the data. */
+int seq_reserve(kvp_pool *pool, int32_t seq, int32_t ntok, int32_t *slots_out, int32_t *cow_out);
+
+/* Host queries. */
+int seq_block_table(const kvp_pool *pool, int32_t seq, int32_t *host_out, int32_t cap,
+                    int32_t *nblocks_out);
+int seq_len(const kvp_pool *pool, int32_t seq, int32_t *len_out);
+int block_refcount(const kvp_pool *pool, int32_t block, int32_t *rc_out);
+int kvp_free_block_count(const kvp_pool *pool, int32_t *n_out);
+int kvp_cow_count(const kvp_pool *pool, int64_t *n_out);
+
+/* Block tables and lengths of n sequences into host arrays h_tables
+ * [n][width] (padded with -1) and h_lens [n]. */
+int kvp_gather_tables(const kvp_pool *pool, const int32_t *seqs, int32_t n, int32_t width,
+                      int32_t *h_tables, int32_t *h_lens);
+
+/* Same, written to device arrays d_tables [n][width] and d_lens [n] (either
+ * may be NULL) with an asynchronous host-to-device copy on `stream`. */
+int kvp_export_tables(kvp_pool *pool, const int32_t *seqs, int32_t n, int32_t width,
+                      int32_t *d_tables, int32_t *d_lens, void *stream);
+
+/* ------------------------------------------------------------- attention */
+
+typedef struct {
+    int32_t num_layers;    /* L: q/out/lse and both pools carry a leading layer axis */
+    int32_t num_q_heads;   /* Hq */
+    int32_t num_kv_heads;  /* Hkv; Hq % Hkv == 0 and Hq / Hkv <= 64 */
+    int32_t head_dim;      /* d: 64 or 128 */
+    int32_t block_size;    /* bs */
+    int32_t num_blocks;    /* NB: table entries outside [0, NB) are reported, not read */
+    float scale;           /* softmax scale; <= 0 selects 1/sqrt(d) */
+    int32_t use_sharing;   /* 1: blocks shared by several sequences are read once per
+                              row tile (cascade); 0: every sequence reads its own
+                              blocks (the unshared baseline) */
+} kvp_attn_desc;
+
+/* Device workspace bytes that paged_decode_attention needs for this batch
+ * (host tables and lengths as for the call).  Returns 0 on invalid input. */
+size_t kvp_decode_workspace_size(const kvp_attn_desc *desc, const int32_t *h_block_tables,
+                                 const int32_t *h_seq_lens, int32_t num_seqs, int32_t max_blocks);
+
+/*
+ * Decode attention over the paged pool: for each layer, sequence s and query
+ * head h, out = softmax(q k^T * scale) v over the first h_seq_lens[s] tokens
+ * of sequence s, and lse = the natural-log log-sum-exp of the scaled scores.
+ * (Decode is one new token attending to the cached keys and values: "SGLang
+ * RadixAttention", section on the KV-cache lifecycle.)  The call attends to
+ * exactly seq_len tokens; append the new token's K/V first to include it.
+ *
+ * Work is planned on the host from h_block_tables / h_seq_lens (host copies of
+ * block_tables, [num_seqs][max_blocks] / [num_seqs]): sequences whose tables
+ * hold the same physical blocks at the same positions are grouped so that a
+ * shared block is read from HBM once for the whole group (per tile of up to
+ * 64 query rows) rather than once per sequence.  Long key ranges are split
+ * across CTAs and merged by log-sum-exp.  The plan is copied into the
+ * workspace with an asynchronous copy from host memory; the host arrays may be
+ * reused when the call returns.
+ *
+ * q: device [L][num_seqs][Hq][d]; k_pool / v_pool: device pools; block_tables:
+ * device [num_seqs][max_blocks]; out: device [L][num_seqs][Hq][d]; lse: device
+ * [L][num_seqs][Hq] or NULL.  workspace: device, ws_bytes >=
+ * kvp_decode_workspace_size(), 256-byte aligned.  Errors: KVP_ERR_INVALID for
+ * an empty sequence, a table entry outside [0, NB) in the host copy, a
+ * too-small workspace or unsupported shapes.
+ */
+int paged_decode_attention(const void *q, const void *k_pool, const void *v_pool,
+                           const int32_t *block_tables, const int32_t *h_block_tables,
+                           const int32_t *h_seq_lens, int32_t num_seqs, int32_t max_blocks,
+                           const kvp_attn_desc *desc, void *out, float *lse, void *workspace,
+                           size_t ws_bytes, void *stream);
+
+size_t kvp_verify_workspace_size(const kvp_attn_desc *desc, const int32_t *h_ctx_lens,
+                                 int32_t batch, int32_t n_draft);
+
+/*
+ * Speculative tree-verify attention ("Inference-Cost-Aware Dynamic Tree
+ * Construction (CAST)", technical summary sections 1-2: the target model
+ * checks a dynamic draft tree of candidate tokens, EAGLE-2/3 style, in one
+ * forward pass).  Sequence b has h_ctx_lens[b] context tokens followed, in
+ * its pages, by n_draft <= 64 draft tokens.  Draft node i (query row b*n + i)
+ * attends to every context token and to the draft tokens of its ancestors and
+ * itself, anc*(i) = {i, parent(i), parent(parent(i)), ...}.
+ * tree_parent: device [batch][n_draft] int32, parent < i or -1 for a root (a
+ * forest is allowed).  Other arguments as for paged_decode_attention with
+ * num_seqs = batch.  A bad parent pointer sets KVP_DEVERR_TREE_PARENT in the
+ * workspace error word and that node is treated as a root.
+ */
+int tree_verify_attention(const void *q, const int32_t *tree_parent, int32_t n_draft,
+                          const void *k_pool, const void *v_pool, const int32_t *block_tables,
+                          const int32_t *h_ctx_lens, int32_t batch, int32_t max_blocks,
+                          const kvp_attn_desc *desc, void *out, float *lse, void *workspace,
+                          size_t ws_bytes, void *stream);
+
+/* Reads (and clears) the device error word that the last attention call on
+ * this workspace left; synchronises `stream`.  *err_out = 0 when clean. */
+int kvp_device_error(void *workspace, void *stream, int32_t *err_out);
+
+/* Host-side view of the decode plan (no device work; for tests and tools):
+ * number of work items, query-row tiles, 64-token KV tiles and partial rows
+ * per (layer, kv head), and the HBM bytes of distinct blocks one call reads,
+ * for an SM count `sm_count`.  Any out-pointer may be NULL. */
+int kvp_decode_plan_stats(const kvp_attn_desc *desc, const int32_t *h_block_tables,
+                          const int32_t *h_seq_lens, int32_t num_seqs, int32_t max_blocks,
+                          int32_t sm_count, int32_t *n_items, int32_t *n_row_tiles,
+                          int32_t *n_kv_tiles, int32_t *n_partial_rows, int64_t *unique_kv_bytes);
+
+const char *kvp_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVP_H */

@@ -1,0 +1,304 @@
+"""Python binding of libkvp (paged, prefix-shared KV pool + attention on GB300).
+
+Argument marshalling only: every function forwards to the C ABI entry point
+of the same name declared in include/kvp.h.  Device arguments are torch CUDA
+tensors (or raw integer device addresses); host arrays are numpy int32
+arrays; `stream` defaults to torch's current CUDA stream.  There is no CPU
+fallback: importing works without a GPU, but every call needs libkvp.so
+(built by `paged_prefix_shared_decode_gb300.build`) and raises KvpError if it
+is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "KvpError", "PoolDesc", "AttnDesc", "load", "lib_path",
+    "kv_pool_create", "kv_pool_destroy", "seq_alloc", "seq_fork", "seq_free", "seq_append",
+    "seq_append_batch", "seq_reserve", "seq_block_table", "seq_len", "block_refcount",
+    "kvp_free_block_count", "kvp_cow_count", "kvp_gather_tables", "kvp_export_tables",
+    "kvp_decode_workspace_size", "paged_decode_attention", "kvp_verify_workspace_size",
+    "tree_verify_attention", "kvp_device_error", "kvp_decode_plan_stats", "kvp_strerror",
+    "KVP_OK", "KVP_ERR_INVALID", "KVP_ERR_OOM", "KVP_ERR_STATE", "KVP_ERR_CUDA", "KVP_ERR_DEVICE",
+]
+
+KVP_OK, KVP_ERR_INVALID, KVP_ERR_OOM, KVP_ERR_STATE, KVP_ERR_CUDA, KVP_ERR_DEVICE = 0, -1, -2, -3, -4, -5
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_HERE, "libkvp.so")
+_lib = None
+
+
+class KvpError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        msg = _strerror(code)
+        super().__init__(f"{what}: {msg} ({code})" if what else f"{msg} ({code})")
+
+
+def _strerror(code):
+    try:
+        return load().kvp_strerror(code).decode()
+    except Exception:  # library missing: still describe the code
+        return {0: "ok", -1: "invalid argument", -2: "out of blocks or sequence slots",
+                -3: "operation not possible in this state", -4: "CUDA runtime error",
+                -5: "device-side check failed"}.get(code, "unknown error")
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("max_seqs", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("alloc_seed", ctypes.c_uint64)]
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("use_sharing", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_SIGS = {
+    "kv_pool_create": ([ctypes.POINTER(PoolDesc), _P, _P, ctypes.POINTER(_P)], ctypes.c_int),
+    "kv_pool_destroy": ([_P], ctypes.c_int),
+    "seq_alloc": ([_P, _I32P], ctypes.c_int),
+    "seq_fork": ([_P, _I32, _I32P], ctypes.c_int),
+    "seq_free": ([_P, _I32], ctypes.c_int),
+    "seq_append": ([_P, _I32, _P, _P, _I32, _P], ctypes.c_int),
+    "seq_append_batch": ([_P, _I32, _P, _P, _P, _P, _P], ctypes.c_int),
+    "seq_reserve": ([_P, _I32, _I32, _P, _P], ctypes.c_int),
+    "seq_block_table": ([_P, _I32, _P, _I32, _I32P], ctypes.c_int),
+    "seq_len": ([_P, _I32, _I32P], ctypes.c_int),
+    "block_refcount": ([_P, _I32, _I32P], ctypes.c_int),
+    "kvp_free_block_count": ([_P, _I32P], ctypes.c_int),
+    "kvp_cow_count": ([_P, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+    "kvp_gather_tables": ([_P, _P, _I32, _I32, _P, _P], ctypes.c_int),
+    "kvp_export_tables": ([_P, _P, _I32, _I32, _P, _P, _P], ctypes.c_int),
+    "kvp_decode_workspace_size": ([ctypes.POINTER(AttnDesc), _P, _P, _I32, _I32], ctypes.c_size_t),
+    "paged_decode_attention": ([_P, _P, _P, _P, _P, _P, _I32, _I32, ctypes.POINTER(AttnDesc),
+                                _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "kvp_verify_workspace_size": ([ctypes.POINTER(AttnDesc), _P, _I32, _I32], ctypes.c_size_t),
+    "tree_verify_attention": ([_P, _P, _I32, _P, _P, _P, _P, _I32, _I32, ctypes.POINTER(AttnDesc),
+                               _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "kvp_device_error": ([_P, _P, _I32P], ctypes.c_int),
+    "kvp_decode_plan_stats": ([ctypes.POINTER(AttnDesc), _P, _P, _I32, _I32, _I32, _I32P, _I32P,
+                               _I32P, _I32P, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+    "kvp_strerror": ([ctypes.c_int], ctypes.c_char_p),
+}
+
+
+def load():
+    """Load libkvp.so (raises KvpError-compatible RuntimeError if not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(lib_path):
+            raise RuntimeError(f"libkvp.so is not built ({lib_path}); run "
+                               "`python -m paged_prefix_shared_decode_gb300.build`")
+        lib = ctypes.CDLL(lib_path)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def _check(rc, what):
+    if rc != KVP_OK:
+        raise KvpError(rc, what)
+
+
+def _dev(x):
+    """Device address of a torch CUDA tensor (or an int address / None)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if not x.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _host_i32(a):
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ------------------------------------------------------------------ pool
+
+def kv_pool_create(desc: PoolDesc, k_storage=None, v_storage=None):
+    h = _P()
+    _check(load().kv_pool_create(ctypes.byref(desc), _dev(k_storage), _dev(v_storage), ctypes.byref(h)),
+           "kv_pool_create")
+    return h.value
+
+
+def kv_pool_destroy(pool):
+    _check(load().kv_pool_destroy(pool), "kv_pool_destroy")
+
+
+def seq_alloc(pool) -> int:
+    s = _I32()
+    _check(load().seq_alloc(pool, ctypes.byref(s)), "seq_alloc")
+    return s.value
+
+
+def seq_fork(pool, parent: int) -> int:
+    s = _I32()
+    _check(load().seq_fork(pool, parent, ctypes.byref(s)), "seq_fork")
+    return s.value
+
+
+def seq_free(pool, seq: int):
+    _check(load().seq_free(pool, seq), "seq_free")
+
+
+def seq_append(pool, seq: int, k, v, ntok: int, stream=None):
+    _check(load().seq_append(pool, seq, _dev(k), _dev(v), ntok, _stream(stream)), "seq_append")
+
+
+def seq_append_batch(pool, seqs, ntoks, k, v, stream=None):
+    s, sp = _host_i32(seqs)
+    n, np_ = _host_i32(ntoks)
+    _check(load().seq_append_batch(pool, len(s), sp, np_, _dev(k), _dev(v), _stream(stream)),
+           "seq_append_batch")
+
+
+def seq_reserve(pool, seq: int, ntok: int):
+    """Bookkeeping-only append: returns (slots int32 [ntok], cow int32 [3])."""
+    slots = np.zeros(max(ntok, 1), np.int32)
+    cow = np.zeros(3, np.int32)
+    _check(load().seq_reserve(pool, seq, ntok, slots.ctypes.data_as(_P), cow.ctypes.data_as(_P)),
+           "seq_reserve")
+    return slots[:ntok], cow
+
+
+def seq_block_table(pool, seq: int) -> np.ndarray:
+    n = _I32()
+    _check(load().seq_block_table(pool, seq, None, 0, ctypes.byref(n)), "seq_block_table")
+    out = np.zeros(max(n.value, 1), np.int32)
+    _check(load().seq_block_table(pool, seq, out.ctypes.data_as(_P), len(out), ctypes.byref(n)),
+           "seq_block_table")
+    return out[:n.value]
+
+
+def seq_len(pool, seq: int) -> int:
+    n = _I32()
+    _check(load().seq_len(pool, seq, ctypes.byref(n)), "seq_len")
+    return n.value
+
+
+def block_refcount(pool, block: int) -> int:
+    n = _I32()
+    _check(load().block_refcount(pool, block, ctypes.byref(n)), "block_refcount")
+    return n.value
+
+
+def kvp_free_block_count(pool) -> int:
+    n = _I32()
+    _check(load().kvp_free_block_count(pool, ctypes.byref(n)), "kvp_free_block_count")
+    return n.value
+
+
+def kvp_cow_count(pool) -> int:
+    n = ctypes.c_int64()
+    _check(load().kvp_cow_count(pool, ctypes.byref(n)), "kvp_cow_count")
+    return n.value
+
+
+def kvp_gather_tables(pool, seqs, width: int):
+    s, sp = _host_i32(seqs)
+    t = np.full((len(s), width), -1, np.int32)
+    lens = np.zeros(len(s), np.int32)
+    _check(load().kvp_gather_tables(pool, sp, len(s), width, t.ctypes.data_as(_P),
+                                    lens.ctypes.data_as(_P)), "kvp_gather_tables")
+    return t, lens
+
+
+def kvp_export_tables(pool, seqs, width: int, d_tables, d_lens=None, stream=None):
+    s, sp = _host_i32(seqs)
+    _check(load().kvp_export_tables(pool, sp, len(s), width, _dev(d_tables), _dev(d_lens),
+                                    _stream(stream)), "kvp_export_tables")
+
+
+# ------------------------------------------------------------- attention
+
+def kvp_decode_workspace_size(desc: AttnDesc, h_tables, h_lens) -> int:
+    t, tp = _host_i32(h_tables)
+    ln, lp = _host_i32(h_lens)
+    n = load().kvp_decode_workspace_size(ctypes.byref(desc), tp, lp, t.shape[0], t.shape[1])
+    if n == 0:
+        raise KvpError(KVP_ERR_INVALID, "kvp_decode_workspace_size")
+    return n
+
+
+def paged_decode_attention(q, k_pool, v_pool, block_tables, h_tables, h_lens, desc: AttnDesc,
+                           out, lse, workspace, ws_bytes=None, stream=None):
+    t, tp = _host_i32(h_tables)
+    ln, lp = _host_i32(h_lens)
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().paged_decode_attention(_dev(q), _dev(k_pool), _dev(v_pool), _dev(block_tables), tp, lp,
+                                         t.shape[0], t.shape[1], ctypes.byref(desc), _dev(out),
+                                         _dev(lse), _dev(workspace), ws_bytes, _stream(stream)),
+           "paged_decode_attention")
+
+
+def kvp_verify_workspace_size(desc: AttnDesc, h_ctx_lens, n_draft: int) -> int:
+    c, cp = _host_i32(h_ctx_lens)
+    n = load().kvp_verify_workspace_size(ctypes.byref(desc), cp, len(c), n_draft)
+    if n == 0:
+        raise KvpError(KVP_ERR_INVALID, "kvp_verify_workspace_size")
+    return n
+
+
+def tree_verify_attention(q, tree_parent, n_draft: int, k_pool, v_pool, block_tables, h_ctx_lens,
+                          max_blocks: int, desc: AttnDesc, out, lse, workspace, ws_bytes=None,
+                          stream=None):
+    c, cp = _host_i32(h_ctx_lens)
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().tree_verify_attention(_dev(q), _dev(tree_parent), n_draft, _dev(k_pool), _dev(v_pool),
+                                        _dev(block_tables), cp, len(c), max_blocks, ctypes.byref(desc),
+                                        _dev(out), _dev(lse), _dev(workspace), ws_bytes,
+                                        _stream(stream)), "tree_verify_attention")
+
+
+def kvp_device_error(workspace, stream=None) -> int:
+    e = _I32()
+    _check(load().kvp_device_error(_dev(workspace), _stream(stream), ctypes.byref(e)), "kvp_device_error")
+    return e.value
+
+
+def kvp_decode_plan_stats(desc: AttnDesc, h_tables, h_lens, sm_count: int = 152) -> dict:
+    t, tp = _host_i32(h_tables)
+    ln, lp = _host_i32(h_lens)
+    vals = [_I32() for _ in range(4)]
+    ub = ctypes.c_int64()
+    _check(load().kvp_decode_plan_stats(ctypes.byref(desc), tp, lp, t.shape[0], t.shape[1], sm_count,
+                                        *[ctypes.byref(v) for v in vals], ctypes.byref(ub)),
+           "kvp_decode_plan_stats")
+    return dict(items=vals[0].value, row_tiles=vals[1].value, kv_tiles=vals[2].value,
+                partial_rows=vals[3].value, unique_kv_bytes=ub.value)
+
+
+def kvp_strerror(code: int) -> str:
+    return load().kvp_strerror(code).decode()

@@ -1,0 +1,479 @@
+// Paged attention work-item kernel and log-sum-exp merge (sm_103a).
+//
+// One CTA (4 warps) runs one work item for one (layer, kv head): up to 64
+// query rows (sequences or draft nodes x the GQA group sharing this kv head)
+// against a list of 64-token KV tiles gathered through the block tables.
+// Each KV tile is staged once in shared memory (cp.async, 16-byte chunks,
+// XOR-swizzled rows, a 3-4 deep ring) and used by every row of the item; this
+// is how a block shared by several sequences is read once for all of them.
+// Q K^T and P V run on bf16 tensor cores (mma.sync m16n8k16, fp32
+// accumulate) with an online softmax in fp32 (base-2 exponent, scale * log2 e
+// folded into the scores).  Rows outside a tile's member interval, tokens past
+// the tile's end and draft tokens that are not ancestors-or-self of a node
+// are masked.  With fewer than 32 rows the item's warps split each tile's
+// tokens and combine their (m, l, o) through shared memory at the end.
+//
+// The item writes out (bf16) and lse (fp32, natural log) directly, or -- when
+// its rows' keys are split over several items -- normalised partial o and a
+// base-2 lse per row, which merge_kernel combines:
+//   out = sum_c w_c o_c / sum_c w_c,  w_c = 2^(lse_c - max lse),
+//   lse = max lse + log2(sum w)   (converted to natural log).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kvp_internal.h"
+
+namespace kvp {
+namespace {
+
+constexpr int kThreads = 128;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                 "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 2^x on the SFU (hardware instruction); 2^-inf = +0.
+__device__ __forceinline__ float exp2_sfu(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t ld_u32(const void *p) {
+    return __ldg(reinterpret_cast<const unsigned int *>(p));
+}
+
+// ancestor-or-self bitmask of draft node i of sequence b (bit j = node j)
+__device__ uint64_t ancestor_mask(const int32_t *parent, int b, int i, int n, int32_t *err) {
+    uint64_t m = 0;
+    int j = i;
+    for (int step = 0; step < 64 && j >= 0; ++step) {
+        m |= 1ull << j;
+        int p = __ldg(parent + (size_t)b * n + j);
+        if (p >= j || p < -1) {
+            atomicOr(err, 2);
+            break;
+        }
+        j = p;
+    }
+    return m;
+}
+
+template <int D, int TS>
+struct Cfg {
+    static constexpr int CH = D / 8;                       // 16-byte chunks per token row
+    static constexpr int TILE_BYTES = kTileTokens * D * 2;  // one K (or V) tile
+    static constexpr int NSTAGE = D == 64 ? 4 : 3;
+    static constexpr int SMEM = NSTAGE * 2 * TILE_BYTES;
+    static constexpr int TOKW = kTileTokens / TS;  // tokens per warp per tile
+    static constexpr int NT = TOKW / 8;            // score n-tiles per warp
+    static constexpr int KS = D / 16;              // k-steps of Q K^T
+    static constexpr int NO = D / 8;               // n-tiles of O
+};
+
+template <int D, int TS>
+__global__ void __launch_bounds__(kThreads) attn_item_kernel(const AttnLaunch a) {
+    using C = Cfg<D, TS>;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    int bid = blockIdx.x;
+    const int item_idx = bid % a.n_items;
+    bid /= a.n_items;
+    const int kvh = bid % a.Hkv;
+    const int l = bid / a.Hkv;
+    const WorkItem it = a.items[item_idx];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rg = warp / TS, sp = warp % TS;
+    const int G = a.G;
+    const int n_rows = it.n_members * G;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int row0 = rg * 16 + gq, row1 = row0 + 8;
+    const bool has0 = row0 < n_rows, has1 = row1 < n_rows;
+    const int mem0 = row0 / G, mem1 = row1 / G;
+
+    const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(a.q);
+    const __nv_bfloat16 *kpool = static_cast<const __nv_bfloat16 *>(a.k_pool);
+    const __nv_bfloat16 *vpool = static_cast<const __nv_bfloat16 *>(a.v_pool);
+
+    int qt0 = 0, qt1 = 0;
+    const __nv_bfloat16 *q0 = nullptr, *q1 = nullptr;
+    if (has0) {
+        qt0 = a.members[it.member_off + mem0];
+        q0 = qb + (((size_t)l * a.nq + qt0) * a.Hq + kvh * G + row0 % G) * D;
+    }
+    if (has1) {
+        qt1 = a.members[it.member_off + mem1];
+        q1 = qb + (((size_t)l * a.nq + qt1) * a.Hq + kvh * G + row1 % G) * D;
+    }
+    uint32_t qf[C::KS][4];
+#pragma unroll
+    for (int kk = 0; kk < C::KS; ++kk) {
+        const int c = kk * 16 + 2 * tq;
+        qf[kk][0] = has0 ? ld_u32(q0 + c) : 0u;
+        qf[kk][1] = has1 ? ld_u32(q1 + c) : 0u;
+        qf[kk][2] = has0 ? ld_u32(q0 + c + 8) : 0u;
+        qf[kk][3] = has1 ? ld_u32(q1 + c + 8) : 0u;
+    }
+    uint64_t tm0 = ~0ull, tm1 = ~0ull;
+    if (a.tree_parent) {
+        if (has0) tm0 = ancestor_mask(a.tree_parent, qt0 / a.n_draft, qt0 % a.n_draft, a.n_draft, a.err);
+        if (has1) tm1 = ancestor_mask(a.tree_parent, qt1 / a.n_draft, qt1 % a.n_draft, a.n_draft, a.err);
+    }
+
+    float o[C::NO][4];
+#pragma unroll
+    for (int n = 0; n < C::NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    const int ntile = it.tile_end - it.tile_begin;
+    const size_t head_stride = (size_t)a.bs * D;
+
+    auto issue = [&](int t) {
+        const KvTile kt = a.tiles[it.tile_begin + t];
+        const int ntok = kt.ntok_flags & 0xFFFF;
+        unsigned char *sK = smem + (t % C::NSTAGE) * 2 * C::TILE_BYTES;
+        const uint32_t dK = smem_addr(sK), dV = dK + C::TILE_BYTES;
+        const int32_t *trow = a.tables + (size_t)kt.row * a.MB;
+#pragma unroll
+        for (int i = 0; i < kTileTokens * C::CH / kThreads; ++i) {
+            const int x = threadIdx.x + i * kThreads;
+            const int tok = x / C::CH, c = x % C::CH;
+            const uint32_t off = tok * D * 2 + ((c ^ (tok & 7)) << 4);
+            const __nv_bfloat16 *sk = kpool, *sv = vpool;
+            int bytes = 0;
+            if (tok < ntok) {
+                const int pos = kt.tok0 + tok;
+                const int blk = __ldg(trow + pos / a.bs);
+                if ((unsigned)blk < (unsigned)a.NB) {
+                    const size_t e = (((size_t)l * a.NB + blk) * a.Hkv + kvh) * head_stride +
+                                     (size_t)(pos % a.bs) * D + c * 8;
+                    sk = kpool + e;
+                    sv = vpool + e;
+                    bytes = 16;
+                } else if (c == 0) {
+                    atomicOr(a.err, 1);
+                }
+            }
+            cp_async16(dK + off, sk, bytes);
+            cp_async16(dV + off, sv, bytes);
+        }
+    };
+
+#pragma unroll
+    for (int t = 0; t < C::NSTAGE - 1; ++t) {
+        if (t < ntile) issue(t);
+        cp_async_commit();
+    }
+
+    for (int t = 0; t < ntile; ++t) {
+        cp_async_wait<C::NSTAGE - 2>();
+        __syncthreads();
+        if (t + C::NSTAGE - 1 < ntile) issue(t + C::NSTAGE - 1);
+        cp_async_commit();
+
+        const KvTile kt = a.tiles[it.tile_begin + t];
+        const int ntok = kt.ntok_flags & 0xFFFF;
+        const bool tree = (kt.ntok_flags >> 16) & kTileTree;
+        const int mlo = kt.members & 0xFFFF, mhi = kt.members >> 16;
+        const bool in0 = has0 && mem0 >= mlo && mem0 < mhi;
+        const bool in1 = has1 && mem1 >= mlo && mem1 < mhi;
+        const int tb = sp * C::TOKW;
+        if (!__any_sync(0xffffffffu, in0 || in1) || tb >= ntok) continue;
+
+        const unsigned char *sK = smem + (t % C::NSTAGE) * 2 * C::TILE_BYTES;
+        const uint32_t aK = smem_addr(sK), aV = aK + C::TILE_BYTES;
+
+        float s[C::NT][4];
+#pragma unroll
+        for (int j = 0; j < C::NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < C::KS; ++kk) {
+#pragma unroll
+            for (int j2 = 0; j2 < C::NT / 2; ++j2) {
+                const int tok = tb + j2 * 16 + (lane & 7) + ((lane >> 4) << 3);
+                const int ch = kk * 2 + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(aK + tok * D * 2 + ((ch ^ (tok & 7)) << 4), b0, b1, b2, b3);
+                mma16816(s[2 * j2], qf[kk], b0, b1);
+                mma16816(s[2 * j2 + 1], qf[kk], b2, b3);
+            }
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < C::NT; ++j) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tok = tb + j * 8 + 2 * tq + (e & 1);
+                const bool hi = e >= 2;
+                bool ok = tok < ntok && (hi ? in1 : in0);
+                if (tree) ok = ok && (((hi ? tm1 : tm0) >> (tok & 63)) & 1ull);
+                const float v = ok ? s[j][e] * a.scale_log2 : -INFINITY;
+                s[j][e] = v;
+                if (hi) mx1 = fmaxf(mx1, v);
+                else mx0 = fmaxf(mx0, v);
+            }
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float b0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float b1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = exp2_sfu(m0 - b0), al1 = exp2_sfu(m1 - b1);
+        m0 = mn0;
+        m1 = mn1;
+        float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < C::NT; ++j) {
+            s[j][0] = exp2_sfu(s[j][0] - b0);
+            s[j][1] = exp2_sfu(s[j][1] - b0);
+            s[j][2] = exp2_sfu(s[j][2] - b1);
+            s[j][3] = exp2_sfu(s[j][3] - b1);
+            rs0 += s[j][0] + s[j][1];
+            rs1 += s[j][2] + s[j][3];
+        }
+        l0 = l0 * al0 + rs0;
+        l1 = l1 * al1 + rs1;
+#pragma unroll
+        for (int n = 0; n < C::NO; ++n) {
+            o[n][0] *= al0;
+            o[n][1] *= al0;
+            o[n][2] *= al1;
+            o[n][3] *= al1;
+        }
+#pragma unroll
+        for (int k2 = 0; k2 < C::NT / 2; ++k2) {
+            const uint32_t pa[4] = {pack_bf16x2(s[2 * k2][0], s[2 * k2][1]),
+                                    pack_bf16x2(s[2 * k2][2], s[2 * k2][3]),
+                                    pack_bf16x2(s[2 * k2 + 1][0], s[2 * k2 + 1][1]),
+                                    pack_bf16x2(s[2 * k2 + 1][2], s[2 * k2 + 1][3])};
+            const int tok = tb + k2 * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+            for (int n2 = 0; n2 < C::NO / 2; ++n2) {
+                const int ch = n2 * 2 + (lane >> 4);
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_t(aV + tok * D * 2 + ((ch ^ (tok & 7)) << 4), v0, v1, v2, v3);
+                mma16816(o[2 * n2], pa, v0, v1);
+                mma16816(o[2 * n2 + 1], pa, v2, v3);
+            }
+        }
+    }
+
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+    if constexpr (TS > 1) {
+        // combine the token-split warps of each row group through shared memory
+        cp_async_wait<0>();
+        __syncthreads();
+        float *red = reinterpret_cast<float *>(smem);
+        constexpr int PER_WARP = (C::NO * 4 + 4) * 32;
+        float *mine = red + warp * PER_WARP;
+#pragma unroll
+        for (int n = 0; n < C::NO; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mine[(n * 4 + e) * 32 + lane] = o[n][e];
+        mine[(C::NO * 4 + 0) * 32 + lane] = m0;
+        mine[(C::NO * 4 + 1) * 32 + lane] = m1;
+        mine[(C::NO * 4 + 2) * 32 + lane] = l0;
+        mine[(C::NO * 4 + 3) * 32 + lane] = l1;
+        __syncthreads();
+        if (sp == 0) {
+#pragma unroll
+            for (int s2 = 1; s2 < TS; ++s2) {
+                const float *oth = red + (warp + s2) * PER_WARP;
+                const float om0 = oth[(C::NO * 4 + 0) * 32 + lane];
+                const float om1 = oth[(C::NO * 4 + 1) * 32 + lane];
+                const float ol0 = oth[(C::NO * 4 + 2) * 32 + lane];
+                const float ol1 = oth[(C::NO * 4 + 3) * 32 + lane];
+                const float nm0 = fmaxf(m0, om0), nm1 = fmaxf(m1, om1);
+                const float c0 = nm0 == -INFINITY ? 0.f : nm0, c1 = nm1 == -INFINITY ? 0.f : nm1;
+                const float sa0 = exp2_sfu(m0 - c0), sb0 = exp2_sfu(om0 - c0);
+                const float sa1 = exp2_sfu(m1 - c1), sb1 = exp2_sfu(om1 - c1);
+#pragma unroll
+                for (int n = 0; n < C::NO; ++n) {
+                    o[n][0] = o[n][0] * sa0 + oth[(n * 4 + 0) * 32 + lane] * sb0;
+                    o[n][1] = o[n][1] * sa0 + oth[(n * 4 + 1) * 32 + lane] * sb0;
+                    o[n][2] = o[n][2] * sa1 + oth[(n * 4 + 2) * 32 + lane] * sb1;
+                    o[n][3] = o[n][3] * sa1 + oth[(n * 4 + 3) * 32 + lane] * sb1;
+                }
+                l0 = l0 * sa0 + ol0 * sb0;
+                l1 = l1 * sa1 + ol1 * sb1;
+                m0 = nm0;
+                m1 = nm1;
+            }
+        }
+    }
+    if (sp != 0) return;
+
+    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
+    const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+    const float lse2_0 = l0 > 0.f ? m0 + __log2f(l0) : -INFINITY;
+    const float lse2_1 = l1 > 0.f ? m1 + __log2f(l1) : -INFINITY;
+    if (it.out_base < 0) {
+        __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(a.out);
+        if (has0) {
+            __nv_bfloat16 *dst = ob + (((size_t)l * a.nq + qt0) * a.Hq + kvh * G + row0 % G) * D;
+#pragma unroll
+            for (int n = 0; n < C::NO; ++n)
+                *reinterpret_cast<uint32_t *>(dst + n * 8 + 2 * tq) =
+                    pack_bf16x2(o[n][0] * inv0, o[n][1] * inv0);
+            if (a.lse && tq == 0)
+                a.lse[((size_t)l * a.nq + qt0) * a.Hq + kvh * G + row0 % G] = lse2_0 * 0.6931471805599453f;
+        }
+        if (has1) {
+            __nv_bfloat16 *dst = ob + (((size_t)l * a.nq + qt1) * a.Hq + kvh * G + row1 % G) * D;
+#pragma unroll
+            for (int n = 0; n < C::NO; ++n)
+                *reinterpret_cast<uint32_t *>(dst + n * 8 + 2 * tq) =
+                    pack_bf16x2(o[n][2] * inv1, o[n][3] * inv1);
+            if (a.lse && tq == 0)
+                a.lse[((size_t)l * a.nq + qt1) * a.Hq + kvh * G + row1 % G] = lse2_1 * 0.6931471805599453f;
+        }
+    } else {
+        const size_t rb = ((size_t)l * a.Hkv + kvh) * a.P + it.out_base;
+        if (has0) {
+            float *dst = a.part_o + (rb + row0) * D;
+#pragma unroll
+            for (int n = 0; n < C::NO; ++n)
+                *reinterpret_cast<float2 *>(dst + n * 8 + 2 * tq) = make_float2(o[n][0] * inv0, o[n][1] * inv0);
+            if (tq == 0) a.part_lse[rb + row0] = lse2_0;
+        }
+        if (has1) {
+            float *dst = a.part_o + (rb + row1) * D;
+#pragma unroll
+            for (int n = 0; n < C::NO; ++n)
+                *reinterpret_cast<float2 *>(dst + n * 8 + 2 * tq) = make_float2(o[n][2] * inv1, o[n][3] * inv1);
+            if (tq == 0) a.part_lse[rb + row1] = lse2_1;
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) merge_kernel(const AttnLaunch a) {
+    const int qt = blockIdx.x, l = blockIdx.y;
+    const MergeDesc md = a.merge[qt];
+    if (md.n_chunks == 0) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int V = D / 32;   // values per lane
+    for (int h = warp; h < a.Hq; h += kThreads / 32) {
+        const int kvh = h / a.G, g = h % a.G;
+        const size_t rb = ((size_t)l * a.Hkv + kvh) * a.P + md.base + md.m_pos * a.G + g;
+        float M = -INFINITY;
+        for (int c = lane; c < md.n_chunks; c += 32) M = fmaxf(M, a.part_lse[rb + (size_t)c * md.stride]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float Mb = M == -INFINITY ? 0.f : M;
+        float acc[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = 0.f;
+        float wsum = 0.f;
+        for (int c = 0; c < md.n_chunks; ++c) {
+            const size_t pr = rb + (size_t)c * md.stride;
+            const float w = exp2_sfu(a.part_lse[pr] - Mb);
+            wsum += w;
+            const float *src = a.part_o + pr * D + lane * V;
+            if constexpr (V == 2) {
+                const float2 x = *reinterpret_cast<const float2 *>(src);
+                acc[0] += w * x.x;
+                acc[1] += w * x.y;
+            } else {
+                const float4 x = *reinterpret_cast<const float4 *>(src);
+                acc[0] += w * x.x;
+                acc[1] += w * x.y;
+                acc[2] += w * x.z;
+                acc[3] += w * x.w;
+            }
+        }
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
+                             (((size_t)l * a.nq + qt) * a.Hq + h) * D + lane * V;
+#pragma unroll
+        for (int v = 0; v < V; v += 2)
+            *reinterpret_cast<uint32_t *>(dst + v) = pack_bf16x2(acc[v] * inv, acc[v + 1] * inv);
+        if (a.lse && lane == 0)
+            a.lse[((size_t)l * a.nq + qt) * a.Hq + h] =
+                (wsum > 0.f ? Mb + __log2f(wsum) : -INFINITY) * 0.6931471805599453f;
+    }
+}
+
+template <int D, int TS>
+cudaError_t launch_items(const AttnLaunch &a, cudaStream_t stream) {
+    using C = Cfg<D, TS>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(attn_item_kernel<D, TS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const long long blocks = (long long)a.n_items * a.Hkv * a.L;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    attn_item_kernel<D, TS><<<(unsigned)blocks, kThreads, C::SMEM, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const AttnLaunch &a, cudaStream_t stream) {
+    cudaError_t e;
+    if (a.ts == 4) e = launch_items<D, 4>(a, stream);
+    else if (a.ts == 2) e = launch_items<D, 2>(a, stream);
+    else e = launch_items<D, 1>(a, stream);
+    if (e != cudaSuccess || a.P == 0) return e;
+    dim3 grid(a.nq, a.L);
+    merge_kernel<D><<<grid, kThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream) {
+    if (a.D == 64) return launch_d<64>(a, stream);
+    if (a.D == 128) return launch_d<128>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kvp

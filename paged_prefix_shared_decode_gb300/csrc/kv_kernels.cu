@@ -1,0 +1,123 @@
+// K/V write kernel (sm_103a): copy-on-write block copies and the scatter of
+// appended tokens into their (block, slot), in one launch.
+//
+// Copy-on-write ("Dendrite" page, section details: blocks are shared until a
+// branch writes and are copied only then): for each (source, copy, used)
+// triple, the first `used` slots of every (layer, kv head) tile of the source
+// block are copied into the copy block, K and V.  Because a tile is stored
+// [bs][d], those slots are one contiguous run of used*d elements.
+// The scatter writes token i of the append, [L][ntok][Hkv][d], to slot
+// slots[i] = block*bs + slot.  The copies touch slots < used of the copy
+// block and the scatter slots >= used, so both run in the same grid.
+// Every thread moves 16-byte chunks (d is a multiple of 8).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "kvp_internal.h"
+
+namespace kvp {
+namespace {
+
+constexpr int kMaxSlots = 4096;   // tokens per launch (16 KB of parameters)
+constexpr int kMaxCow = 256;      // copy-on-write triples per launch
+
+struct KvWriteArgs {
+    uint4 *k_pool;
+    uint4 *v_pool;
+    const uint4 *k;
+    const uint4 *v;
+    int32_t L, NB, Hkv, bs, CH;       // CH = 16-byte chunks per head row (d / 8)
+    int32_t ntok_total;               // tokens in k / v (row stride of the source)
+    int32_t tok_begin, ntok;          // this launch's tokens
+    int32_t ncow;
+    int64_t cow_chunks;               // sum over triples of L*Hkv*used*CH
+    int32_t cow[3 * kMaxCow];
+    int32_t slots[kMaxSlots];
+};
+
+__global__ void __launch_bounds__(256) kv_write_kernel(const __grid_constant__ KvWriteArgs a) {
+    const int64_t tok_chunks = (int64_t)a.L * a.ntok * a.Hkv * a.CH;
+    const int64_t total = 2 * (a.cow_chunks + tok_chunks);
+    const int64_t tile = (int64_t)a.bs * a.CH;     // chunks per (block, head) tile
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
+         x += (int64_t)gridDim.x * blockDim.x) {
+        const bool is_v = x & 1;
+        int64_t y = x >> 1;
+        uint4 *pool = is_v ? a.v_pool : a.k_pool;
+        if (y < a.cow_chunks) {
+            // find the triple (few per launch)
+            int i = 0;
+            int64_t per = 0;
+            for (; i < a.ncow; ++i) {
+                per = (int64_t)a.L * a.Hkv * a.cow[3 * i + 2] * a.CH;
+                if (y < per) break;
+                y -= per;
+            }
+            const int64_t run = (int64_t)a.cow[3 * i + 2] * a.CH;   // chunks per (layer, head)
+            const int64_t lh = y / run, c = y % run;
+            const int64_t l = lh / a.Hkv, h = lh % a.Hkv;
+            const int64_t src = ((l * a.NB + a.cow[3 * i]) * a.Hkv + h) * tile + c;
+            const int64_t dst = ((l * a.NB + a.cow[3 * i + 1]) * a.Hkv + h) * tile + c;
+            pool[dst] = pool[src];
+        } else {
+            y -= a.cow_chunks;
+            const int64_t c = y % a.CH;
+            int64_t r = y / a.CH;
+            const int64_t h = r % a.Hkv;
+            r /= a.Hkv;
+            const int64_t t = r % a.ntok;
+            const int64_t l = r / a.ntok;
+            const int32_t slot = a.slots[t];
+            const int64_t blk = slot / a.bs, sl = slot % a.bs;
+            const uint4 *srcp = is_v ? a.v : a.k;
+            const int64_t src = ((l * a.ntok_total + a.tok_begin + t) * a.Hkv + h) * a.CH + c;
+            const int64_t dst = ((l * a.NB + blk) * a.Hkv + h) * tile + sl * a.CH + c;
+            pool[dst] = srcp[src];
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_write(const KvWrite &w, cudaStream_t stream) {
+    static KvWriteArgs args;   // large; filled per launch (host code is not reentrant per pool)
+    int cow_done = 0, tok_done = 0;
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 152;
+    if (w.ncow == 0 && w.ntok == 0) return cudaSuccess;
+    while (cow_done < w.ncow || tok_done < w.ntok) {
+        KvWriteArgs &a = args;
+        a.k_pool = static_cast<uint4 *>(w.k_pool);
+        a.v_pool = static_cast<uint4 *>(w.v_pool);
+        a.k = static_cast<const uint4 *>(w.k);
+        a.v = static_cast<const uint4 *>(w.v);
+        a.L = w.L; a.NB = w.NB; a.Hkv = w.Hkv; a.bs = w.bs; a.CH = w.d / 8;
+        a.ntok_total = w.ntok;
+        a.ncow = std::min(kMaxCow, w.ncow - cow_done);
+        a.cow_chunks = 0;
+        for (int i = 0; i < a.ncow; ++i) {
+            a.cow[3 * i] = w.cow[3 * (cow_done + i)];
+            a.cow[3 * i + 1] = w.cow[3 * (cow_done + i) + 1];
+            a.cow[3 * i + 2] = w.cow[3 * (cow_done + i) + 2];
+            a.cow_chunks += (int64_t)w.L * w.Hkv * a.cow[3 * i + 2] * a.CH;
+        }
+        a.tok_begin = tok_done;
+        a.ntok = std::min(kMaxSlots, w.ntok - tok_done);
+        for (int i = 0; i < a.ntok; ++i) a.slots[i] = w.slots[tok_done + i];
+        const int64_t total = 2 * (a.cow_chunks + (int64_t)w.L * a.ntok * w.Hkv * a.CH);
+        const int64_t want = (total + 255) / 256;
+        const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * 16));
+        kv_write_kernel<<<blocks, 256, 0, stream>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        cow_done += a.ncow;
+        tok_done += a.ntok;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace kvp

@@ -1,0 +1,62 @@
+"""The C ABI library loads without a GPU and exports every symbol that
+include/kvp.h declares; error codes map to messages."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_prefix_shared_decode_gb300 as kvp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", fn)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", src, re.M):
+            if m.group(1) not in ("if", "while", "for", "sizeof", "return"):
+                names.append(m.group(1))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    for must in ("kv_pool_create", "seq_alloc", "seq_fork", "seq_append", "seq_free",
+                 "paged_decode_attention", "tree_verify_attention"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(kvp.load()._name)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_exposes_same_names():
+    missing = [n for n in declared_functions() if not hasattr(kvp, n)]
+    assert not missing, missing
+
+
+def test_strerror_and_invalid_arguments():
+    assert kvp.kvp_strerror(kvp.KVP_ERR_OOM) == "out of blocks or sequence slots"
+    lib = kvp.load()
+    assert lib.kv_pool_create(None, None, None, None) == kvp.KVP_ERR_INVALID
+    assert lib.seq_alloc(None, None) == kvp.KVP_ERR_INVALID
+    d = kvp.PoolDesc(1, 4, 16, 1, 12, 2, 2, 0)          # head_dim not a multiple of 8
+    with pytest.raises(kvp.KvpError):
+        kvp.kv_pool_create(d)
+
+
+def test_bookkeeping_pool_refuses_device_appends():
+    p = kvp.kv_pool_create(kvp.PoolDesc(1, 8, 16, 1, 8, 2, 4, 0))
+    s = kvp.seq_alloc(p)
+    with pytest.raises(kvp.KvpError) as e:
+        kvp.seq_append(p, s, 0, 0, 1, stream=0)
+    assert e.value.code == kvp.KVP_ERR_STATE
+    kvp.kv_pool_destroy(p)
