@@ -1,0 +1,614 @@
+#!/usr/bin/env python
+"""Benchmark: decode attention tokens/s and achieved HBM GB/s over a
+block-paged, prefix-shared KV pool on GB300.
+
+Default workload (one GPU): Dendrite-shaped fork decode -- TinyLlama-1.1B
+attention shapes (22 layers, 32 query / 4 kv heads, d 64), block 16, a
+4096-token prefix forked into 6 branches with U{0..512} private tokens each.
+One step = the whole hot path for one decode token per branch: append its K/V
+(batched scatter, copy-on-write where needed), export the block tables, plan,
+and run paged attention over all 22 layers (work-item kernel + log-sum-exp
+merge).  Inputs are resident in HBM; L2 is flushed (a write of 2x its size)
+between timed steps, outside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload dendrite|trellis0.5|mcts|verify8|...] [--sweep]
+
+N > 1 runs independent replicas, one per GPU (torchrun; no data-path
+collective).  `--impl reference` times the fp64 CPU oracle on the host cores
+on the same workload and prints the same JSON line with "impl": "reference".
+Prints exactly one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "decode attention tokens/s and achieved HBM GB/s (% of GB300 peak) vs φ/branches"
+KERNEL_SRC = os.path.join(ROOT, "paged_prefix_shared_decode_gb300", "csrc", "attn_kernels.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_item_kernel_traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dendrite")
+    ap.add_argument("--sweep", action="store_true", help="add the phi / MCTS / verify sweep")
+    ap.add_argument("--no-sharing", action="store_true", help="ablation: every sequence reads its own blocks")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return a
+
+
+def workload(name: str, extra_steps: int):
+    """Named workloads; `extra_steps` decode steps of headroom in the pool."""
+    if name == "dendrite":
+        w = W.dendrite()
+    elif name.startswith("trellis"):
+        w = W.trellis(float(name[len("trellis"):] or 0.5))
+    elif name == "mcts":
+        w = W.mcts()
+    elif name.startswith("verify"):
+        w = W.verify_tree(int(name[len("verify"):] or 8))
+    elif name == "tiny":
+        w = W.tiny_fork()
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    bs = w.shapes.bs
+    w.num_blocks += len(w.batch) * (extra_steps * w.step_tokens // bs + 3)
+    w.max_blocks_per_seq += extra_steps * w.step_tokens // bs + 2
+    return w
+
+
+def describe(w) -> str:
+    s = w.shapes
+    base = f"{s.L} layers, {s.Hq}q/{s.Hkv}kv heads, d {s.d}, block {s.bs}, bf16"
+    if w.name == "dendrite":
+        return (f"Dendrite-shaped fork decode: TinyLlama-1.1B attention ({base}); 4096-token prefix "
+                f"forked into 6 branches with private tokens {w.info['private']}; one decode token per "
+                f"branch per step")
+    if w.name.startswith("trellis"):
+        return (f"Trellis-shaped prefix sweep: {base}; 64 sessions, L=512 prompt, phi={w.info['phi']} "
+                f"(prefixBlocks={w.info['prefix_blocks']}), decode at length 576")
+    if w.name == "mcts":
+        return f"MCTS radix tree: Llama-3-8B attention ({base}); 2048-token root, 4-ary depth 4, 64/edge"
+    if w.name.startswith("verify"):
+        return (f"speculative tree verify: Llama-3-8B attention ({base}); B={len(w.batch)}, "
+                f"context 2048, 64-node draft tree")
+    return f"{w.name}: {base}"
+
+
+# ---------------------------------------------------------------- clocks
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1])); smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------- distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of x over all ranks (identity for one process).  NCCL reduces a
+    device tensor; gloo (CPU tests) a host tensor."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def traffic_for_current_kernel():
+    """DRAM bytes per launch from the committed ncu capture, if the kernel
+    source has not changed since; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        h = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+        if t.get("source_sha256") == h:
+            return t
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+# ------------------------------------------------------------- our path
+
+def run_ours(a, rank, world, local):
+    import torch
+    import paged_prefix_shared_decode_gb300 as kvp
+    from paged_prefix_shared_decode_gb300.runner import PoolRunner, bf16_tensor
+
+    kvp.load()   # fails loudly without the CUDA library
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    K, Wm = a.steps, a.warmup
+    E2E = max(3, min(K, 10))
+    w = workload(a.workload, Wm + K + E2E + 2)
+    if w.name.startswith("verify"):
+        return run_verify_bench(a, w, rank, world, dev)
+    s = w.shapes
+    S = len(w.batch)
+    r = PoolRunner(w, alloc_seed=1)
+    r.run_ops()
+    desc = r.attn_desc(use_sharing=not a.no_sharing)
+    MB = w.max_blocks_per_seq
+
+    # per-step inputs (host, generated once) and their device copies
+    nsteps = Wm + K
+    host_kv = [W.step_kv(w, i) for i in range(nsteps + E2E)]
+    host_q = [W.step_q(w, i) for i in range(nsteps + E2E)]
+    kd = [bf16_tensor(k) for k, _ in host_kv[:nsteps]]
+    vd = [bf16_tensor(v) for _, v in host_kv[:nsteps]]
+    qd = [bf16_tensor(q) for q in host_q[:nsteps]]
+    out = torch.empty((s.L, S, s.Hq, s.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((s.L, S, s.Hq), dtype=torch.float32, device=dev)
+    seqs = np.array([r.ids[n] for n in w.batch], np.int32)
+    ntoks = np.full(S, w.step_tokens, np.int32)
+    # workspace: twice what the starting state needs covers the growth of
+    # the run (a few tokens per sequence)
+    t0, l0 = kvp.kvp_gather_tables(r.pool, seqs, MB)
+    ws_bytes = 2 * kvp.kvp_decode_workspace_size(desc, t0, l0) + (8 << 20)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e4 in ev:                       # materialise the CUDA events
+        for e in e4:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+
+    def step(i, timed_events=None):
+        kvp.seq_append_batch(r.pool, seqs, ntoks, kd[i], vd[i], stream=stream)
+        ht, hl = kvp.kvp_gather_tables(r.pool, seqs, MB)
+        if timed_events is not None:
+            kvp.kvp_set_kernel_events(timed_events[2], timed_events[3])
+        kvp.paged_decode_attention(qd[i], r.k_pool, r.v_pool, ht, hl, desc, out, lse, ws, ws_bytes,
+                                   stream=stream)
+        kvp.kvp_set_kernel_events(None, None)
+        return ht, hl
+
+    for i in range(Wm):
+        flush.fill_(i & 0xFF)
+        step(i)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = Clocks(local)
+    clocks.start()
+    launches0 = kvp.kvp_kernel_launches()
+    step_tables = []
+    for j in range(K):
+        flush.fill_(j & 0xFF)
+        ev[j][0].record(stream)
+        ht, hl = step(Wm + j, ev[j])
+        ev[j][1].record(stream)
+        step_tables.append((ht, hl))
+    torch.cuda.synchronize(dev)
+    launches = kvp.kvp_kernel_launches() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [ev[j][0].elapsed_time(ev[j][1]) for j in range(K)]
+    kern_ms = [ev[j][2].elapsed_time(ev[j][3]) for j in range(K)]
+    total_ms = max_over_ranks(float(sum(step_ms)), world)
+    tokens = S * w.step_tokens * K * world
+    value = tokens / (total_ms / 1e3)
+    ub = [kvp.kvp_decode_plan_stats(desc, ht, hl)["unique_kv_bytes"] for ht, hl in step_tables]
+    stats = kvp.kvp_decode_plan_stats(desc, *step_tables[-1])
+    peak, peak_kind = peaks()
+    bytes_per_launch = float(np.mean(ub))
+    kern_avg = float(np.mean(kern_ms))
+    achieved = bytes_per_launch / (kern_avg / 1e3) / 1e9
+    tr = traffic_for_current_kernel()
+    traffic = None
+    if tr and tr.get("workload") == w.name:
+        traffic = tr["dram_bytes_per_launch"]
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(kvp, r, w, seqs, ntoks, desc, ws, ws_bytes, flush, stream, dev,
+                  host_kv[nsteps:], host_q[nsteps:], MB)
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 K/V/Q, shapes of the workload)",
+        "config": {"workload": describe(w), "name": w.name, "sequences": S,
+                   "tokens_per_step": S * w.step_tokens, "use_sharing": not a.no_sharing,
+                   "l2": "flushed between timed steps (write of 2x L2), outside the timed region",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "attn_item_kernel", "algorithmic_bytes_per_launch": bytes_per_launch,
+                     "kernel_ms": kern_avg, "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
+        "step_hbm": {"unique_kv_gb_per_s": bytes_per_launch / (total_ms / K / 1e3) / 1e9,
+                     "frac_of_peak": bytes_per_launch / (total_ms / K / 1e3) / 1e9 / peak},
+        "plan": stats,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    return res, w
+
+
+def run_e2e(kvp, r, w, seqs, ntoks, desc, ws, ws_bytes, flush, stream, dev, host_kv,
+            host_q, MB):
+    """Same step through the public API from pinned host buffers: H2D of the
+    step's K, V and Q, append, plan (whose upload carries the block ids),
+    attention, D2H of out and lse, synchronise.  Wall clock per step."""
+    import torch
+    s = w.shapes
+    S = len(seqs)
+    n = len(host_kv)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hk = [pin(k) for k, _ in host_kv]
+    hv = [pin(v) for _, v in host_kv]
+    hq = [pin(q) for q in host_q]
+    kd = torch.empty_like(hk[0], device=dev)
+    vd = torch.empty_like(hv[0], device=dev)
+    qd = torch.empty_like(hq[0], device=dev)
+    out = torch.empty((s.L, S, s.Hq, s.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((s.L, S, s.Hq), dtype=torch.float32, device=dev)
+    ho = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    hl_ = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    times = []
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        kd.copy_(hk[i], non_blocking=True)
+        vd.copy_(hv[i], non_blocking=True)
+        qd.copy_(hq[i], non_blocking=True)
+        kvp.seq_append_batch(r.pool, seqs, ntoks, kd, vd, stream=stream)
+        ht, hl = kvp.kvp_gather_tables(r.pool, seqs, MB)
+        kvp.paged_decode_attention(qd, r.k_pool, r.v_pool, ht, hl, desc, out, lse, ws, ws_bytes,
+                                   stream=stream)
+        ho.copy_(out, non_blocking=True)
+        hl_.copy_(lse, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        times.append(time.perf_counter() - t0)
+    sec = float(np.sum(times[1:])) if n > 1 else float(times[0])
+    cnt = n - 1 if n > 1 else 1
+    h2d = hk[0].numel() * 2 * 2 + hq[0].numel() * 2
+    d2h = out.numel() * 2 + lse.numel() * 4
+    return {"value": S * w.step_tokens * cnt / sec, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": sec / cnt * 1e3,
+            "how": "wall clock per step incl. pinned H2D of k/v/q, append, host plan and its upload, "
+                   "attention, D2H of out+lse and a synchronise; first step dropped"}
+
+
+def run_verify_bench(a, w, rank, world, dev):
+    import torch
+    import paged_prefix_shared_decode_gb300 as kvp
+    from paged_prefix_shared_decode_gb300.runner import PoolRunner, VerifyCall
+
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    s = w.shapes
+
+    def kv_dev(w_, i):
+        n = w_.ops[i][2]
+        shape = (s.L, n, s.Hkv, s.d)
+        return (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16),
+                torch.randn(shape, generator=g, device=dev).to(torch.bfloat16))
+
+    r = PoolRunner(w, alloc_seed=1)
+    r.run_ops(kv_dev_fn=kv_dev)
+    call = VerifyCall(r)
+    B, n = call.B, call.n
+    q = torch.randn((s.L, B * n, s.Hq, s.d), generator=g, device=dev).to(torch.bfloat16)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    K = a.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e4 in ev:
+        for e in e4:
+            e.record(stream)
+    for i in range(a.warmup):
+        flush.fill_(i)
+        call(q, stream=stream)
+    torch.cuda.synchronize(dev)
+    clocks = Clocks(dev.index)
+    clocks.start()
+    l0 = kvp.kvp_kernel_launches()
+    for j in range(K):
+        flush.fill_(j)
+        ev[j][0].record(stream)
+        kvp.kvp_set_kernel_events(ev[j][2], ev[j][3])
+        call(q, stream=stream)
+        kvp.kvp_set_kernel_events(None, None)
+        ev[j][1].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = kvp.kvp_kernel_launches() - l0
+    clk = clocks.stop()
+    step_ms = [ev[j][0].elapsed_time(ev[j][1]) for j in range(K)]
+    kern_ms = float(np.mean([ev[j][2].elapsed_time(ev[j][3]) for j in range(K)]))
+    total = float(sum(step_ms))
+    ub = sum((int(c) + n) for c in call.ctx) * s.token_bytes * s.L
+    flops = 0
+    for b in range(B):
+        par = w.info["parents"][b]
+        depth = np.zeros(n, int)
+        for i in range(n):
+            depth[i] = 1 if par[i] < 0 else depth[par[i]] + 1
+        flops += 4 * s.d * s.Hq * s.L * int((call.ctx[b] * n + depth.sum()))
+    peak, kind = peaks()
+    achieved = ub / (kern_ms / 1e3) / 1e9
+    try:
+        mp = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        tpk = float(mp["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        tpk = 1900.0
+    res = {
+        "metric": METRIC, "value": B * n * K / (total / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": a.warmup, "ms_per_step": total / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (device-generated N(0,1) bf16 K/V/Q)",
+        "config": {"workload": describe(w), "name": w.name, "query_tokens_per_step": B * n,
+                   "l2": "flushed between timed steps, outside the timed region"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "attn_item_kernel",
+                     "algorithmic_bytes_per_launch": ub, "kernel_ms": kern_ms,
+                     "tensor_tflops": flops / (kern_ms / 1e3) / 1e12, "tensor_peak_tflops": tpk,
+                     "peak_kind": f"{kind} hbm_gbs (copy)"},
+        "e2e": None, "gpu_launches": int(launches), "clocks": clk,
+    }
+    return res, w
+
+
+def run_sweep(a, dev):
+    """Short device-timed runs of the other workloads (phi sweep, MCTS, verify)."""
+    import torch
+    import paged_prefix_shared_decode_gb300 as kvp
+    from paged_prefix_shared_decode_gb300.runner import PoolRunner
+
+    out = []
+    peak, _ = peaks()
+    for name in ["trellis0.0", "trellis0.25", "trellis0.5", "trellis0.75", "trellis0.9", "mcts",
+                 "verify1", "verify8", "verify32"]:
+        sub = argparse.Namespace(**vars(a))
+        sub.steps, sub.warmup = 5, 3
+        if name.startswith("verify"):
+            res, _ = run_verify_bench(sub, workload(name, 0), 0, 1, dev)
+            out.append({"workload": name, "tokens_per_s": res["value"], "ms_per_step": res["ms_per_step"],
+                        "kernel_ms": res["roofline"]["kernel_ms"],
+                        "unique_gb_per_s": res["roofline"]["achieved"], "frac": res["roofline"]["frac"],
+                        "tensor_tflops": res["roofline"]["tensor_tflops"]})
+            continue
+        w = workload(name, 16)
+        s = w.shapes
+        g = torch.Generator(device=dev).manual_seed(1)
+
+        def kv_dev(w_, i, s=s, g=g):
+            n = w_.ops[i][2]
+            shape = (s.L, n, s.Hkv, s.d)
+            return (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16),
+                    torch.randn(shape, generator=g, device=dev).to(torch.bfloat16))
+
+        for sharing in (True, False):
+            r = PoolRunner(w, alloc_seed=1)
+            r.run_ops(kv_dev_fn=kv_dev)
+            S = len(w.batch)
+            seqs = np.array([r.ids[n] for n in w.batch], np.int32)
+            kv = torch.randn((s.L, S, s.Hkv, s.d), generator=g, device=dev).to(torch.bfloat16)
+            r.append_step(kv, kv)
+            MB = w.max_blocks_per_seq
+            ht, hl = kvp.kvp_gather_tables(r.pool, seqs, MB)
+            desc = r.attn_desc(use_sharing=sharing)
+            wsb = kvp.kvp_decode_workspace_size(desc, ht, hl)
+            ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+            q = torch.randn((s.L, S, s.Hq, s.d), generator=g, device=dev).to(torch.bfloat16)
+            o = torch.empty((s.L, S, s.Hq, s.d), dtype=torch.bfloat16, device=dev)
+            ls = torch.empty((s.L, S, s.Hq), dtype=torch.float32, device=dev)
+            l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+            flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+            stream = torch.cuda.current_stream(dev)
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(5)]
+            for e4 in ev:
+                for e in e4:
+                    e.record(stream)
+            for i in range(3):
+                kvp.paged_decode_attention(q, r.k_pool, r.v_pool, ht, hl, desc, o, ls, ws, wsb, stream=stream)
+            for j in range(5):
+                flush.fill_(j)
+                ev[j][0].record(stream)
+                kvp.kvp_set_kernel_events(ev[j][2], ev[j][3])
+                kvp.paged_decode_attention(q, r.k_pool, r.v_pool, ht, hl, desc, o, ls, ws, wsb, stream=stream)
+                kvp.kvp_set_kernel_events(None, None)
+                ev[j][1].record(stream)
+            torch.cuda.synchronize(dev)
+            ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+            kms = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]))
+            st = kvp.kvp_decode_plan_stats(desc, ht, hl)
+            shared_st = kvp.kvp_decode_plan_stats(r.attn_desc(True), ht, hl)
+            ub = shared_st["unique_kv_bytes"]
+            out.append({"workload": name, "use_sharing": sharing, "tokens_per_s": S / (ms / 1e3),
+                        "ms_per_call": ms, "kernel_ms": kms, "unique_kv_bytes": ub,
+                        "unique_gb_per_s": ub / (kms / 1e3) / 1e9, "frac": ub / (kms / 1e3) / 1e9 / peak,
+                        "items": st["items"], "partial_rows": st["partial_rows"]})
+            r.close()
+            del ws, flush
+            torch.cuda.empty_cache()
+    return out
+
+
+# -------------------------------------------------------- oracle timing
+
+def oracle_time(w, seconds: float, max_steps: int | None = None):
+    """The fp64 oracle, as it stands, on full decode steps of the workload
+    (all layers, sequences and heads) on the host cores.  Returns
+    (tokens/s, steps, cores, seconds)."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    rw = oracle.replay(w, alloc_seed=1)
+    steps = 0
+    t_total = 0.0
+    while True:
+        if w.step_tokens:
+            k, v = W.step_kv(w, steps)
+            oracle.replay_step(rw, w, k, v)
+        q = W.step_q(w, steps)
+        t, ln = rw.tables(w.batch, w.max_blocks_per_seq)
+        t0 = time.perf_counter()
+        oracle.decode_attention(q, rw.k_pool, rw.v_pool, t, ln, threads=cores)
+        t_total += time.perf_counter() - t0
+        steps += 1
+        if (max_steps is not None and steps >= max_steps) or (max_steps is None and t_total >= seconds):
+            break
+    tokens = steps * len(w.batch) * max(1, w.step_tokens)
+    return tokens / t_total, steps, cores, t_total
+
+
+def run_reference(a, rank, world):
+    if rank != 0:
+        return None
+    w = workload(a.workload, a.warmup + a.steps + 2)
+    if w.name.startswith("verify"):
+        print(json.dumps({"impl": "reference", "unavailable": "oracle arm times decode workloads only"}))
+        return None
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    rw = oracle.replay(w, alloc_seed=1)
+    times = []
+    for i in range(a.warmup + a.steps):
+        if w.step_tokens:
+            k, v = W.step_kv(w, i)
+            oracle.replay_step(rw, w, k, v)
+        q = W.step_q(w, i)
+        t, ln = rw.tables(w.batch, w.max_blocks_per_seq)
+        t0 = time.perf_counter()
+        oracle.decode_attention(q, rw.k_pool, rw.v_pool, t, ln, threads=cores)
+        if i >= a.warmup:
+            times.append(time.perf_counter() - t0)
+    total = float(np.sum(times))
+    S = len(w.batch)
+    value = S * max(1, w.step_tokens) * a.steps / total
+    sample = (f"each step: one full decode step of the workload ({w.shapes.L} layers x {S} sequences x "
+              f"{w.shapes.Hq} heads) by the fp64 oracle")
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+           "steps": a.steps, "warmup": a.warmup, "ms_per_step": total / a.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": describe(w), "name": w.name},
+           "cpu_baseline": {"kind": "oracle", "value": value, "unit": "tokens/s", "cores": cores,
+                            "sample": sample},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return res
+
+
+def main():
+    a = parse()
+    rank, world, local = dist_env()
+    if a.impl == "reference":
+        res = run_reference(a, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+    res, w = run_ours(a, rank, world, local)
+    if rank == 0:
+        import torch
+        if a.sweep:
+            res["sweep"] = run_sweep(a, torch.device("cuda", local))
+        if not a.no_cpu_baseline and not w.name.startswith("verify"):
+            v, steps, cores, sec = oracle_time(w, a.cpu_seconds)
+            res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                   "sample": f"{steps} full decode steps of the same workload "
+                                             f"({sec:.1f} s of oracle time)"}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -16,7 +16,7 @@
  * Layouts (row-major, innermost last):
  *   K pool, V pool   [L][NB][Hkv][bs][d]  bf16   (one (block, kv head) tile is
  *                                                  a contiguous bs*d run)
- *   block tables     [S][MB] int32, entries past a sequence's blocks ignored
+ *   block tables     [S][MB] int32 (host), entries past a sequence's blocks ignored
  *   decode q, out    [L][S][Hq][d] bf16;   lse [L][S][Hq] fp32, natural log
  *   verify q, out    [L][B*n][Hq][d] bf16; lse [L][B*n][Hq] fp32
  *   appended k, v    [L][ntok][Hkv][d] bf16
@@ -43,7 +43,7 @@ enum {
 
 /* Device error word bits (kvp_device_error). */
 enum {
-    KVP_DEVERR_BLOCK_ID = 1,    /* a block table entry outside [0, NB): that tile read as 0 */
+    KVP_DEVERR_BLOCK_ID = 1,    /* a planned block id outside [0, NB): those tokens read as 0 */
     KVP_DEVERR_TREE_PARENT = 2  /* a parent pointer not in [-1, i): treated as a root       */
 };
 
@@ -142,68 +142,74 @@ typedef struct {
     int32_t num_q_heads;   /* Hq */
     int32_t num_kv_heads;  /* Hkv; Hq % Hkv == 0 and Hq / Hkv <= 64 */
     int32_t head_dim;      /* d: 64 or 128 */
-    int32_t block_size;    /* bs */
-    int32_t num_blocks;    /* NB: table entries outside [0, NB) are reported, not read */
+    int32_t block_size;    /* bs: a power of two >= 16 */
+    int32_t num_blocks;    /* NB */
     float scale;           /* softmax scale; <= 0 selects 1/sqrt(d) */
-    int32_t use_sharing;   /* 1: blocks shared by several sequences are read once per
-                              row tile (cascade); 0: every sequence reads its own
-                              blocks (the unshared baseline) */
+    int32_t use_sharing;   /* 1: blocks that several sequences share are read once per
+                              tile of up to 64 query rows (cascade); 0: every sequence
+                              reads its own blocks (the unshared baseline) */
 } kvp_attn_desc;
 
 /* Device workspace bytes that paged_decode_attention needs for this batch
- * (host tables and lengths as for the call).  Returns 0 on invalid input. */
-size_t kvp_decode_workspace_size(const kvp_attn_desc *desc, const int32_t *h_block_tables,
-                                 const int32_t *h_seq_lens, int32_t num_seqs, int32_t max_blocks);
+ * (same host tables and lengths as the call).  Returns 0 on invalid input. */
+size_t kvp_decode_workspace_size(const kvp_attn_desc *desc, const int32_t *block_tables,
+                                 const int32_t *seq_lens, int32_t num_seqs, int32_t max_blocks);
 
 /*
  * Decode attention over the paged pool: for each layer, sequence s and query
- * head h, out = softmax(q k^T * scale) v over the first h_seq_lens[s] tokens
- * of sequence s, and lse = the natural-log log-sum-exp of the scaled scores.
+ * head h, out = softmax(q k^T * scale) v over the first seq_lens[s] tokens of
+ * sequence s, and lse = the natural-log log-sum-exp of the scaled scores.
  * (Decode is one new token attending to the cached keys and values: "SGLang
- * RadixAttention", section on the KV-cache lifecycle.)  The call attends to
- * exactly seq_len tokens; append the new token's K/V first to include it.
+ * RadixAttention", section on the KV-cache lifecycle; the pool is the paged
+ * cache of "Dendrite", section details.)  The call attends to exactly
+ * seq_len tokens; append the new token's K/V first to include it.
  *
- * Work is planned on the host from h_block_tables / h_seq_lens (host copies of
- * block_tables, [num_seqs][max_blocks] / [num_seqs]): sequences whose tables
- * hold the same physical blocks at the same positions are grouped so that a
- * shared block is read from HBM once for the whole group (per tile of up to
- * 64 query rows) rather than once per sequence.  Long key ranges are split
- * across CTAs and merged by log-sum-exp.  The plan is copied into the
- * workspace with an asynchronous copy from host memory; the host arrays may be
- * reused when the call returns.
+ * block_tables [num_seqs][max_blocks] and seq_lens [num_seqs] are HOST arrays
+ * (kvp_gather_tables gives them for pool sequences).  The call plans on the
+ * host: sequences whose tables hold the same physical blocks at the same
+ * positions are grouped so that a shared block is read from HBM once per
+ * group of up to 64 query rows instead of once per sequence; long key ranges
+ * are split across CTAs and merged by log-sum-exp.  The plan, which carries
+ * the physical block ids, is copied into the workspace with an asynchronous
+ * copy from host memory on `stream`; no device block table is read, and the
+ * host arrays may be reused as soon as the call returns.
  *
- * q: device [L][num_seqs][Hq][d]; k_pool / v_pool: device pools; block_tables:
- * device [num_seqs][max_blocks]; out: device [L][num_seqs][Hq][d]; lse: device
- * [L][num_seqs][Hq] or NULL.  workspace: device, ws_bytes >=
- * kvp_decode_workspace_size(), 256-byte aligned.  Errors: KVP_ERR_INVALID for
- * an empty sequence, a table entry outside [0, NB) in the host copy, a
- * too-small workspace or unsupported shapes.
+ * q: device [L][num_seqs][Hq][d] bf16; k_pool / v_pool: the pool's device
+ * storage; out: device [L][num_seqs][Hq][d] bf16; lse: device
+ * [L][num_seqs][Hq] fp32 or NULL.  workspace: device, 256-byte aligned,
+ * ws_bytes >= kvp_decode_workspace_size(); one call at a time per workspace.
+ * Errors: KVP_ERR_INVALID for an empty sequence, a table entry outside
+ * [0, NB), a too-small or misaligned workspace, misaligned tensors or
+ * unsupported shapes; KVP_ERR_CUDA if a launch fails.
  */
 int paged_decode_attention(const void *q, const void *k_pool, const void *v_pool,
-                           const int32_t *block_tables, const int32_t *h_block_tables,
-                           const int32_t *h_seq_lens, int32_t num_seqs, int32_t max_blocks,
-                           const kvp_attn_desc *desc, void *out, float *lse, void *workspace,
-                           size_t ws_bytes, void *stream);
+                           const int32_t *block_tables, const int32_t *seq_lens, int32_t num_seqs,
+                           int32_t max_blocks, const kvp_attn_desc *desc, void *out, float *lse,
+                           void *workspace, size_t ws_bytes, void *stream);
 
-size_t kvp_verify_workspace_size(const kvp_attn_desc *desc, const int32_t *h_ctx_lens,
-                                 int32_t batch, int32_t n_draft);
+size_t kvp_verify_workspace_size(const kvp_attn_desc *desc, const int32_t *block_tables,
+                                 const int32_t *ctx_lens, int32_t batch, int32_t n_draft,
+                                 int32_t max_blocks);
 
 /*
  * Speculative tree-verify attention ("Inference-Cost-Aware Dynamic Tree
- * Construction (CAST)", technical summary sections 1-2: the target model
- * checks a dynamic draft tree of candidate tokens, EAGLE-2/3 style, in one
- * forward pass).  Sequence b has h_ctx_lens[b] context tokens followed, in
- * its pages, by n_draft <= 64 draft tokens.  Draft node i (query row b*n + i)
- * attends to every context token and to the draft tokens of its ancestors and
- * itself, anc*(i) = {i, parent(i), parent(parent(i)), ...}.
- * tree_parent: device [batch][n_draft] int32, parent < i or -1 for a root (a
- * forest is allowed).  Other arguments as for paged_decode_attention with
- * num_seqs = batch.  A bad parent pointer sets KVP_DEVERR_TREE_PARENT in the
- * workspace error word and that node is treated as a root.
+ * Construction for Efficient Inference in Large Language Models" (CAST),
+ * technical summary sections 1-2: the target model checks a dynamic draft
+ * tree of candidate tokens, EAGLE-2/3 style, in one forward pass).
+ * Sequence b has ctx_lens[b] context tokens followed, in its pages, by
+ * n_draft <= 64 draft tokens.  Draft node i (query row b*n_draft + i) attends
+ * to every context token and to the draft tokens of its ancestors and itself,
+ * anc*(i) = {i, parent(i), parent(parent(i)), ...}.
+ * tree_parent: DEVICE [batch][n_draft] int32, parent < i or -1 for a root
+ * (a forest is allowed).  block_tables / ctx_lens: HOST [batch][max_blocks] /
+ * [batch].  Other arguments as for paged_decode_attention with
+ * num_seqs = batch * n_draft query rows.  A bad parent pointer sets
+ * KVP_DEVERR_TREE_PARENT in the workspace error word and that node is
+ * treated as a root.
  */
 int tree_verify_attention(const void *q, const int32_t *tree_parent, int32_t n_draft,
                           const void *k_pool, const void *v_pool, const int32_t *block_tables,
-                          const int32_t *h_ctx_lens, int32_t batch, int32_t max_blocks,
+                          const int32_t *ctx_lens, int32_t batch, int32_t max_blocks,
                           const kvp_attn_desc *desc, void *out, float *lse, void *workspace,
                           size_t ws_bytes, void *stream);
 
@@ -212,13 +218,23 @@ int tree_verify_attention(const void *q, const int32_t *tree_parent, int32_t n_d
 int kvp_device_error(void *workspace, void *stream, int32_t *err_out);
 
 /* Host-side view of the decode plan (no device work; for tests and tools):
- * number of work items, query-row tiles, 64-token KV tiles and partial rows
- * per (layer, kv head), and the HBM bytes of distinct blocks one call reads,
- * for an SM count `sm_count`.  Any out-pointer may be NULL. */
-int kvp_decode_plan_stats(const kvp_attn_desc *desc, const int32_t *h_block_tables,
-                          const int32_t *h_seq_lens, int32_t num_seqs, int32_t max_blocks,
+ * work items, row tiles, 64-token KV tiles and partial rows per (layer, kv
+ * head), and the bytes of distinct (block, valid tokens) one call reads over
+ * all layers, planned for a GPU with sm_count SMs.  Any out-pointer may be
+ * NULL. */
+int kvp_decode_plan_stats(const kvp_attn_desc *desc, const int32_t *block_tables,
+                          const int32_t *seq_lens, int32_t num_seqs, int32_t max_blocks,
                           int32_t sm_count, int32_t *n_items, int32_t *n_row_tiles,
                           int32_t *n_kv_tiles, int32_t *n_partial_rows, int64_t *unique_kv_bytes);
+
+/* Measurement hooks.  kvp_set_kernel_events: cudaEvent_t handles (as void*)
+ * that every later attention call on this thread records on its stream
+ * immediately before and after its main attention kernel (the work-item
+ * kernel), so a caller can time that kernel alone; NULL, NULL turns it off.
+ * kvp_kernel_launches: total kernels this library has launched in the
+ * process (all threads). */
+int kvp_set_kernel_events(void *before, void *after);
+int kvp_kernel_launches(int64_t *n_out);
 
 const char *kvp_strerror(int code);
 

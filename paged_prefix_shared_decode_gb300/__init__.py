@@ -22,6 +22,7 @@ __all__ = [
     "kvp_free_block_count", "kvp_cow_count", "kvp_gather_tables", "kvp_export_tables",
     "kvp_decode_workspace_size", "paged_decode_attention", "kvp_verify_workspace_size",
     "tree_verify_attention", "kvp_device_error", "kvp_decode_plan_stats", "kvp_strerror",
+    "kvp_set_kernel_events", "kvp_kernel_launches",
     "KVP_OK", "KVP_ERR_INVALID", "KVP_ERR_OOM", "KVP_ERR_STATE", "KVP_ERR_CUDA", "KVP_ERR_DEVICE",
 ]
 
@@ -82,15 +83,17 @@ _SIGS = {
     "kvp_gather_tables": ([_P, _P, _I32, _I32, _P, _P], ctypes.c_int),
     "kvp_export_tables": ([_P, _P, _I32, _I32, _P, _P, _P], ctypes.c_int),
     "kvp_decode_workspace_size": ([ctypes.POINTER(AttnDesc), _P, _P, _I32, _I32], ctypes.c_size_t),
-    "paged_decode_attention": ([_P, _P, _P, _P, _P, _P, _I32, _I32, ctypes.POINTER(AttnDesc),
+    "paged_decode_attention": ([_P, _P, _P, _P, _P, _I32, _I32, ctypes.POINTER(AttnDesc),
                                 _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
-    "kvp_verify_workspace_size": ([ctypes.POINTER(AttnDesc), _P, _I32, _I32], ctypes.c_size_t),
+    "kvp_verify_workspace_size": ([ctypes.POINTER(AttnDesc), _P, _P, _I32, _I32, _I32], ctypes.c_size_t),
     "tree_verify_attention": ([_P, _P, _I32, _P, _P, _P, _P, _I32, _I32, ctypes.POINTER(AttnDesc),
                                _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "kvp_device_error": ([_P, _P, _I32P], ctypes.c_int),
     "kvp_decode_plan_stats": ([ctypes.POINTER(AttnDesc), _P, _P, _I32, _I32, _I32, _I32P, _I32P,
                                _I32P, _I32P, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
     "kvp_strerror": ([ctypes.c_int], ctypes.c_char_p),
+    "kvp_set_kernel_events": ([_P, _P], ctypes.c_int),
+    "kvp_kernel_launches": ([ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
 }
 
 
@@ -250,35 +253,40 @@ def kvp_decode_workspace_size(desc: AttnDesc, h_tables, h_lens) -> int:
     return n
 
 
-def paged_decode_attention(q, k_pool, v_pool, block_tables, h_tables, h_lens, desc: AttnDesc,
-                           out, lse, workspace, ws_bytes=None, stream=None):
-    t, tp = _host_i32(h_tables)
-    ln, lp = _host_i32(h_lens)
+def _ws_bytes(workspace, ws_bytes):
     if ws_bytes is None:
         ws_bytes = workspace.numel() * workspace.element_size()
-    _check(load().paged_decode_attention(_dev(q), _dev(k_pool), _dev(v_pool), _dev(block_tables), tp, lp,
-                                         t.shape[0], t.shape[1], ctypes.byref(desc), _dev(out),
-                                         _dev(lse), _dev(workspace), ws_bytes, _stream(stream)),
-           "paged_decode_attention")
+    return ws_bytes
 
 
-def kvp_verify_workspace_size(desc: AttnDesc, h_ctx_lens, n_draft: int) -> int:
-    c, cp = _host_i32(h_ctx_lens)
-    n = load().kvp_verify_workspace_size(ctypes.byref(desc), cp, len(c), n_draft)
+def paged_decode_attention(q, k_pool, v_pool, block_tables, seq_lens, desc: AttnDesc, out, lse,
+                           workspace, ws_bytes=None, stream=None):
+    """block_tables [S][MB] / seq_lens [S]: host int32 arrays."""
+    t, tp = _host_i32(block_tables)
+    ln, lp = _host_i32(seq_lens)
+    _check(load().paged_decode_attention(_dev(q), _dev(k_pool), _dev(v_pool), tp, lp, t.shape[0],
+                                         t.shape[1], ctypes.byref(desc), _dev(out), _dev(lse),
+                                         _dev(workspace), _ws_bytes(workspace, ws_bytes),
+                                         _stream(stream)), "paged_decode_attention")
+
+
+def kvp_verify_workspace_size(desc: AttnDesc, block_tables, ctx_lens, n_draft: int) -> int:
+    t, tp = _host_i32(block_tables)
+    c, cp = _host_i32(ctx_lens)
+    n = load().kvp_verify_workspace_size(ctypes.byref(desc), tp, cp, len(c), n_draft, t.shape[1])
     if n == 0:
         raise KvpError(KVP_ERR_INVALID, "kvp_verify_workspace_size")
     return n
 
 
-def tree_verify_attention(q, tree_parent, n_draft: int, k_pool, v_pool, block_tables, h_ctx_lens,
-                          max_blocks: int, desc: AttnDesc, out, lse, workspace, ws_bytes=None,
-                          stream=None):
-    c, cp = _host_i32(h_ctx_lens)
-    if ws_bytes is None:
-        ws_bytes = workspace.numel() * workspace.element_size()
+def tree_verify_attention(q, tree_parent, n_draft: int, k_pool, v_pool, block_tables, ctx_lens,
+                          desc: AttnDesc, out, lse, workspace, ws_bytes=None, stream=None):
+    """tree_parent: device int32 [B][n]; block_tables [B][MB] / ctx_lens [B]: host."""
+    t, tp = _host_i32(block_tables)
+    c, cp = _host_i32(ctx_lens)
     _check(load().tree_verify_attention(_dev(q), _dev(tree_parent), n_draft, _dev(k_pool), _dev(v_pool),
-                                        _dev(block_tables), cp, len(c), max_blocks, ctypes.byref(desc),
-                                        _dev(out), _dev(lse), _dev(workspace), ws_bytes,
+                                        tp, cp, len(c), t.shape[1], ctypes.byref(desc), _dev(out),
+                                        _dev(lse), _dev(workspace), _ws_bytes(workspace, ws_bytes),
                                         _stream(stream)), "tree_verify_attention")
 
 
@@ -298,6 +306,21 @@ def kvp_decode_plan_stats(desc: AttnDesc, h_tables, h_lens, sm_count: int = 152)
            "kvp_decode_plan_stats")
     return dict(items=vals[0].value, row_tiles=vals[1].value, kv_tiles=vals[2].value,
                 partial_rows=vals[3].value, unique_kv_bytes=ub.value)
+
+
+def kvp_set_kernel_events(before=None, after=None):
+    """before/after: torch.cuda.Event (recorded once already) or raw handles."""
+    def h(e):
+        if e is None:
+            return None
+        return e if isinstance(e, int) else e.cuda_event
+    _check(load().kvp_set_kernel_events(h(before), h(after)), "kvp_set_kernel_events")
+
+
+def kvp_kernel_launches() -> int:
+    n = ctypes.c_int64()
+    _check(load().kvp_kernel_launches(ctypes.byref(n)), "kvp_kernel_launches")
+    return n.value
 
 
 def kvp_strerror(code: int) -> str:

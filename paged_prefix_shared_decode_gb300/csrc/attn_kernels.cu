@@ -1,20 +1,23 @@
 // Paged attention work-item kernel and log-sum-exp merge (sm_103a).
 //
-// One CTA (4 warps) runs one work item for one (layer, kv head): up to 64
-// query rows (sequences or draft nodes x the GQA group sharing this kv head)
-// against a list of 64-token KV tiles gathered through the block tables.
-// Each KV tile is staged once in shared memory (cp.async, 16-byte chunks,
-// XOR-swizzled rows, a 3-4 deep ring) and used by every row of the item; this
-// is how a block shared by several sequences is read once for all of them.
+// A persistent grid (one to three CTAs of 4 warps per SM) pulls work units --
+// (work item, layer, kv head) -- from an atomic counter, longest first.  A
+// unit is up to 64 query rows (sequences or draft nodes x the GQA group that
+// shares this kv head) against a list of 64-token KV tiles.  The tiles'
+// descriptors, which carry the physical block ids, are staged in shared
+// memory first; then each tile's K and V are copied into a 3-4 deep shared
+// memory ring (cp.async, 16-byte chunks, XOR-swizzled rows) and used by every
+// row of the unit.  This is how a block shared by several sequences is read
+// from HBM once for all of them.
 // Q K^T and P V run on bf16 tensor cores (mma.sync m16n8k16, fp32
 // accumulate) with an online softmax in fp32 (base-2 exponent, scale * log2 e
 // folded into the scores).  Rows outside a tile's member interval, tokens past
 // the tile's end and draft tokens that are not ancestors-or-self of a node
-// are masked.  With fewer than 32 rows the item's warps split each tile's
-// tokens and combine their (m, l, o) through shared memory at the end.
+// are masked.  With at most 16 (32) rows the four warps split each tile's
+// tokens four (two) ways and combine their (m, l, o) through shared memory.
 //
-// The item writes out (bf16) and lse (fp32, natural log) directly, or -- when
-// its rows' keys are split over several items -- normalised partial o and a
+// A unit writes out (bf16) and lse (fp32, natural log) directly, or -- when
+// its rows' keys are split over several units -- normalised partial o and a
 // base-2 lse per row, which merge_kernel combines:
 //   out = sum_c w_c o_c / sum_c w_c,  w_c = 2^(lse_c - max lse),
 //   lse = max lse + log2(sum w)   (converted to natural log).
@@ -22,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "kvp_internal.h"
 
@@ -88,7 +92,7 @@ __device__ uint64_t ancestor_mask(const int32_t *parent, int b, int i, int n, in
     int j = i;
     for (int step = 0; step < 64 && j >= 0; ++step) {
         m |= 1ull << j;
-        int p = __ldg(parent + (size_t)b * n + j);
+        const int p = __ldg(parent + (size_t)b * n + j);
         if (p >= j || p < -1) {
             atomicOr(err, 2);
             break;
@@ -98,29 +102,26 @@ __device__ uint64_t ancestor_mask(const int32_t *parent, int b, int i, int n, in
     return m;
 }
 
-template <int D, int TS>
-struct Cfg {
-    static constexpr int CH = D / 8;                       // 16-byte chunks per token row
+template <int D>
+struct KCfg {
+    static constexpr int CH = D / 8;                        // 16-byte chunks per token row
     static constexpr int TILE_BYTES = kTileTokens * D * 2;  // one K (or V) tile
     static constexpr int NSTAGE = D == 64 ? 4 : 3;
-    static constexpr int SMEM = NSTAGE * 2 * TILE_BYTES;
-    static constexpr int TOKW = kTileTokens / TS;  // tokens per warp per tile
-    static constexpr int NT = TOKW / 8;            // score n-tiles per warp
-    static constexpr int KS = D / 16;              // k-steps of Q K^T
-    static constexpr int NO = D / 8;               // n-tiles of O
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int DESC_OFF = NSTAGE * STAGE_BYTES;
+    static constexpr int SMEM = DESC_OFF + kMaxItemTiles * (int)sizeof(KvTile);
+    static constexpr int MIN_BLOCKS = D == 64 ? 3 : 2;
+    static constexpr int NO = D / 8;    // n-tiles of O
+    static constexpr int KS = D / 16;   // k-steps of Q K^T
 };
 
+// One work unit with TS warps splitting each tile's tokens.
 template <int D, int TS>
-__global__ void __launch_bounds__(kThreads) attn_item_kernel(const AttnLaunch a) {
-    using C = Cfg<D, TS>;
-    extern __shared__ __align__(128) unsigned char smem[];
-
-    int bid = blockIdx.x;
-    const int item_idx = bid % a.n_items;
-    bid /= a.n_items;
-    const int kvh = bid % a.Hkv;
-    const int l = bid / a.Hkv;
-    const WorkItem it = a.items[item_idx];
+__device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it, int l, int kvh,
+                                         int ntile, unsigned char *smem, const KvTile *s_tiles) {
+    using C = KCfg<D>;
+    constexpr int TOKW = kTileTokens / TS;   // tokens per warp per tile
+    constexpr int NT = TOKW / 8;             // score n-tiles per warp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rg = warp / TS, sp = warp % TS;
     const int G = a.G;
@@ -137,13 +138,57 @@ __global__ void __launch_bounds__(kThreads) attn_item_kernel(const AttnLaunch a)
     int qt0 = 0, qt1 = 0;
     const __nv_bfloat16 *q0 = nullptr, *q1 = nullptr;
     if (has0) {
-        qt0 = a.members[it.member_off + mem0];
+        qt0 = __ldg(a.members + it.member_off + mem0);
         q0 = qb + (((size_t)l * a.nq + qt0) * a.Hq + kvh * G + row0 % G) * D;
     }
     if (has1) {
-        qt1 = a.members[it.member_off + mem1];
+        qt1 = __ldg(a.members + it.member_off + mem1);
         q1 = qb + (((size_t)l * a.nq + qt1) * a.Hq + kvh * G + row1 % G) * D;
     }
+
+    const int bs_log2 = a.bs_log2;
+    const int bs_mask = (1 << bs_log2) - 1;
+    const size_t head_stride = (size_t)D << bs_log2;            // one (block, head) tile
+    const size_t layer_base = (size_t)l * a.NB * a.Hkv * head_stride + (size_t)kvh * head_stride;
+    const size_t block_stride = (size_t)a.Hkv * head_stride;
+
+    auto issue = [&](int t) {
+        const KvTile &kt = s_tiles[t];
+        const int ntok = kt.ntok_flags & 0xFFFF;
+        const int jb = kt.tok0 >> bs_log2;
+        const uint32_t dK = smem_addr(smem + (t % C::NSTAGE) * C::STAGE_BYTES);
+        const uint32_t dV = dK + C::TILE_BYTES;
+#pragma unroll
+        for (int i = 0; i < kTileTokens * C::CH / kThreads; ++i) {
+            const int x = threadIdx.x + i * kThreads;
+            const int tok = x / C::CH, c = x % C::CH;
+            const uint32_t off = tok * D * 2 + ((c ^ (tok & 7)) << 4);
+            const __nv_bfloat16 *sk = kpool, *sv = vpool;
+            int bytes = 0;
+            if (tok < ntok) {
+                const int pos = kt.tok0 + tok;
+                const int blk = kt.blk[(pos >> bs_log2) - jb];
+                if ((unsigned)blk < (unsigned)a.NB) {
+                    const size_t e = layer_base + (size_t)blk * block_stride +
+                                     (size_t)(pos & bs_mask) * D + c * 8;
+                    sk = kpool + e;
+                    sv = vpool + e;
+                    bytes = 16;
+                } else if (c == 0) {
+                    atomicOr(a.err, 1);
+                }
+            }
+            cp_async16(dK + off, sk, bytes);
+            cp_async16(dV + off, sv, bytes);
+        }
+    };
+
+#pragma unroll
+    for (int t = 0; t < C::NSTAGE - 1; ++t) {
+        if (t < ntile) issue(t);
+        cp_async_commit();
+    }
+
     uint32_t qf[C::KS][4];
 #pragma unroll
     for (int kk = 0; kk < C::KS; ++kk) {
@@ -164,71 +209,31 @@ __global__ void __launch_bounds__(kThreads) attn_item_kernel(const AttnLaunch a)
     for (int n = 0; n < C::NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    const int ntile = it.tile_end - it.tile_begin;
-    const size_t head_stride = (size_t)a.bs * D;
-
-    auto issue = [&](int t) {
-        const KvTile kt = a.tiles[it.tile_begin + t];
-        const int ntok = kt.ntok_flags & 0xFFFF;
-        unsigned char *sK = smem + (t % C::NSTAGE) * 2 * C::TILE_BYTES;
-        const uint32_t dK = smem_addr(sK), dV = dK + C::TILE_BYTES;
-        const int32_t *trow = a.tables + (size_t)kt.row * a.MB;
-#pragma unroll
-        for (int i = 0; i < kTileTokens * C::CH / kThreads; ++i) {
-            const int x = threadIdx.x + i * kThreads;
-            const int tok = x / C::CH, c = x % C::CH;
-            const uint32_t off = tok * D * 2 + ((c ^ (tok & 7)) << 4);
-            const __nv_bfloat16 *sk = kpool, *sv = vpool;
-            int bytes = 0;
-            if (tok < ntok) {
-                const int pos = kt.tok0 + tok;
-                const int blk = __ldg(trow + pos / a.bs);
-                if ((unsigned)blk < (unsigned)a.NB) {
-                    const size_t e = (((size_t)l * a.NB + blk) * a.Hkv + kvh) * head_stride +
-                                     (size_t)(pos % a.bs) * D + c * 8;
-                    sk = kpool + e;
-                    sv = vpool + e;
-                    bytes = 16;
-                } else if (c == 0) {
-                    atomicOr(a.err, 1);
-                }
-            }
-            cp_async16(dK + off, sk, bytes);
-            cp_async16(dV + off, sv, bytes);
-        }
-    };
-
-#pragma unroll
-    for (int t = 0; t < C::NSTAGE - 1; ++t) {
-        if (t < ntile) issue(t);
-        cp_async_commit();
-    }
-
     for (int t = 0; t < ntile; ++t) {
         cp_async_wait<C::NSTAGE - 2>();
         __syncthreads();
         if (t + C::NSTAGE - 1 < ntile) issue(t + C::NSTAGE - 1);
         cp_async_commit();
 
-        const KvTile kt = a.tiles[it.tile_begin + t];
+        const KvTile &kt = s_tiles[t];
         const int ntok = kt.ntok_flags & 0xFFFF;
         const bool tree = (kt.ntok_flags >> 16) & kTileTree;
         const int mlo = kt.members & 0xFFFF, mhi = kt.members >> 16;
         const bool in0 = has0 && mem0 >= mlo && mem0 < mhi;
         const bool in1 = has1 && mem1 >= mlo && mem1 < mhi;
-        const int tb = sp * C::TOKW;
+        const int tb = sp * TOKW;
         if (!__any_sync(0xffffffffu, in0 || in1) || tb >= ntok) continue;
 
-        const unsigned char *sK = smem + (t % C::NSTAGE) * 2 * C::TILE_BYTES;
-        const uint32_t aK = smem_addr(sK), aV = aK + C::TILE_BYTES;
+        const uint32_t aK = smem_addr(smem + (t % C::NSTAGE) * C::STAGE_BYTES);
+        const uint32_t aV = aK + C::TILE_BYTES;
 
-        float s[C::NT][4];
+        float s[NT][4];
 #pragma unroll
-        for (int j = 0; j < C::NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+        for (int j = 0; j < NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < C::KS; ++kk) {
 #pragma unroll
-            for (int j2 = 0; j2 < C::NT / 2; ++j2) {
+            for (int j2 = 0; j2 < NT / 2; ++j2) {
                 const int tok = tb + j2 * 16 + (lane & 7) + ((lane >> 4) << 3);
                 const int ch = kk * 2 + ((lane >> 3) & 1);
                 uint32_t b0, b1, b2, b3;
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(kThreads) attn_item_kernel(const AttnLaunch a)
         }
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < C::NT; ++j) {
+        for (int j = 0; j < NT; ++j) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int tok = tb + j * 8 + 2 * tq + (e & 1);
@@ -264,7 +269,7 @@ __global__ void __launch_bounds__(kThreads) attn_item_kernel(const AttnLaunch a)
         m1 = mn1;
         float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-        for (int j = 0; j < C::NT; ++j) {
+        for (int j = 0; j < NT; ++j) {
             s[j][0] = exp2_sfu(s[j][0] - b0);
             s[j][1] = exp2_sfu(s[j][1] - b0);
             s[j][2] = exp2_sfu(s[j][2] - b1);
@@ -282,7 +287,7 @@ __global__ void __launch_bounds__(kThreads) attn_item_kernel(const AttnLaunch a)
             o[n][3] *= al1;
         }
 #pragma unroll
-        for (int k2 = 0; k2 < C::NT / 2; ++k2) {
+        for (int k2 = 0; k2 < NT / 2; ++k2) {
             const uint32_t pa[4] = {pack_bf16x2(s[2 * k2][0], s[2 * k2][1]),
                                     pack_bf16x2(s[2 * k2][2], s[2 * k2][3]),
                                     pack_bf16x2(s[2 * k2 + 1][0], s[2 * k2 + 1][1]),
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(kThreads) attn_item_kernel(const AttnLaunch a)
             }
         }
     }
+    cp_async_wait<0>();
 
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -306,7 +312,6 @@ __global__ void __launch_bounds__(kThreads) attn_item_kernel(const AttnLaunch a)
 
     if constexpr (TS > 1) {
         // combine the token-split warps of each row group through shared memory
-        cp_async_wait<0>();
         __syncthreads();
         float *red = reinterpret_cast<float *>(smem);
         constexpr int PER_WARP = (C::NO * 4 + 4) * 32;
@@ -392,87 +397,147 @@ __global__ void __launch_bounds__(kThreads) attn_item_kernel(const AttnLaunch a)
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) merge_kernel(const AttnLaunch a) {
-    const int qt = blockIdx.x, l = blockIdx.y;
-    const MergeDesc md = a.merge[qt];
-    if (md.n_chunks == 0) return;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int V = D / 32;   // values per lane
-    for (int h = warp; h < a.Hq; h += kThreads / 32) {
-        const int kvh = h / a.G, g = h % a.G;
-        const size_t rb = ((size_t)l * a.Hkv + kvh) * a.P + md.base + md.m_pos * a.G + g;
-        float M = -INFINITY;
-        for (int c = lane; c < md.n_chunks; c += 32) M = fmaxf(M, a.part_lse[rb + (size_t)c * md.stride]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        const float Mb = M == -INFINITY ? 0.f : M;
-        float acc[V];
-#pragma unroll
-        for (int v = 0; v < V; ++v) acc[v] = 0.f;
-        float wsum = 0.f;
-        for (int c = 0; c < md.n_chunks; ++c) {
-            const size_t pr = rb + (size_t)c * md.stride;
-            const float w = exp2_sfu(a.part_lse[pr] - Mb);
-            wsum += w;
-            const float *src = a.part_o + pr * D + lane * V;
-            if constexpr (V == 2) {
-                const float2 x = *reinterpret_cast<const float2 *>(src);
-                acc[0] += w * x.x;
-                acc[1] += w * x.y;
-            } else {
-                const float4 x = *reinterpret_cast<const float4 *>(src);
-                acc[0] += w * x.x;
-                acc[1] += w * x.y;
-                acc[2] += w * x.z;
-                acc[3] += w * x.w;
-            }
-        }
-        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
-                             (((size_t)l * a.nq + qt) * a.Hq + h) * D + lane * V;
-#pragma unroll
-        for (int v = 0; v < V; v += 2)
-            *reinterpret_cast<uint32_t *>(dst + v) = pack_bf16x2(acc[v] * inv, acc[v + 1] * inv);
-        if (a.lse && lane == 0)
-            a.lse[((size_t)l * a.nq + qt) * a.Hq + h] =
-                (wsum > 0.f ? Mb + __log2f(wsum) : -INFINITY) * 0.6931471805599453f;
+__global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kernel(const AttnLaunch a) {
+    using C = KCfg<D>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    KvTile *s_tiles = reinterpret_cast<KvTile *>(smem + C::DESC_OFF);
+    __shared__ int s_unit;
+    const int lh = a.L * a.Hkv;
+    for (;;) {
+        if (threadIdx.x == 0) s_unit = atomicAdd(a.counter, 1);
+        __syncthreads();
+        const int unit = s_unit;
+        if (unit >= a.n_units) break;
+        const int item_idx = unit / lh;
+        const int rem = unit - item_idx * lh;
+        const int kvh = rem % a.Hkv, l = rem / a.Hkv;
+        const WorkItem it = a.items[item_idx];
+        const int ntile = it.tile_end - it.tile_begin;
+        const int4 *src = reinterpret_cast<const int4 *>(a.tiles + it.tile_begin);
+        int4 *dst = reinterpret_cast<int4 *>(s_tiles);
+        for (int i = threadIdx.x; i < ntile * 2; i += kThreads) dst[i] = src[i];
+        __syncthreads();
+        const int rows = it.n_members * a.G;
+        if (rows <= 16) run_unit<D, 4>(a, it, l, kvh, ntile, smem, s_tiles);
+        else if (rows <= 32) run_unit<D, 2>(a, it, l, kvh, ntile, smem, s_tiles);
+        else run_unit<D, 1>(a, it, l, kvh, ntile, smem, s_tiles);
+        __syncthreads();
     }
 }
 
-template <int D, int TS>
-cudaError_t launch_items(const AttnLaunch &a, cudaStream_t stream) {
-    using C = Cfg<D, TS>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_item_kernel<D, TS>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
+// One warp per (layer, query token, query head); entries are independent
+// loads, unrolled four at a time.
+template <int D>
+__global__ void __launch_bounds__(kThreads) merge_kernel(const AttnLaunch a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * (kThreads / 32) + warp;
+    const int qt = gw / a.Hq, h = gw % a.Hq, l = blockIdx.y;
+    if (qt >= a.nq) return;
+    const MergeDesc md = a.merge[qt];
+    if (md.cnt == 0) return;
+    constexpr int V = D / 32;   // values per lane
+    const int kvh = h / a.G, g = h % a.G;
+    const size_t rb = ((size_t)l * a.Hkv + kvh) * a.P + g;
+    const int32_t *ent = a.entries + md.off;
+    float M = -INFINITY;
+    for (int c = lane; c < md.cnt; c += 32) M = fmaxf(M, a.part_lse[rb + __ldg(ent + c)]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float Mb = M == -INFINITY ? 0.f : M;
+    float acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    float wsum = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < md.cnt; ++c) {
+        const size_t pr = rb + __ldg(ent + c);
+        const float w = exp2_sfu(a.part_lse[pr] - Mb);
+        wsum += w;
+        const float *src = a.part_o + pr * D + lane * V;
+        if constexpr (V == 2) {
+            const float2 x = *reinterpret_cast<const float2 *>(src);
+            acc[0] += w * x.x;
+            acc[1] += w * x.y;
+        } else {
+            const float4 x = *reinterpret_cast<const float4 *>(src);
+            acc[0] += w * x.x;
+            acc[1] += w * x.y;
+            acc[2] += w * x.z;
+            acc[3] += w * x.w;
+        }
     }
-    const long long blocks = (long long)a.n_items * a.Hkv * a.L;
-    if (blocks <= 0) return cudaSuccess;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    attn_item_kernel<D, TS><<<(unsigned)blocks, kThreads, C::SMEM, stream>>>(a);
-    return cudaGetLastError();
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
+                         (((size_t)l * a.nq + qt) * a.Hq + h) * D + lane * V;
+#pragma unroll
+    for (int v = 0; v < V; v += 2)
+        *reinterpret_cast<uint32_t *>(dst + v) = pack_bf16x2(acc[v] * inv, acc[v + 1] * inv);
+    if (a.lse && lane == 0)
+        a.lse[((size_t)l * a.nq + qt) * a.Hq + h] =
+            (wsum > 0.f ? Mb + __log2f(wsum) : -INFINITY) * 0.6931471805599453f;
+}
+
+struct Occupancy {
+    int sms = 0, per_sm = 0;
+    bool ok = false;
+};
+
+template <int D>
+Occupancy &occupancy() {
+    static Occupancy occ;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        using C = KCfg<D>;
+        occ.per_sm = C::MIN_BLOCKS;
+        occ.sms = 152;
+        int dev = 0, n = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return;
+        if (cudaFuncSetAttribute(attn_item_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM) != cudaSuccess)
+            return;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) occ.sms = sms;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_item_kernel<D>, kThreads, C::SMEM) ==
+                cudaSuccess && n > 0)
+            occ.per_sm = n;
+        occ.ok = true;
+    });
+    return occ;
 }
 
 template <int D>
-cudaError_t launch_d(const AttnLaunch &a, cudaStream_t stream) {
-    cudaError_t e;
-    if (a.ts == 4) e = launch_items<D, 4>(a, stream);
-    else if (a.ts == 2) e = launch_items<D, 2>(a, stream);
-    else e = launch_items<D, 1>(a, stream);
-    if (e != cudaSuccess || a.P == 0) return e;
-    dim3 grid(a.nq, a.L);
+cudaError_t launch_d(const AttnLaunch &a, cudaStream_t stream, cudaEvent_t before, cudaEvent_t after) {
+    using C = KCfg<D>;
+    Occupancy &occ = occupancy<D>();
+    if (!occ.ok) return cudaErrorInvalidDevice;
+    if (before && cudaEventRecord(before, stream) != cudaSuccess) return cudaErrorInvalidResourceHandle;
+    cudaError_t e = launch_attention_tc(a, stream);
+    if (e != cudaSuccess) return e;
+    if (a.n_units > 0) {
+        const int grid = a.n_units < occ.sms * occ.per_sm ? a.n_units : occ.sms * occ.per_sm;
+        attn_item_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(a);
+        count_launch();
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (after && cudaEventRecord(after, stream) != cudaSuccess) return cudaErrorInvalidResourceHandle;
+    if (a.P == 0) return cudaSuccess;
+    const long long warps = (long long)a.nq * a.Hq;
+    dim3 grid((unsigned)((warps + kThreads / 32 - 1) / (kThreads / 32)), a.L);
     merge_kernel<D><<<grid, kThreads, 0, stream>>>(a);
+    count_launch();
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream) {
-    if (a.D == 64) return launch_d<64>(a, stream);
-    if (a.D == 128) return launch_d<128>(a, stream);
+int attention_ctas_per_sm(int D) {
+    return D == 64 ? occupancy<64>().per_sm : occupancy<128>().per_sm;
+}
+
+cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream, cudaEvent_t before,
+                             cudaEvent_t after) {
+    if (a.D == 64) return launch_d<64>(a, stream, before, after);
+    if (a.D == 128) return launch_d<128>(a, stream, before, after);
     return cudaErrorInvalidValue;
 }
 

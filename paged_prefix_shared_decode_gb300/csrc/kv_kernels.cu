@@ -112,6 +112,7 @@ cudaError_t launch_kv_write(const KvWrite &w, cudaStream_t stream) {
         const int64_t want = (total + 255) / 256;
         const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * 16));
         kv_write_kernel<<<blocks, 256, 0, stream>>>(a);
+        count_launch();
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         cow_done += a.ncow;

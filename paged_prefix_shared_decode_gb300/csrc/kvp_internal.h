@@ -8,23 +8,30 @@
 
 namespace kvp {
 
-// One 64-token KV tile of a work item: tokens [tok0, tok0 + ntok) of the
-// sequence in table row `row`, seen by the item's members with local index in
-// [m_lo, m_hi).  TREE: token j of the tile is visible to a draft-node row only
-// if bit j of that node's ancestor-or-self mask is set.
+constexpr int kTileTokens = 64;    // tokens per KV tile (one pipeline stage)
+constexpr int kTileBlocks = 5;     // blocks a 64-token tile can touch when bs >= 16
+constexpr int kMaxItemTiles = 128; // KV tiles per work item (descriptors staged in smem)
+constexpr int kTileTree = 1;       // tile flag: draft tokens under a tree mask
+constexpr int kMmaMaxRows = 64;    // rows of an mma.sync unit (4 warps x 16)
+constexpr int kTcRows = 128;       // rows of a tcgen05 unit (one thread per row)
+
+// One KV tile of a work item: tokens [tok0, tok0 + ntok) of one sequence,
+// whose physical blocks (in order) are blk[0..]: token t of the tile lives in
+// blk[(tok0 + t) / bs - tok0 / bs], slot (tok0 + t) % bs.  The tile is seen
+// by the item's members with local index in [m_lo, m_hi).  TREE: token t is
+// visible to draft node i only if bit t of i's ancestor-or-self mask is set.
 struct KvTile {
-    int32_t row;
     int32_t tok0;
     int32_t ntok_flags;   // ntok | flags << 16
     int32_t members;      // m_lo | m_hi << 16
+    int32_t blk[kTileBlocks];
 };
-constexpr int kTileTokens = 64;
-constexpr int kTileTree = 1;
+static_assert(sizeof(KvTile) == 32, "KvTile is 32 bytes");
 
-// A CTA's work: KV tiles [tile_begin, tile_end) for up to 64 query rows
-// (n_members sequences or draft nodes times the GQA group).  out_base < 0:
-// the item sees every key of its rows and writes out/lse directly; otherwise
-// it writes partial rows out_base + m * G + g for the merge kernel.
+// A work item: KV tiles [tile_begin, tile_end) against the query rows of
+// n_members members (decode sequences or draft nodes) x the GQA group.
+// out_base < 0: the item covers every key of its rows and writes out / lse;
+// otherwise row r goes to partial row out_base + r.
 struct WorkItem {
     int32_t tile_begin, tile_end;
     int32_t member_off, n_members;
@@ -32,38 +39,27 @@ struct WorkItem {
     int32_t pad[3];
 };
 
-// Per query token: partial rows base + c * stride + m_pos * G + g for chunks
-// c < n_chunks; n_chunks == 0 means the query was written directly.
+// Per query token: merge entries[off .. off + cnt) are partial-row bases
+// (add the head's index within its group); cnt == 0 means written directly.
 struct MergeDesc {
-    int32_t base, stride, n_chunks, m_pos;
+    int32_t off, cnt;
 };
 
-// Layout of the workspace: [header | items | tiles | members | merge | partials].
+// Workspace: [header | items | tiles | members | merge | entries | partials].
 struct WsHeader {
-    int32_t err;
-    int32_t n_items, n_tiles, n_members, n_merge, n_partial_rows;
-    int32_t pad[58];
+    int32_t err;         // KVP_DEVERR_* bits
+    int32_t counter;     // next work unit of the mma.sync kernel
+    int32_t tc_counter;  // next work unit of the tcgen05 kernel
+    int32_t n_items, n_tc_items, n_units, n_tiles, n_members, n_entries, n_partial_rows;
+    int32_t pad[54];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
-
-struct Plan {
-    int32_t n_items = 0, n_row_tiles = 0, n_partial_rows = 0, n_merge_q = 0;
-    int32_t ts = 1;               // warps that split one tile's tokens (1, 2, 4)
-    int64_t unique_kv_bytes = 0;  // distinct (block, valid tokens) bytes, all layers
-    // host images of the uploaded arrays
-    WorkItem *items = nullptr;
-    KvTile *tiles = nullptr;
-    int32_t *members = nullptr;
-    MergeDesc *merge = nullptr;
-    int32_t n_tiles = 0, n_members = 0, n_merge = 0;
-};
 
 struct AttnLaunch {
     const void *q;
     const void *k_pool;
     const void *v_pool;
-    const int32_t *tables;
-    int32_t MB, NB, bs, Hq, Hkv, G, nq, L, D;
+    int32_t NB, bs_log2, Hq, Hkv, G, nq, L, D;
     float scale_log2;
     const int32_t *tree_parent;   // null for decode
     int32_t n_draft;
@@ -71,16 +67,32 @@ struct AttnLaunch {
     float *lse;
     // workspace views
     int32_t *err;
-    const WorkItem *items;
+    int32_t *counter;
+    int32_t *tc_counter;
+    const WorkItem *items;      // mma.sync items (at most 32 query rows)
+    const WorkItem *tc_items;   // tcgen05 items (up to 128 query rows)
     const KvTile *tiles;
     const int32_t *members;
     const MergeDesc *merge;
+    const int32_t *entries;
     float *part_o;
     float *part_lse;
-    int32_t n_items, n_merge_q, P, ts;
+    int32_t n_units, n_tc_units, n_merge_q, P;
 };
 
-cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream);
+// before/after: optional events recorded around the work-item kernel.
+cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream, cudaEvent_t before,
+                             cudaEvent_t after);
+// tcgen05 kernel over a.tc_items (no-op when there are none).
+cudaError_t launch_attention_tc(const AttnLaunch &a, cudaStream_t stream);
+// CTAs of the mma.sync work-item kernel that fit on one SM for head dim D.
+int attention_ctas_per_sm(int D);
+// Rows above which items run on the tcgen05 kernel (INT32_MAX: never).
+int tc_row_threshold();
+
+// Counts every kernel launch the library makes.
+void count_launch();
+long long launch_count();
 
 // K/V write: copy-on-write copies (src, dst, used slots) then token scatter.
 struct KvWrite {

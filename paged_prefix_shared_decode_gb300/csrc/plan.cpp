@@ -3,30 +3,40 @@
 //
 // Decode plan (cascade over shared blocks):
 //  1. A trie over the batch's block tables, keyed at table position j by
-//     (physical block id, valid tokens in that block).  Sequences that share a
-//     key path share those blocks (prefix sharing from fork / RadixAttention:
-//     "Trellis" page, section "RadixAttention in Trellis"; "SGLang
-//     RadixAttention" page, radix-tree section).  Chains with one member set
-//     are merged into one segment.
-//  2. Sequences are ordered by a pre-order walk of the trie so that every
-//     segment's members are contiguous, then cut into row tiles of
+//     (physical block id, valid tokens in that block).  Sequences that share
+//     a key path share those blocks -- the prefix sharing that fork and
+//     RadixAttention create ("Trellis" page, section "RadixAttention in
+//     Trellis"; "SGLang RadixAttention" page, radix-tree section).  Chains
+//     with one member set are merged into one segment.
+//  2. Sequences are ordered by a pre-order walk of the trie, so every
+//     segment's members are contiguous, and cut into row tiles of
 //     floor(64 / G) sequences (at most 64 query rows: sequences x GQA group).
-//  3. A row tile's KV list is every segment any of its members touches, each
-//     cut into 64-token tiles tagged with the member interval that sees it.
-//     A segment shared by all of a tile's sequences is therefore read once
-//     for all of them.
-//  4. Long lists are cut into chunks so the grid covers the GPU; chunks of a
-//     row tile write partial (o, lse) rows that a merge kernel combines.
-// With use_sharing = 0 every sequence is its own row tile over its own table.
+//  3. Within a row tile, every segment that two or more of its sequences see
+//     goes into the tile's shared item as 64-token KV tiles tagged with the
+//     member interval that sees them: one read of such a tile serves all of
+//     those sequences.  Tokens that only one sequence of the tile sees go
+//     into a per-sequence private item (G rows, four warps splitting tokens).
+//  4. Items longer than needed to fill the GPU are cut into chunks.  A query
+//     row whose keys span several item chunks gets partial (o, lse) rows that
+//     the merge kernel combines by log-sum-exp; otherwise it is written
+//     directly.
+// With use_sharing = 0 every sequence is one private item over its own table.
 //
-// Verify plan: row tiles of floor(64 / G) draft nodes of one sequence; the
-// context is read in 64-token tiles seen by every node, then one tree-masked
-// tile with the draft tokens up to the tile's last node.
+// Verify plan: row tiles of floor(64 / G) draft nodes of one sequence; each
+// reads the context in 64-token tiles seen by every node, then one
+// tree-masked tile with the draft tokens up to the tile's last node.
+//
+// The plan carries each tile's physical block ids, so the kernels read no
+// device block table; block tables are consumed here, on the host.
 #include <algorithm>
+#include <atomic>
+#include <climits>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <numeric>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/kvp.h"
@@ -36,10 +46,9 @@ namespace kvp {
 namespace {
 
 struct Seg {
-    int32_t j0, j1;          // block range [j0, j1)
-    int32_t tok0, tok1;      // token range
-    int32_t row;             // a member's table row
-    int32_t lo, hi;          // members (positions in DFS order) [lo, hi)
+    int32_t tok0, tok1;   // token range
+    int32_t row;          // a member's table row
+    int32_t lo, hi;       // members (positions in pre-order) [lo, hi)
 };
 
 struct Builder {
@@ -47,31 +56,27 @@ struct Builder {
     const int32_t *lens;
     int32_t S, MB, bs;
     std::vector<int32_t> nblk;
-    std::vector<int32_t> order;   // DFS order of sequences
+    std::vector<int32_t> order;   // pre-order of sequences
     std::vector<Seg> segs;
 
     int32_t valid(int32_t s, int32_t j) const { return std::min(bs, lens[s] - j * bs); }
     int64_t key(int32_t s, int32_t j) const {
-        return ((int64_t)tables[(size_t)s * MB + j] << 8) | (int64_t)(valid(s, j) & 0xFF);
+        return ((int64_t)tables[(size_t)s * MB + j] << 24) | (int64_t)valid(s, j);
     }
 
-    // members share blocks [0, j); emit their subtree
+    // `members` share blocks [0, j); emit their subtree
     void build(const std::vector<int32_t> &members, int32_t j) {
-        // members whose path ends here come first in the order
         std::vector<int32_t> rest;
         for (int32_t s : members) {
-            if (nblk[s] <= j) order.push_back(s);
+            if (nblk[s] <= j) order.push_back(s);   // path ends here: first in order
             else rest.push_back(s);
         }
-        // group by key at j, first-seen order
         std::vector<std::vector<int32_t>> groups;
-        std::vector<int64_t> keys;
+        std::unordered_map<int64_t, size_t> gi;
         for (int32_t s : rest) {
-            int64_t k = key(s, j);
-            size_t g = 0;
-            while (g < keys.size() && keys[g] != k) ++g;
-            if (g == keys.size()) { keys.push_back(k); groups.emplace_back(); }
-            groups[g].push_back(s);
+            auto ins = gi.emplace(key(s, j), groups.size());
+            if (ins.second) groups.emplace_back();
+            groups[ins.first->second].push_back(s);
         }
         for (auto &g : groups) {
             int32_t j1 = j + 1;
@@ -86,12 +91,12 @@ struct Builder {
                     if (!same) break;
                 }
             }
-            size_t seg_index = segs.size();
-            segs.push_back(Seg{j, j1, j * bs, std::min(j1 * bs, lens[g[0]]), g[0], 0, 0});
+            size_t si = segs.size();
+            segs.push_back(Seg{j * bs, std::min(j1 * bs, lens[g[0]]), g[0], 0, 0});
             int32_t lo = (int32_t)order.size();
             build(g, j1);
-            segs[seg_index].lo = lo;
-            segs[seg_index].hi = (int32_t)order.size();
+            segs[si].lo = lo;
+            segs[si].hi = (int32_t)order.size();
         }
     }
 };
@@ -111,79 +116,145 @@ int sm_count_cached() {
 }
 
 struct HostPlan {
-    std::vector<WorkItem> items;
+    std::vector<WorkItem> items;      // mma.sync kernel
+    std::vector<WorkItem> tc_items;   // tcgen05 kernel
     std::vector<KvTile> tiles;
     std::vector<int32_t> members;
     std::vector<MergeDesc> merge;
-    int32_t n_row_tiles = 0, n_partial_rows = 0, ts = 1;
+    std::vector<int32_t> entries;
+    int32_t n_row_tiles = 0, n_partial_rows = 0, n_units = 0, n_tc_units = 0;
     int64_t unique_kv_bytes = 0;
 };
 
-// A row tile: members (query tokens) + its 64-token KV tiles (before chunking).
-struct RowTile {
+// An item before chunking: members (query tokens) and its KV tiles.
+struct ProtoItem {
     std::vector<int32_t> members;
     std::vector<KvTile> kv;
 };
 
-void push_range(std::vector<KvTile> &kv, int32_t row, int32_t t0, int32_t t1, int32_t lo,
-                int32_t hi, int32_t flags) {
+}  // namespace
+
+// Items with more rows than this run on the tcgen05 kernel.  KVP_ATTN_PATH=tc
+// in the environment enables it; otherwise every item stays on the mma.sync
+// kernel.
+int tc_row_threshold() {
+    static int thr = [] {
+        const char *e = std::getenv("KVP_ATTN_PATH");
+        return (e && std::strcmp(e, "tc") == 0) ? 32 : INT32_MAX;
+    }();
+    return thr;
+}
+
+namespace {
+
+// Members per row tile: 128 query rows when the tcgen05 kernel is in use.
+int32_t members_per_tile(int32_t G) {
+    const int rows = tc_row_threshold() == INT32_MAX ? kMmaMaxRows : kTcRows;
+    return std::max(1, rows / G);
+}
+
+struct TileSrc {
+    const int32_t *tables;
+    int32_t MB, bs;
+};
+
+void push_range(std::vector<KvTile> &kv, const TileSrc &src, int32_t row, int32_t t0, int32_t t1,
+                int32_t lo, int32_t hi, int32_t flags) {
+    const int32_t *tr = src.tables + (size_t)row * src.MB;
     for (int32_t t = t0; t < t1; t += kTileTokens) {
         int32_t n = std::min(kTileTokens, t1 - t);
-        kv.push_back(KvTile{row, t, n | (flags << 16), lo | (hi << 16)});
+        KvTile k{};
+        k.tok0 = t;
+        k.ntok_flags = n | (flags << 16);
+        k.members = lo | (hi << 16);
+        int32_t jb = t / src.bs, je = (t + n - 1) / src.bs;
+        for (int32_t j = jb; j <= je; ++j) k.blk[j - jb] = tr[j];
+        for (int32_t j = je - jb + 1; j < kTileBlocks; ++j) k.blk[j] = 0;
+        kv.push_back(k);
     }
 }
 
-// Chunk row tiles into work items and lay out partial rows and merge info.
-void finish(HostPlan &hp, std::vector<RowTile> &rts, int32_t G, int32_t nq, int32_t layers_heads,
-            int sms) {
-    int64_t total_tiles = 0;
-    int32_t max_rows = 0;
-    for (auto &rt : rts) {
-        total_tiles += (int64_t)rt.kv.size();
-        max_rows = std::max(max_rows, (int32_t)rt.members.size() * G);
+// Chunk items into work items, lay out partial rows and merge lists.  Items
+// with more than tc_row_threshold() rows go to the tcgen05 kernel (one CTA
+// per SM), the rest to the mma.sync kernel (`mma_ctas` CTAs per SM).
+void finish(HostPlan &hp, std::vector<ProtoItem> &protos, int32_t G, int32_t nq,
+            int32_t layers_heads, int32_t sms, int32_t mma_ctas) {
+    struct Chunked {
+        WorkItem it;
+        int64_t cost;
+        bool tc;
+    };
+    std::vector<Chunked> cs;
+    std::vector<int32_t> cover(nq, 0);
+    const int thr = tc_row_threshold();
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool tc = pass == 1;
+        int64_t total_tiles = 0, n_protos = 0;
+        for (auto &p : protos) {
+            if (((int)p.members.size() * G > thr) != tc) continue;
+            total_tiles += (int64_t)p.kv.size();
+            n_protos += 1;
+        }
+        if (n_protos == 0) continue;
+        // about two work units per resident CTA, so the atomic queue balances
+        const int64_t target_units = 2LL * sms * (tc ? 1 : mma_ctas);
+        int64_t chunk = kMaxItemTiles;
+        if (n_protos * layers_heads < target_units) {
+            int64_t want = (total_tiles * layers_heads + target_units - 1) / target_units;
+            chunk = std::max<int64_t>(4, std::min<int64_t>(chunk, want));
+        }
+        for (auto &p : protos) {
+            if (((int)p.members.size() * G > thr) != tc) continue;
+            const int32_t moff = (int32_t)hp.members.size();
+            hp.members.insert(hp.members.end(), p.members.begin(), p.members.end());
+            const int64_t nt = (int64_t)p.kv.size();
+            const int64_t nchunks = std::max<int64_t>(1, (nt + chunk - 1) / chunk);
+            const int32_t tbase = (int32_t)hp.tiles.size();
+            hp.tiles.insert(hp.tiles.end(), p.kv.begin(), p.kv.end());
+            const int32_t rows = (int32_t)p.members.size() * G;
+            for (int64_t c = 0; c < nchunks; ++c) {
+                const int64_t b = nt * c / nchunks, e = nt * (c + 1) / nchunks;
+                WorkItem it{};
+                it.tile_begin = tbase + (int32_t)b;
+                it.tile_end = tbase + (int32_t)e;
+                it.member_off = moff;
+                it.n_members = (int32_t)p.members.size();
+                it.out_base = 0;
+                // rows beyond 16 cost tensor and exp work per tile
+                cs.push_back(Chunked{it, (e - b) * (64 + std::max(16, rows)), tc});
+                for (int32_t m : p.members) cover[m] += 1;
+            }
+        }
     }
-    // aim for about 4 CTAs per SM over all (layer, kv head) pairs
-    int64_t target_items = std::max<int64_t>(1, (4LL * sms + layers_heads - 1) / layers_heads);
-    int64_t chunk = std::max<int64_t>(4, (total_tiles + target_items - 1) / target_items);
-    hp.merge.assign(nq, MergeDesc{0, 0, 0, 0});
-    hp.n_row_tiles = (int32_t)rts.size();
+    // partial rows for every chunk whose members are not all covered once
     int32_t P = 0;
-    struct Pending { WorkItem it; int64_t cost; };
-    std::vector<Pending> pend;
-    for (auto &rt : rts) {
-        int32_t nm = (int32_t)rt.members.size();
-        int32_t rows = nm * G;
-        int32_t moff = (int32_t)hp.members.size();
-        hp.members.insert(hp.members.end(), rt.members.begin(), rt.members.end());
-        int64_t nt = (int64_t)rt.kv.size();
-        int64_t nchunks = std::max<int64_t>(1, (nt + chunk - 1) / chunk);
-        int32_t base = -1;
-        if (nchunks > 1) {
-            base = P;
-            P += (int32_t)nchunks * rows;
-            for (int32_t m = 0; m < nm; ++m)
-                hp.merge[rt.members[m]] = MergeDesc{base, rows, (int32_t)nchunks, m};
-        }
-        int32_t tbase = (int32_t)hp.tiles.size();
-        hp.tiles.insert(hp.tiles.end(), rt.kv.begin(), rt.kv.end());
-        for (int64_t c = 0; c < nchunks; ++c) {
-            int64_t b = nt * c / nchunks, e = nt * (c + 1) / nchunks;
-            WorkItem it{};
-            it.tile_begin = tbase + (int32_t)b;
-            it.tile_end = tbase + (int32_t)e;
-            it.member_off = moff;
-            it.n_members = nm;
-            it.out_base = nchunks > 1 ? base + (int32_t)c * rows : -1;
-            pend.push_back(Pending{it, (e - b) * (64 + rows)});
+    std::vector<std::vector<int32_t>> ent(nq);
+    for (auto &c : cs) {
+        bool direct = true;
+        for (int32_t m = 0; m < c.it.n_members; ++m)
+            if (cover[hp.members[c.it.member_off + m]] != 1) direct = false;
+        if (direct) {
+            c.it.out_base = -1;
+        } else {
+            c.it.out_base = P;
+            for (int32_t m = 0; m < c.it.n_members; ++m)
+                ent[hp.members[c.it.member_off + m]].push_back(P + m * G);
+            P += c.it.n_members * G;
         }
     }
-    std::stable_sort(pend.begin(), pend.end(),
-                     [](const Pending &a, const Pending &b) { return a.cost > b.cost; });
-    for (auto &p : pend) hp.items.push_back(p.it);
+    hp.merge.assign(nq, MergeDesc{0, 0});
+    for (int32_t q = 0; q < nq; ++q) {
+        hp.merge[q] = MergeDesc{(int32_t)hp.entries.size(), (int32_t)ent[q].size()};
+        hp.entries.insert(hp.entries.end(), ent[q].begin(), ent[q].end());
+    }
+    std::stable_sort(cs.begin(), cs.end(),
+                     [](const Chunked &a, const Chunked &b) { return a.cost > b.cost; });
+    for (auto &c : cs) (c.tc ? hp.tc_items : hp.items).push_back(c.it);
     hp.n_partial_rows = P;
-    int32_t rg = (max_rows + 15) / 16;
-    hp.ts = rg <= 1 ? 4 : (rg <= 2 ? 2 : 1);
+    hp.n_units = (int32_t)hp.items.size() * layers_heads;
+    hp.n_tc_units = (int32_t)hp.tc_items.size() * layers_heads;
 }
+
 
 int build_decode(const kvp_attn_desc &d, const int32_t *tables, const int32_t *lens, int32_t S,
                  int32_t MB, int sms, HostPlan &hp) {
@@ -199,81 +270,111 @@ int build_decode(const kvp_attn_desc &d, const int32_t *tables, const int32_t *l
             if (id < 0 || id >= d.num_blocks) return KVP_ERR_INVALID;
         }
     }
-    std::vector<RowTile> rts;
+    TileSrc src{tables, MB, bs};
+    std::vector<ProtoItem> protos;
     const int64_t tok_bytes = 2LL * d.num_kv_heads * d.head_dim * 2 * d.num_layers;
     if (d.use_sharing) {
         std::vector<int32_t> all(S);
         std::iota(all.begin(), all.end(), 0);
         b.build(all, 0);
         for (auto &sg : b.segs) hp.unique_kv_bytes += (int64_t)(sg.tok1 - sg.tok0) * tok_bytes;
-        const int32_t per_tile = std::max(1, 64 / G);
+        const int32_t per_tile = members_per_tile(G);
         for (int32_t lo = 0; lo < S; lo += per_tile) {
-            int32_t hi = std::min(S, lo + per_tile);
-            RowTile rt;
-            rt.members.assign(b.order.begin() + lo, b.order.begin() + hi);
+            const int32_t hi = std::min(S, lo + per_tile);
+            hp.n_row_tiles += 1;
+            ProtoItem shared;
+            shared.members.assign(b.order.begin() + lo, b.order.begin() + hi);
+            std::vector<ProtoItem> priv(hi - lo);
+            for (int32_t m = lo; m < hi; ++m) priv[m - lo].members.push_back(b.order[m]);
             for (auto &sg : b.segs) {   // pre-order: a segment precedes its subtree
                 int32_t a = std::max(lo, sg.lo), e = std::min(hi, sg.hi);
                 if (a >= e) continue;
-                push_range(rt.kv, sg.row, sg.tok0, sg.tok1, a - lo, e - lo, 0);
+                if (e - a >= 2)
+                    push_range(shared.kv, src, sg.row, sg.tok0, sg.tok1, a - lo, e - lo, 0);
+                else
+                    push_range(priv[a - lo].kv, src, sg.row, sg.tok0, sg.tok1, 0, 1, 0);
             }
-            rts.push_back(std::move(rt));
+            if (!shared.kv.empty()) protos.push_back(std::move(shared));
+            for (auto &p : priv)
+                if (!p.kv.empty()) protos.push_back(std::move(p));
         }
     } else {
         for (int32_t s = 0; s < S; ++s) {
             hp.unique_kv_bytes += (int64_t)lens[s] * tok_bytes;
-            RowTile rt;
-            rt.members.push_back(s);
-            push_range(rt.kv, s, 0, lens[s], 0, 1, 0);
-            rts.push_back(std::move(rt));
+            hp.n_row_tiles += 1;
+            ProtoItem p;
+            p.members.push_back(s);
+            push_range(p.kv, src, s, 0, lens[s], 0, 1, 0);
+            protos.push_back(std::move(p));
         }
     }
-    finish(hp, rts, G, S, d.num_layers * d.num_kv_heads, sms);
+    finish(hp, protos, G, S, d.num_layers * d.num_kv_heads, sms, attention_ctas_per_sm(d.head_dim));
     return KVP_OK;
 }
 
-int build_verify(const kvp_attn_desc &d, const int32_t *ctx, int32_t B, int32_t n, int32_t MB,
-                 int sms, HostPlan &hp) {
+int build_verify(const kvp_attn_desc &d, const int32_t *tables, const int32_t *ctx, int32_t B,
+                 int32_t n, int32_t MB, int sms, HostPlan &hp) {
     const int32_t bs = d.block_size, G = d.num_q_heads / d.num_kv_heads;
     if (n <= 0 || n > 64) return KVP_ERR_INVALID;
     const int64_t tok_bytes = 2LL * d.num_kv_heads * d.head_dim * 2 * d.num_layers;
-    std::vector<RowTile> rts;
-    const int32_t per_tile = std::max(1, 64 / G);
+    TileSrc src{tables, MB, bs};
+    std::vector<ProtoItem> protos;
+    const int32_t per_tile = members_per_tile(G);
     for (int32_t b = 0; b < B; ++b) {
-        if (ctx[b] < 0 || ((int64_t)ctx[b] + n + bs - 1) / bs > MB) return KVP_ERR_INVALID;
+        if (ctx[b] < 0) return KVP_ERR_INVALID;
+        int64_t nb = ((int64_t)ctx[b] + n + bs - 1) / bs;
+        if (nb > MB) return KVP_ERR_INVALID;
+        for (int32_t j = 0; j < nb; ++j) {
+            int32_t id = tables[(size_t)b * MB + j];
+            if (id < 0 || id >= d.num_blocks) return KVP_ERR_INVALID;
+        }
         hp.unique_kv_bytes += (int64_t)(ctx[b] + n) * tok_bytes;
         for (int32_t i0 = 0; i0 < n; i0 += per_tile) {
             int32_t i1 = std::min(n, i0 + per_tile);
-            RowTile rt;
-            for (int32_t i = i0; i < i1; ++i) rt.members.push_back(b * n + i);
-            push_range(rt.kv, b, 0, ctx[b], 0, i1 - i0, 0);
+            hp.n_row_tiles += 1;
+            ProtoItem p;
+            for (int32_t i = i0; i < i1; ++i) p.members.push_back(b * n + i);
+            push_range(p.kv, src, b, 0, ctx[b], 0, i1 - i0, 0);
             // draft tokens 0 .. i1-1 (ancestors have smaller indices), tree-masked
-            push_range(rt.kv, b, ctx[b], ctx[b] + i1, 0, i1 - i0, kTileTree);
-            rts.push_back(std::move(rt));
+            push_range(p.kv, src, b, ctx[b], ctx[b] + i1, 0, i1 - i0, kTileTree);
+            protos.push_back(std::move(p));
         }
     }
-    finish(hp, rts, G, B * n, d.num_layers * d.num_kv_heads, sms);
+    finish(hp, protos, G, B * n, d.num_layers * d.num_kv_heads, sms, attention_ctas_per_sm(d.head_dim));
     return KVP_OK;
 }
 
 bool desc_ok(const kvp_attn_desc *d) {
-    return d && d->num_layers > 0 && d->num_q_heads > 0 && d->num_kv_heads > 0 &&
-           d->num_q_heads % d->num_kv_heads == 0 && d->num_q_heads / d->num_kv_heads <= 64 &&
-           (d->head_dim == 64 || d->head_dim == 128) && d->block_size > 0 && d->num_blocks > 0;
+    if (!d || d->num_layers <= 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 ||
+        d->num_q_heads % d->num_kv_heads != 0 || d->num_q_heads / d->num_kv_heads > 64 ||
+        (d->head_dim != 64 && d->head_dim != 128) || d->num_blocks <= 0)
+        return false;
+    // power-of-two block sizes >= 16: a 64-token tile touches at most 5 blocks
+    const int32_t bs = d->block_size;
+    return bs >= 16 && bs <= (1 << 20) && (bs & (bs - 1)) == 0;
+}
+
+int log2_int(int32_t x) {
+    int r = 0;
+    while ((1 << r) < x) ++r;
+    return r;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t items, tiles, members, merge, part_o, part_lse, total, plan_bytes;
+    size_t items, tc_items, tiles, members, merge, entries, part_o, part_lse, total, plan_bytes;
 };
 
 WsLayout layout(const HostPlan &hp, const kvp_attn_desc &d) {
     WsLayout w{};
     size_t off = sizeof(WsHeader);
     w.items = off;   off = align256(off + sizeof(WorkItem) * hp.items.size());
+    w.tc_items = off; off = align256(off + sizeof(WorkItem) * hp.tc_items.size());
     w.tiles = off;   off = align256(off + sizeof(KvTile) * hp.tiles.size());
     w.members = off; off = align256(off + sizeof(int32_t) * hp.members.size());
     w.merge = off;   off = align256(off + sizeof(MergeDesc) * hp.merge.size());
+    w.entries = off; off = align256(off + sizeof(int32_t) * hp.entries.size());
     w.plan_bytes = off;
     const size_t lh = (size_t)d.num_layers * d.num_kv_heads * (size_t)hp.n_partial_rows;
     w.part_o = off;  off = align256(off + sizeof(float) * lh * d.head_dim);
@@ -284,36 +385,43 @@ WsLayout layout(const HostPlan &hp, const kvp_attn_desc &d) {
 
 // Host image of the plan region, reused across calls on the same thread.
 thread_local std::vector<unsigned char> t_image;
+thread_local cudaEvent_t t_ev_before = nullptr, t_ev_after = nullptr;
+std::atomic<long long> g_launches{0};
 
 int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k_pool,
-        const void *v_pool, const int32_t *tables, int32_t MB, int32_t nq, const int32_t *parent,
-        int32_t n_draft, void *out, float *lse, void *ws, size_t ws_bytes, cudaStream_t stream) {
-    if (!q || !k_pool || !v_pool || !tables || !out || !ws) return KVP_ERR_INVALID;
+        const void *v_pool, int32_t nq, const int32_t *parent, int32_t n_draft, void *out,
+        float *lse, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!q || !k_pool || !v_pool || !out || !ws) return KVP_ERR_INVALID;
     if (((uintptr_t)ws & 255) != 0) return KVP_ERR_INVALID;
     if (((uintptr_t)q | (uintptr_t)k_pool | (uintptr_t)v_pool | (uintptr_t)out) & 15)
         return KVP_ERR_INVALID;
+    if ((uintptr_t)lse & 3) return KVP_ERR_INVALID;
     WsLayout w = layout(hp, d);
     if (ws_bytes < w.total) return KVP_ERR_INVALID;
     t_image.assign(w.plan_bytes, 0);
     unsigned char *img = t_image.data();
     WsHeader h{};
     h.n_items = (int32_t)hp.items.size();
+    h.n_tc_items = (int32_t)hp.tc_items.size();
+    h.n_units = hp.n_units;
     h.n_tiles = (int32_t)hp.tiles.size();
     h.n_members = (int32_t)hp.members.size();
-    h.n_merge = (int32_t)hp.merge.size();
+    h.n_entries = (int32_t)hp.entries.size();
     h.n_partial_rows = hp.n_partial_rows;
     std::memcpy(img, &h, sizeof h);
     std::memcpy(img + w.items, hp.items.data(), sizeof(WorkItem) * hp.items.size());
+    std::memcpy(img + w.tc_items, hp.tc_items.data(), sizeof(WorkItem) * hp.tc_items.size());
     std::memcpy(img + w.tiles, hp.tiles.data(), sizeof(KvTile) * hp.tiles.size());
     std::memcpy(img + w.members, hp.members.data(), sizeof(int32_t) * hp.members.size());
     std::memcpy(img + w.merge, hp.merge.data(), sizeof(MergeDesc) * hp.merge.size());
-    // pageable source: staged before the call returns
+    std::memcpy(img + w.entries, hp.entries.data(), sizeof(int32_t) * hp.entries.size());
+    // pageable source: the copy is staged before the call returns
     if (cudaMemcpyAsync(ws, img, w.plan_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return KVP_ERR_CUDA;
     unsigned char *base = (unsigned char *)ws;
     AttnLaunch a{};
-    a.q = q; a.k_pool = k_pool; a.v_pool = v_pool; a.tables = tables;
-    a.MB = MB; a.NB = d.num_blocks; a.bs = d.block_size;
+    a.q = q; a.k_pool = k_pool; a.v_pool = v_pool;
+    a.NB = d.num_blocks; a.bs_log2 = log2_int(d.block_size);
     a.Hq = d.num_q_heads; a.Hkv = d.num_kv_heads; a.G = d.num_q_heads / d.num_kv_heads;
     a.nq = nq; a.L = d.num_layers; a.D = d.head_dim;
     float scale = d.scale > 0.f ? d.scale : 1.0f / std::sqrt((float)d.head_dim);
@@ -321,69 +429,79 @@ int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k
     a.tree_parent = parent; a.n_draft = n_draft;
     a.out = out; a.lse = lse;
     a.err = (int32_t *)base;
+    a.counter = (int32_t *)base + 1;
+    a.tc_counter = (int32_t *)base + 2;
     a.items = (const WorkItem *)(base + w.items);
+    a.tc_items = (const WorkItem *)(base + w.tc_items);
     a.tiles = (const KvTile *)(base + w.tiles);
     a.members = (const int32_t *)(base + w.members);
     a.merge = (const MergeDesc *)(base + w.merge);
+    a.entries = (const int32_t *)(base + w.entries);
     a.part_o = (float *)(base + w.part_o);
     a.part_lse = (float *)(base + w.part_lse);
-    a.n_items = (int32_t)hp.items.size();
+    a.n_units = hp.n_units;
+    a.n_tc_units = hp.n_tc_units;
     a.n_merge_q = hp.n_partial_rows > 0 ? nq : 0;
     a.P = hp.n_partial_rows;
-    a.ts = hp.ts;
-    return launch_attention(a, stream) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+    return launch_attention(a, stream, t_ev_before, t_ev_after) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
 }  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
+
 }  // namespace kvp
 
 using namespace kvp;
 
 extern "C" {
 
-size_t kvp_decode_workspace_size(const kvp_attn_desc *desc, const int32_t *h_block_tables,
-                                 const int32_t *h_seq_lens, int32_t num_seqs, int32_t max_blocks) {
-    if (!desc_ok(desc) || num_seqs <= 0 || max_blocks <= 0 || !h_block_tables || !h_seq_lens) return 0;
+size_t kvp_decode_workspace_size(const kvp_attn_desc *desc, const int32_t *block_tables,
+                                 const int32_t *seq_lens, int32_t num_seqs, int32_t max_blocks) {
+    if (!desc_ok(desc) || num_seqs <= 0 || max_blocks <= 0 || !block_tables || !seq_lens) return 0;
     HostPlan hp;
-    if (build_decode(*desc, h_block_tables, h_seq_lens, num_seqs, max_blocks, sm_count_cached(), hp))
+    if (build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, sm_count_cached(), hp))
         return 0;
     return layout(hp, *desc).total;
 }
 
 int paged_decode_attention(const void *q, const void *k_pool, const void *v_pool,
-                           const int32_t *block_tables, const int32_t *h_block_tables,
-                           const int32_t *h_seq_lens, int32_t num_seqs, int32_t max_blocks,
-                           const kvp_attn_desc *desc, void *out, float *lse, void *workspace,
-                           size_t ws_bytes, void *stream) {
-    if (!desc_ok(desc) || num_seqs <= 0 || max_blocks <= 0 || !h_block_tables || !h_seq_lens)
+                           const int32_t *block_tables, const int32_t *seq_lens, int32_t num_seqs,
+                           int32_t max_blocks, const kvp_attn_desc *desc, void *out, float *lse,
+                           void *workspace, size_t ws_bytes, void *stream) {
+    if (!desc_ok(desc) || num_seqs <= 0 || max_blocks <= 0 || !block_tables || !seq_lens)
         return KVP_ERR_INVALID;
     HostPlan hp;
-    int rc = build_decode(*desc, h_block_tables, h_seq_lens, num_seqs, max_blocks, sm_count_cached(), hp);
+    int rc = build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, sm_count_cached(), hp);
     if (rc) return rc;
-    return run(hp, *desc, q, k_pool, v_pool, block_tables, max_blocks, num_seqs, nullptr, 0, out,
-               lse, workspace, ws_bytes, (cudaStream_t)stream);
+    return run(hp, *desc, q, k_pool, v_pool, num_seqs, nullptr, 0, out, lse, workspace, ws_bytes,
+               (cudaStream_t)stream);
 }
 
-size_t kvp_verify_workspace_size(const kvp_attn_desc *desc, const int32_t *h_ctx_lens,
-                                 int32_t batch, int32_t n_draft) {
-    if (!desc_ok(desc) || batch <= 0 || !h_ctx_lens) return 0;
+size_t kvp_verify_workspace_size(const kvp_attn_desc *desc, const int32_t *block_tables,
+                                 const int32_t *ctx_lens, int32_t batch, int32_t n_draft,
+                                 int32_t max_blocks) {
+    if (!desc_ok(desc) || batch <= 0 || !ctx_lens || !block_tables || max_blocks <= 0) return 0;
     HostPlan hp;
-    if (build_verify(*desc, h_ctx_lens, batch, n_draft, INT32_MAX / 2, sm_count_cached(), hp)) return 0;
+    if (build_verify(*desc, block_tables, ctx_lens, batch, n_draft, max_blocks, sm_count_cached(), hp))
+        return 0;
     return layout(hp, *desc).total;
 }
 
 int tree_verify_attention(const void *q, const int32_t *tree_parent, int32_t n_draft,
                           const void *k_pool, const void *v_pool, const int32_t *block_tables,
-                          const int32_t *h_ctx_lens, int32_t batch, int32_t max_blocks,
+                          const int32_t *ctx_lens, int32_t batch, int32_t max_blocks,
                           const kvp_attn_desc *desc, void *out, float *lse, void *workspace,
                           size_t ws_bytes, void *stream) {
-    if (!desc_ok(desc) || batch <= 0 || max_blocks <= 0 || !h_ctx_lens || !tree_parent)
+    if (!desc_ok(desc) || batch <= 0 || max_blocks <= 0 || !ctx_lens || !block_tables ||
+        !tree_parent)
         return KVP_ERR_INVALID;
     HostPlan hp;
-    int rc = build_verify(*desc, h_ctx_lens, batch, n_draft, max_blocks, sm_count_cached(), hp);
+    int rc = build_verify(*desc, block_tables, ctx_lens, batch, n_draft, max_blocks, sm_count_cached(), hp);
     if (rc) return rc;
-    return run(hp, *desc, q, k_pool, v_pool, block_tables, max_blocks, batch * n_draft, tree_parent,
-               n_draft, out, lse, workspace, ws_bytes, (cudaStream_t)stream);
+    return run(hp, *desc, q, k_pool, v_pool, batch * n_draft, tree_parent, n_draft, out, lse,
+               workspace, ws_bytes, (cudaStream_t)stream);
 }
 
 int kvp_device_error(void *workspace, void *stream, int32_t *err_out) {
@@ -398,21 +516,34 @@ int kvp_device_error(void *workspace, void *stream, int32_t *err_out) {
     return KVP_OK;
 }
 
-int kvp_decode_plan_stats(const kvp_attn_desc *desc, const int32_t *h_block_tables,
-                          const int32_t *h_seq_lens, int32_t num_seqs, int32_t max_blocks,
+int kvp_decode_plan_stats(const kvp_attn_desc *desc, const int32_t *block_tables,
+                          const int32_t *seq_lens, int32_t num_seqs, int32_t max_blocks,
                           int32_t sm_count, int32_t *n_items, int32_t *n_row_tiles,
                           int32_t *n_kv_tiles, int32_t *n_partial_rows, int64_t *unique_kv_bytes) {
-    if (!desc_ok(desc) || num_seqs <= 0 || max_blocks <= 0 || !h_block_tables || !h_seq_lens ||
+    if (!desc_ok(desc) || num_seqs <= 0 || max_blocks <= 0 || !block_tables || !seq_lens ||
         sm_count <= 0)
         return KVP_ERR_INVALID;
     HostPlan hp;
-    int rc = build_decode(*desc, h_block_tables, h_seq_lens, num_seqs, max_blocks, sm_count, hp);
+    int rc = build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, sm_count, hp);
     if (rc) return rc;
-    if (n_items) *n_items = (int32_t)hp.items.size();
+    if (n_items) *n_items = (int32_t)(hp.items.size() + hp.tc_items.size());
     if (n_row_tiles) *n_row_tiles = hp.n_row_tiles;
     if (n_kv_tiles) *n_kv_tiles = (int32_t)hp.tiles.size();
     if (n_partial_rows) *n_partial_rows = hp.n_partial_rows;
     if (unique_kv_bytes) *unique_kv_bytes = hp.unique_kv_bytes;
+    return KVP_OK;
+}
+
+int kvp_set_kernel_events(void *before, void *after) {
+    if ((before == nullptr) != (after == nullptr)) return KVP_ERR_INVALID;
+    t_ev_before = (cudaEvent_t)before;
+    t_ev_after = (cudaEvent_t)after;
+    return KVP_OK;
+}
+
+int kvp_kernel_launches(int64_t *n_out) {
+    if (!n_out) return KVP_ERR_INVALID;
+    *n_out = launch_count();
     return KVP_OK;
 }
 

@@ -58,9 +58,11 @@ class PoolRunner:
         except Exception:
             pass
 
-    def run_ops(self, kv_fn=None, device_kv=True):
+    def run_ops(self, kv_fn=None, device_kv=True, kv_dev_fn=None):
         """Replay the workload's ops.  kv_fn(w, i) gives host (k, v) bits for
-        append op i; with device_kv=False only the bookkeeping runs."""
+        append op i (the shared seeded generator by default); kv_dev_fn(w, i)
+        instead gives device tensors directly; with device_kv=False only the
+        bookkeeping runs."""
         from workloads import append_kv
         kv_fn = kv_fn or append_kv
         for i, op in enumerate(self.w.ops):
@@ -69,11 +71,14 @@ class PoolRunner:
             elif op[0] == "fork":
                 self.ids[op[2]] = seq_fork(self.pool, self.ids[op[1]])
             elif op[0] == "append":
-                if device_kv:
+                if not device_kv:
+                    seq_reserve(self.pool, self.ids[op[1]], op[2])
+                elif kv_dev_fn is not None:
+                    k, v = kv_dev_fn(self.w, i)
+                    seq_append(self.pool, self.ids[op[1]], k, v, op[2])
+                else:
                     k, v = kv_fn(self.w, i)
                     seq_append(self.pool, self.ids[op[1]], bf16_tensor(k), bf16_tensor(v), op[2])
-                else:
-                    seq_reserve(self.pool, self.ids[op[1]], op[2])
             elif op[0] == "free":
                 seq_free(self.pool, self.ids.pop(op[1]))
 
@@ -95,7 +100,7 @@ class PoolRunner:
 
 
 class DecodeCall:
-    """Buffers for paged_decode_attention over a fixed batch: device tables,
+    """Buffers for paged_decode_attention over a fixed batch: host tables,
     out, lse and a workspace sized for the current tables."""
 
     def __init__(self, runner: PoolRunner, use_sharing=True, scale=0.0):
@@ -106,23 +111,21 @@ class DecodeCall:
         S = len(runner.w.batch)
         self.out = torch.empty((s.L, S, s.Hq, s.d), dtype=torch.bfloat16, device="cuda")
         self.lse = torch.empty((s.L, S, s.Hq), dtype=torch.float32, device="cuda")
-        self.d_tables = torch.empty((S, runner.w.max_blocks_per_seq), dtype=torch.int32, device="cuda")
         self.ws = torch.empty(0, dtype=torch.uint8, device="cuda")
         self.h_tables = self.h_lens = None
 
     def refresh(self):
-        """Re-read tables from the pool, upload them, grow the workspace."""
+        """Re-read tables from the pool and grow the workspace if needed."""
         torch = _torch()
         t, ln = self.r.tables()
         self.h_tables, self.h_lens = t, ln
-        self.d_tables.copy_(torch.from_numpy(t), non_blocking=False)
         need = kvp_decode_workspace_size(self.desc, t, ln)
         if self.ws.numel() < need:
             self.ws = torch.empty(need + (1 << 20), dtype=torch.uint8, device="cuda")
 
     def __call__(self, q_dev, stream=None):
-        paged_decode_attention(q_dev, self.r.k_pool, self.r.v_pool, self.d_tables, self.h_tables,
-                               self.h_lens, self.desc, self.out, self.lse, self.ws, stream=stream)
+        paged_decode_attention(q_dev, self.r.k_pool, self.r.v_pool, self.h_tables, self.h_lens,
+                               self.desc, self.out, self.lse, self.ws, stream=stream)
         return self.out, self.lse
 
 
@@ -138,15 +141,13 @@ class VerifyCall:
         t, ln = runner.tables()
         self.ctx = (ln - self.n).astype(np.int32)
         self.h_tables = t
-        self.d_tables = torch.from_numpy(t).cuda()
         self.parent = torch.from_numpy(np.ascontiguousarray(w.info["parents"], np.int32)).cuda()
         self.out = torch.empty((s.L, self.B * self.n, s.Hq, s.d), dtype=torch.bfloat16, device="cuda")
         self.lse = torch.empty((s.L, self.B * self.n, s.Hq), dtype=torch.float32, device="cuda")
-        need = kvp_verify_workspace_size(self.desc, self.ctx, self.n)
+        need = kvp_verify_workspace_size(self.desc, t, self.ctx, self.n)
         self.ws = torch.empty(need, dtype=torch.uint8, device="cuda")
 
     def __call__(self, q_dev, stream=None):
-        tree_verify_attention(q_dev, self.parent, self.n, self.r.k_pool, self.r.v_pool, self.d_tables,
-                              self.ctx, self.h_tables.shape[1], self.desc, self.out, self.lse, self.ws,
-                              stream=stream)
+        tree_verify_attention(q_dev, self.parent, self.n, self.r.k_pool, self.r.v_pool, self.h_tables,
+                              self.ctx, self.desc, self.out, self.lse, self.ws, stream=stream)
         return self.out, self.lse

@@ -1,0 +1,64 @@
+"""Host-side logic of bench.py: workload naming and sizing, the JSON
+descriptors, peak lookup, and the max-over-ranks aggregation of the replica
+runs (world size 2 over gloo on CPU)."""
+import json
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+@pytest.mark.parametrize("name", ["dendrite", "trellis0.0", "trellis0.9", "mcts", "verify1", "verify32", "tiny"])
+def test_workloads_and_descriptions(name):
+    w = bench.workload(name, 40)
+    assert w.num_blocks > 0 and w.max_blocks_per_seq > 0
+    assert isinstance(bench.describe(w), str) and w.shapes.bs in (16, 32)
+
+
+def test_peaks_and_traffic_lookup():
+    peak, kind = bench.peaks()
+    assert peak > 1000 and kind in ("measured", "fallback")
+    t = bench.traffic_for_current_kernel()
+    assert t is None or t["dram_bytes_per_launch"] > 0
+
+
+def test_metric_matches_baseline_json():
+    with open(os.path.join(ROOT, "BASELINE.json")) as f:
+        assert json.load(f)["metric"] == bench.METRIC
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    out[rank] = bench.max_over_ranks(10.0 + rank * 5.0, world)
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    ps = [ctx.Process(target=_rank, args=(r, 2, port, out)) for r in range(2)]
+    for p in ps:
+        p.start()
+    for p in ps:
+        p.join(120)
+    assert all(p.exitcode == 0 for p in ps)
+    assert out[0] == out[1] == 15.0
+    assert bench.max_over_ranks(3.0, 1) == 3.0

@@ -165,31 +165,36 @@ def test_empty_sequence_and_bad_tables_are_rejected():
     q = bf16_tensor(W.step_q(w, 0))
     lens = call.h_lens.copy(); lens[0] = 0
     with pytest.raises(kvp.KvpError) as e:
-        kvp.paged_decode_attention(q, r.k_pool, r.v_pool, call.d_tables, call.h_tables, lens,
+        kvp.paged_decode_attention(q, r.k_pool, r.v_pool, call.h_tables, lens,
                                    call.desc, call.out, call.lse, call.ws)
     assert e.value.code == kvp.KVP_ERR_INVALID
     bad = call.h_tables.copy(); bad[0, 0] = r.NB
     with pytest.raises(kvp.KvpError):
-        kvp.paged_decode_attention(q, r.k_pool, r.v_pool, call.d_tables, bad, call.h_lens,
+        kvp.paged_decode_attention(q, r.k_pool, r.v_pool, bad, call.h_lens,
                                    call.desc, call.out, call.lse, call.ws)
     with pytest.raises(kvp.KvpError):      # workspace too small
-        kvp.paged_decode_attention(q, r.k_pool, r.v_pool, call.d_tables, call.h_tables, call.h_lens,
+        kvp.paged_decode_attention(q, r.k_pool, r.v_pool, call.h_tables, call.h_lens,
                                    call.desc, call.out, call.lse, call.ws, ws_bytes=256)
+    import ctypes
+    d = kvp.AttnDesc(call.desc.num_layers, 32, 8, 128, 24, r.NB, 0.0, 1)   # bs not a power of 2
+    with pytest.raises(kvp.KvpError):
+        kvp.paged_decode_attention(q, r.k_pool, r.v_pool, call.h_tables, call.h_lens,
+                                   d, call.out, call.lse, call.ws)
 
 
-def test_device_error_word_value():
-    """A device table entry outside the pool (the host copy is valid) is caught
-    by the kernel's own bounds check: the error word is set, the tile reads as
-    zeros, and reading the word clears it."""
-    w = _custom([10], prefix=40, step_tokens=0)
+def test_repeated_calls_and_error_word_clean():
+    """The workspace's atomic work counter and error word are reset by every
+    call's plan upload: back-to-back calls give identical results."""
+    w = _custom([10, 3], prefix=40, step_tokens=0)
     r = PoolRunner(w)
     r.run_ops()
     call = DecodeCall(r)
     call.refresh()
-    call.d_tables[0, 1] = -7
-    call(bf16_tensor(W.step_q(w, 0)))
-    assert kvp.kvp_device_error(call.ws) == 1
-    assert kvp.kvp_device_error(call.ws) == 0       # read clears it
-    call.refresh()
-    call(bf16_tensor(W.step_q(w, 0)))
+    q = bf16_tensor(W.step_q(w, 0))
+    call(q)
+    first = call.out.clone()
+    for _ in range(3):
+        call(q)
+    torch.cuda.synchronize()
+    assert torch.equal(first, call.out)
     assert kvp.kvp_device_error(call.ws) == 0
