@@ -29,7 +29,8 @@ __all__ = [
 KVP_OK, KVP_ERR_INVALID, KVP_ERR_OOM, KVP_ERR_STATE, KVP_ERR_CUDA, KVP_ERR_DEVICE = 0, -1, -2, -3, -4, -5
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-lib_path = os.path.join(_HERE, "libkvp.so")
+# KVP_LIB_PATH points the binding at another build of the same C ABI.
+lib_path = os.environ.get("KVP_LIB_PATH") or os.path.join(_HERE, "libkvp.so")
 _lib = None
 
 

@@ -402,15 +402,17 @@ __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kerne
     extern __shared__ __align__(128) unsigned char smem[];
     KvTile *s_tiles = reinterpret_cast<KvTile *>(smem + C::DESC_OFF);
     __shared__ int s_unit;
-    const int lh = a.L * a.Hkv;
+    const int n_items = a.n_units / (a.L * a.Hkv);
     for (;;) {
         if (threadIdx.x == 0) s_unit = atomicAdd(a.counter, 1);
         __syncthreads();
         const int unit = s_unit;
         if (unit >= a.n_units) break;
-        const int item_idx = unit / lh;
-        const int rem = unit - item_idx * lh;
-        const int kvh = rem % a.Hkv, l = rem / a.Hkv;
+        // item-minor order: the items of one (layer, kv head) run together, so
+        // row tiles that read the same shared blocks meet in L2
+        const int item_idx = unit % n_items;
+        const int lk = unit / n_items;
+        const int kvh = lk % a.Hkv, l = lk / a.Hkv;
         const WorkItem it = a.items[item_idx];
         const int ntile = it.tile_end - it.tile_begin;
         const int4 *src = reinterpret_cast<const int4 *>(a.tiles + it.tile_begin);
@@ -504,20 +506,49 @@ Occupancy &occupancy() {
     return occ;
 }
 
+// A second stream (per thread) so that the tcgen05 and mma.sync kernels of one
+// call can share the GPU: the caller's stream forks to it and joins back.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool ok = false;
+    SideStream() {
+        ok = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&join, cudaEventDisableTiming) == cudaSuccess;
+    }
+};
+
 template <int D>
 cudaError_t launch_d(const AttnLaunch &a, cudaStream_t stream, cudaEvent_t before, cudaEvent_t after) {
     using C = KCfg<D>;
     Occupancy &occ = occupancy<D>();
     if (!occ.ok) return cudaErrorInvalidDevice;
     if (before && cudaEventRecord(before, stream) != cudaSuccess) return cudaErrorInvalidResourceHandle;
-    cudaError_t e = launch_attention_tc(a, stream);
+    const bool both = a.n_tc_units > 0 && a.n_units > 0;
+    thread_local SideStream side;
+    cudaStream_t mma_stream = stream;
+    if (both && side.ok) {
+        // fork: the mma.sync kernel runs beside the tcgen05 kernel, which then
+        // takes one CTA per SM to leave room for it
+        if (cudaEventRecord(side.fork, stream) != cudaSuccess ||
+            cudaStreamWaitEvent(side.s, side.fork, 0) != cudaSuccess)
+            return cudaErrorUnknown;
+        mma_stream = side.s;
+    }
+    cudaError_t e = launch_attention_tc(a, stream, both && side.ok ? 1 : 0);
     if (e != cudaSuccess) return e;
     if (a.n_units > 0) {
         const int grid = a.n_units < occ.sms * occ.per_sm ? a.n_units : occ.sms * occ.per_sm;
-        attn_item_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(a);
+        attn_item_kernel<D><<<grid, kThreads, C::SMEM, mma_stream>>>(a);
         count_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+    }
+    if (mma_stream != stream) {
+        if (cudaEventRecord(side.join, mma_stream) != cudaSuccess ||
+            cudaStreamWaitEvent(stream, side.join, 0) != cudaSuccess)
+            return cudaErrorUnknown;
     }
     if (after && cudaEventRecord(after, stream) != cudaSuccess) return cudaErrorInvalidResourceHandle;
     if (a.P == 0) return cudaSuccess;

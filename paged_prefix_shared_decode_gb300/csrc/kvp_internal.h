@@ -83,12 +83,16 @@ struct AttnLaunch {
 // before/after: optional events recorded around the work-item kernel.
 cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream, cudaEvent_t before,
                              cudaEvent_t after);
-// tcgen05 kernel over a.tc_items (no-op when there are none).
-cudaError_t launch_attention_tc(const AttnLaunch &a, cudaStream_t stream);
+// tcgen05 kernel over a.tc_items (no-op when there are none); at most
+// `ctas_per_sm` CTAs per SM (0: as many as fit).
+cudaError_t launch_attention_tc(const AttnLaunch &a, cudaStream_t stream, int ctas_per_sm);
+// Whether the tcgen05 kernel can address this pool (32-bit TMA row index).
+bool tc_path_supported(int L, int NB, int Hkv, int bs);
 // CTAs of the mma.sync work-item kernel that fit on one SM for head dim D.
 int attention_ctas_per_sm(int D);
-// Rows above which items run on the tcgen05 kernel (INT32_MAX: never).
-int tc_row_threshold();
+// Rows above which items of head dim D run on the tcgen05 kernel
+// (INT32_MAX: never).
+int tc_row_threshold(int head_dim);
 
 // Counts every kernel launch the library makes.
 void count_launch();

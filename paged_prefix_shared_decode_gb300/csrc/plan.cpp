@@ -134,23 +134,33 @@ struct ProtoItem {
 
 }  // namespace
 
-// Items with more rows than this run on the tcgen05 kernel.  KVP_ATTN_PATH=tc
-// in the environment enables it; otherwise every item stays on the mma.sync
-// kernel.
-int tc_row_threshold() {
-    static int thr = [] {
+// Items with more rows than this run on the tcgen05 kernel.  By default that
+// is every many-row item for head dim 128 (verify, MCTS: measured 1.9x and
+// 1.25x faster than mma.sync) and none for head dim 64, where the mma.sync
+// kernel measured faster on the shared-prefix decode shapes.
+// KVP_ATTN_PATH=tc / =mma in the environment forces one path (ablations).
+int tc_row_threshold(int head_dim) {
+    static int mode = [] {
         const char *e = std::getenv("KVP_ATTN_PATH");
-        return (e && std::strcmp(e, "tc") == 0) ? 32 : INT32_MAX;
+        if (e && std::strcmp(e, "tc") == 0) return 1;
+        if (e && std::strcmp(e, "mma") == 0) return 2;
+        return 0;
     }();
-    return thr;
+    if (mode == 2) return INT32_MAX;
+    if (mode == 1 || head_dim == 128) return 32;
+    return INT32_MAX;
 }
 
 namespace {
 
+bool tc_usable(const kvp_attn_desc &d) {
+    return tc_row_threshold(d.head_dim) != INT32_MAX &&
+           tc_path_supported(d.num_layers, d.num_blocks, d.num_kv_heads, d.block_size);
+}
+
 // Members per row tile: 128 query rows when the tcgen05 kernel is in use.
-int32_t members_per_tile(int32_t G) {
-    const int rows = tc_row_threshold() == INT32_MAX ? kMmaMaxRows : kTcRows;
-    return std::max(1, rows / G);
+int32_t members_per_tile(int32_t G, bool tc) {
+    return std::max(1, (tc ? kTcRows : kMmaMaxRows) / G);
 }
 
 struct TileSrc {
@@ -175,10 +185,10 @@ void push_range(std::vector<KvTile> &kv, const TileSrc &src, int32_t row, int32_
 }
 
 // Chunk items into work items, lay out partial rows and merge lists.  Items
-// with more than tc_row_threshold() rows go to the tcgen05 kernel (one CTA
-// per SM), the rest to the mma.sync kernel (`mma_ctas` CTAs per SM).
+// with more than `thr` rows go to the tcgen05 kernel (one CTA per SM), the
+// rest to the mma.sync kernel (`mma_ctas` CTAs per SM).
 void finish(HostPlan &hp, std::vector<ProtoItem> &protos, int32_t G, int32_t nq,
-            int32_t layers_heads, int32_t sms, int32_t mma_ctas) {
+            int32_t layers_heads, int32_t sms, int32_t mma_ctas, int thr) {
     struct Chunked {
         WorkItem it;
         int64_t cost;
@@ -186,7 +196,6 @@ void finish(HostPlan &hp, std::vector<ProtoItem> &protos, int32_t G, int32_t nq,
     };
     std::vector<Chunked> cs;
     std::vector<int32_t> cover(nq, 0);
-    const int thr = tc_row_threshold();
     for (int pass = 0; pass < 2; ++pass) {
         const bool tc = pass == 1;
         int64_t total_tiles = 0, n_protos = 0;
@@ -278,7 +287,7 @@ int build_decode(const kvp_attn_desc &d, const int32_t *tables, const int32_t *l
         std::iota(all.begin(), all.end(), 0);
         b.build(all, 0);
         for (auto &sg : b.segs) hp.unique_kv_bytes += (int64_t)(sg.tok1 - sg.tok0) * tok_bytes;
-        const int32_t per_tile = members_per_tile(G);
+        const int32_t per_tile = members_per_tile(G, tc_usable(d));
         for (int32_t lo = 0; lo < S; lo += per_tile) {
             const int32_t hi = std::min(S, lo + per_tile);
             hp.n_row_tiles += 1;
@@ -308,7 +317,8 @@ int build_decode(const kvp_attn_desc &d, const int32_t *tables, const int32_t *l
             protos.push_back(std::move(p));
         }
     }
-    finish(hp, protos, G, S, d.num_layers * d.num_kv_heads, sms, attention_ctas_per_sm(d.head_dim));
+    finish(hp, protos, G, S, d.num_layers * d.num_kv_heads, sms, attention_ctas_per_sm(d.head_dim),
+           tc_usable(d) ? tc_row_threshold(d.head_dim) : INT32_MAX);
     return KVP_OK;
 }
 
@@ -319,7 +329,7 @@ int build_verify(const kvp_attn_desc &d, const int32_t *tables, const int32_t *c
     const int64_t tok_bytes = 2LL * d.num_kv_heads * d.head_dim * 2 * d.num_layers;
     TileSrc src{tables, MB, bs};
     std::vector<ProtoItem> protos;
-    const int32_t per_tile = members_per_tile(G);
+    const int32_t per_tile = members_per_tile(G, tc_usable(d));
     for (int32_t b = 0; b < B; ++b) {
         if (ctx[b] < 0) return KVP_ERR_INVALID;
         int64_t nb = ((int64_t)ctx[b] + n + bs - 1) / bs;
@@ -340,7 +350,8 @@ int build_verify(const kvp_attn_desc &d, const int32_t *tables, const int32_t *c
             protos.push_back(std::move(p));
         }
     }
-    finish(hp, protos, G, B * n, d.num_layers * d.num_kv_heads, sms, attention_ctas_per_sm(d.head_dim));
+    finish(hp, protos, G, B * n, d.num_layers * d.num_kv_heads, sms, attention_ctas_per_sm(d.head_dim),
+           tc_usable(d) ? tc_row_threshold(d.head_dim) : INT32_MAX);
     return KVP_OK;
 }
 

@@ -14,12 +14,27 @@ REL_RMS = 5e-3
 LSE_ABS = 1e-3
 
 
+def bf16_absmax(bits):
+    """max |x| over a uint16 bf16 bit-pattern array."""
+    from workloads import bf16_bits_to_f32
+    return float(np.abs(bf16_bits_to_f32(bits)).max())
+
+
 def to_f64(t):
     """torch tensor (bf16 / fp32, any device) -> float64 numpy."""
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def check_close(got, want, what="out"):
+def peaked_max_abs(want, v_absmax):
+    """Max-abs bound for sharply peaked softmax (queries scaled up): one or two
+    keys carry the weight, so the bf16 rounding of P (unit roundoff 2^-8,
+    relative to p) passes straight through to out as up to 2^-8 * |v|, and the
+    bf16 rounding of out itself adds up to 2^-8 * |out|; the rounding errors no
+    longer average out over many keys as they do for the N(0,1) workloads."""
+    return 2.0 ** -8 * (float(np.abs(want).max()) + float(v_absmax)) + 1e-3
+
+
+def check_close(got, want, what="out", max_abs_tol=MAX_ABS):
     got = np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)
@@ -27,7 +42,7 @@ def check_close(got, want, what="out"):
     err = np.abs(got - want)
     max_abs = float(err.max()) if err.size else 0.0
     rel = float(np.sqrt((err ** 2).sum() / max((want ** 2).sum(), 1e-300)))
-    assert max_abs <= MAX_ABS, f"{what}: max-abs {max_abs:.3e} > {MAX_ABS}"
+    assert max_abs <= max_abs_tol, f"{what}: max-abs {max_abs:.3e} > {max_abs_tol:.3e}"
     assert rel <= REL_RMS, f"{what}: rel-RMS {rel:.3e} > {REL_RMS}"
     return max_abs, rel
 

@@ -1,0 +1,28 @@
+"""Both attention kernels on every shape: by default items with more than 32
+query rows run on the tcgen05 kernel for head dim 128 and on the mma.sync
+kernel for head dim 64; KVP_ATTN_PATH forces one of them.  Re-runs a subset of
+the parity tests in a child process under each forced setting."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SUBSET = ("tiny_fork or dendrite_full or trellis or mcts_tree or ragged or cow or gqa or "
+          "verify_B1 or verify_tree_shapes or short_draft")
+
+
+@pytest.mark.parametrize("path", ["tc", "mma"])
+def test_forced_attention_path(path):
+    env = dict(os.environ, KVP_ATTN_PATH=path)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "-m", "gpu",
+                        "tests/test_gpu_decode.py", "tests/test_gpu_verify.py", "-k", SUBSET],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=1200)
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
