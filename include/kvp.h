@@ -213,6 +213,32 @@ int tree_verify_attention(const void *q, const int32_t *tree_parent, int32_t n_d
                           const kvp_attn_desc *desc, void *out, float *lse, void *workspace,
                           size_t ws_bytes, void *stream);
 
+/*
+ * Decode attention for callers that cannot allocate device memory -- e.g. a
+ * serving process whose memory manager has already given (nearly) all device
+ * memory to its own pools, or a plug-in that cannot reach its host program's
+ * allocator and must not bypass it.  Same arguments and results as
+ * paged_decode_attention, without workspace: the scratch space is a
+ * KVP_STATIC_WORKSPACE_BYTES array inside the library, present on every GPU
+ * that loads it until the process exits.  The pages have no counterpart; this
+ * is an interface for such callers.
+ *   - Returns KVP_ERR_INVALID, before enqueuing anything, when the batch's plan
+ *     needs more than KVP_STATIC_WORKSPACE_BYTES (see
+ *     kvp_decode_workspace_size).
+ *   - All calls on a device share the array: calls that overlap on the GPU
+ *     race; serialise them.  Each call rewrites the words that must start at
+ *     zero (error word, work counters) before its kernels run.
+ *   - The first call on each device looks up the array's device address; make
+ *     it before any stream capture.  No call allocates device memory.
+ * kvp_device_error cannot read this call's error word (there is no caller
+ * workspace); bounds violations still skip the access.
+ */
+#define KVP_STATIC_WORKSPACE_BYTES (32u << 20)
+int paged_decode_attention_noalloc(const void *q, const void *k_pool, const void *v_pool,
+                                   const int32_t *block_tables, const int32_t *seq_lens,
+                                   int32_t num_seqs, int32_t max_blocks, const kvp_attn_desc *desc,
+                                   void *out, float *lse, void *stream);
+
 /* Reads (and clears) the device error word that the last attention call on
  * this workspace left; synchronises `stream`.  *err_out = 0 when clean. */
 int kvp_device_error(void *workspace, void *stream, int32_t *err_out);

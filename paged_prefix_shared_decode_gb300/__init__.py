@@ -22,11 +22,13 @@ __all__ = [
     "kvp_free_block_count", "kvp_cow_count", "kvp_gather_tables", "kvp_export_tables",
     "kvp_decode_workspace_size", "paged_decode_attention", "kvp_verify_workspace_size",
     "tree_verify_attention", "kvp_device_error", "kvp_decode_plan_stats", "kvp_strerror",
-    "kvp_set_kernel_events", "kvp_kernel_launches",
+    "kvp_set_kernel_events", "kvp_kernel_launches", "paged_decode_attention_noalloc",
+    "KVP_STATIC_WORKSPACE_BYTES",
     "KVP_OK", "KVP_ERR_INVALID", "KVP_ERR_OOM", "KVP_ERR_STATE", "KVP_ERR_CUDA", "KVP_ERR_DEVICE",
 ]
 
 KVP_OK, KVP_ERR_INVALID, KVP_ERR_OOM, KVP_ERR_STATE, KVP_ERR_CUDA, KVP_ERR_DEVICE = 0, -1, -2, -3, -4, -5
+KVP_STATIC_WORKSPACE_BYTES = 32 << 20   # size of the library's own workspace (include/kvp.h)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 # KVP_LIB_PATH points the binding at another build of the same C ABI.
@@ -94,6 +96,8 @@ _SIGS = {
                                _I32P, _I32P, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
     "kvp_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "kvp_set_kernel_events": ([_P, _P], ctypes.c_int),
+    "paged_decode_attention_noalloc": ([_P, _P, _P, _P, _P, _I32, _I32, ctypes.POINTER(AttnDesc), _P, _P,
+                                        _P], ctypes.c_int),
     "kvp_kernel_launches": ([ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
 }
 
@@ -269,6 +273,18 @@ def paged_decode_attention(q, k_pool, v_pool, block_tables, seq_lens, desc: Attn
                                          t.shape[1], ctypes.byref(desc), _dev(out), _dev(lse),
                                          _dev(workspace), _ws_bytes(workspace, ws_bytes),
                                          _stream(stream)), "paged_decode_attention")
+
+
+def paged_decode_attention_noalloc(q, k_pool, v_pool, block_tables, seq_lens, desc: AttnDesc, out,
+                                   lse, stream=None):
+    """paged_decode_attention without a caller workspace: for callers that
+    cannot allocate device memory.  The library's own KVP_STATIC_WORKSPACE_BYTES
+    array is used; calls on one device must not overlap."""
+    t, tp = _host_i32(block_tables)
+    ln, lp = _host_i32(seq_lens)
+    _check(load().paged_decode_attention_noalloc(_dev(q), _dev(k_pool), _dev(v_pool), tp, lp, t.shape[0],
+                                                 t.shape[1], ctypes.byref(desc), _dev(out), _dev(lse),
+                                                 _stream(stream)), "paged_decode_attention_noalloc")
 
 
 def kvp_verify_workspace_size(desc: AttnDesc, block_tables, ctx_lens, n_draft: int) -> int:
