@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dendrite")
     ap.add_argument("--sweep", action="store_true", help="add the phi / MCTS / verify sweep")
+    ap.add_argument("--sweep-set", default="", help="comma list of sweep workloads (default: all)")
     ap.add_argument("--no-sharing", action="store_true", help="ablation: every sequence reads its own blocks")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -453,8 +454,11 @@ def run_sweep(a, dev):
 
     out = []
     peak, _ = peaks()
-    for name in ["trellis0.0", "trellis0.25", "trellis0.5", "trellis0.75", "trellis0.9", "mcts",
-                 "verify1", "verify8", "verify32"]:
+    names = ["trellis0.0", "trellis0.25", "trellis0.5", "trellis0.75", "trellis0.9", "mcts",
+             "verify1", "verify8", "verify32"]
+    if a.sweep_set:
+        names = [n for n in a.sweep_set.split(",") if n]
+    for name in names:
         sub = argparse.Namespace(**vars(a))
         sub.steps, sub.warmup = 5, 3
         if name.startswith("verify"):

@@ -242,50 +242,67 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
                 mma16816(s[2 * j2 + 1], qf[kk], b2, b3);
             }
         }
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+        // raw scores; masked ones -inf.  Padding rows (past the item's rows)
+        // are never written, so whole tiles seen by every real row skip masking.
+        const bool fast = tb + TOKW <= ntok && !tree && (in0 || !has0) && (in1 || !has1);
+        if (!__all_sync(0xffffffffu, fast)) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = tb + j * 8 + 2 * tq + (e & 1);
+                    const bool hi = e >= 2;
+                    bool ok = tok < ntok && (hi ? in1 : in0);
+                    if (tree) ok = ok && (((hi ? tm1 : tm0) >> (tok & 63)) & 1ull);
+                    if (!ok) s[j][e] = -INFINITY;
+                }
+            }
+        }
+        float mx0 = s[0][0], mx1 = s[0][2];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int tok = tb + j * 8 + 2 * tq + (e & 1);
-                const bool hi = e >= 2;
-                bool ok = tok < ntok && (hi ? in1 : in0);
-                if (tree) ok = ok && (((hi ? tm1 : tm0) >> (tok & 63)) & 1ull);
-                const float v = ok ? s[j][e] * a.scale_log2 : -INFINITY;
-                s[j][e] = v;
-                if (hi) mx1 = fmaxf(mx1, v);
-                else mx0 = fmaxf(mx0, v);
-            }
+            mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
+            mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
         }
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float b0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float b1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = exp2_sfu(m0 - b0), al1 = exp2_sfu(m1 - b1);
-        m0 = mn0;
-        m1 = mn1;
+        // the running max m (base-2, scaled) is raised only when a tile's max
+        // exceeds it by more than 8, so p = 2^(s*scale - m) <= 2^8 and O is
+        // rarely rescaled
+        const float sc = a.scale_log2;
+        const float t0 = mx0 * sc, t1 = mx1 * sc;
+        const bool up0 = m0 == -INFINITY ? t0 != -INFINITY : t0 > m0 + 8.f;
+        const bool up1 = m1 == -INFINITY ? t1 != -INFINITY : t1 > m1 + 8.f;
+        if (__any_sync(0xffffffffu, (up0 && m0 != -INFINITY) || (up1 && m1 != -INFINITY))) {
+            const float al0 = up0 && m0 != -INFINITY ? exp2_sfu(m0 - t0) : 1.f;
+            const float al1 = up1 && m1 != -INFINITY ? exp2_sfu(m1 - t1) : 1.f;
+            l0 *= al0;
+            l1 *= al1;
+#pragma unroll
+            for (int n = 0; n < C::NO; ++n) {
+                o[n][0] *= al0;
+                o[n][1] *= al0;
+                o[n][2] *= al1;
+                o[n][3] *= al1;
+            }
+        }
+        if (up0) m0 = t0;
+        if (up1) m1 = t1;
+        const float nm0 = m0 == -INFINITY ? 0.f : -m0, nm1 = m1 == -INFINITY ? 0.f : -m1;
         float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-            s[j][0] = exp2_sfu(s[j][0] - b0);
-            s[j][1] = exp2_sfu(s[j][1] - b0);
-            s[j][2] = exp2_sfu(s[j][2] - b1);
-            s[j][3] = exp2_sfu(s[j][3] - b1);
+            s[j][0] = exp2_sfu(fmaf(s[j][0], sc, nm0));
+            s[j][1] = exp2_sfu(fmaf(s[j][1], sc, nm0));
+            s[j][2] = exp2_sfu(fmaf(s[j][2], sc, nm1));
+            s[j][3] = exp2_sfu(fmaf(s[j][3], sc, nm1));
             rs0 += s[j][0] + s[j][1];
             rs1 += s[j][2] + s[j][3];
         }
-        l0 = l0 * al0 + rs0;
-        l1 = l1 * al1 + rs1;
-#pragma unroll
-        for (int n = 0; n < C::NO; ++n) {
-            o[n][0] *= al0;
-            o[n][1] *= al0;
-            o[n][2] *= al1;
-            o[n][3] *= al1;
-        }
+        l0 += rs0;
+        l1 += rs1;
 #pragma unroll
         for (int k2 = 0; k2 < NT / 2; ++k2) {
             const uint32_t pa[4] = {pack_bf16x2(s[2 * k2][0], s[2 * k2][1]),

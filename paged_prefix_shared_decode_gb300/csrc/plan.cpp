@@ -158,9 +158,22 @@ bool tc_usable(const kvp_attn_desc &d) {
            tc_path_supported(d.num_layers, d.num_blocks, d.num_kv_heads, d.block_size);
 }
 
+// Query rows per row tile on the mma.sync kernel.  Fewer rows per tile means
+// more tiles read the same shared blocks (from L2, since their units run back
+// to back) for cheaper per-tile work; 64 rows measured fastest on the decode
+// shapes.  KVP_MMA_ROWS (16, 32 or 64) overrides it for ablations.
+int32_t mma_tile_rows() {
+    static int rows = [] {
+        const char *e = std::getenv("KVP_MMA_ROWS");
+        int v = e ? std::atoi(e) : 64;
+        return (v == 16 || v == 32 || v == 64) ? v : 64;
+    }();
+    return rows;
+}
+
 // Members per row tile: 128 query rows when the tcgen05 kernel is in use.
 int32_t members_per_tile(int32_t G, bool tc) {
-    return std::max(1, (tc ? kTcRows : kMmaMaxRows) / G);
+    return std::max(1, (tc ? kTcRows : mma_tile_rows()) / G);
 }
 
 struct TileSrc {
