@@ -102,6 +102,14 @@ __device__ uint64_t ancestor_mask(const int32_t *parent, int b, int i, int n, in
     return m;
 }
 
+// Ancestor-or-self masks of all draft query tokens, once per call, so the
+// attention kernels read one word per query row instead of walking the tree.
+__global__ void tree_mask_kernel(const int32_t *parent, int32_t nq, int32_t n, uint64_t *mask,
+                                 int32_t *err) {
+    const int q = blockIdx.x * blockDim.x + threadIdx.x;
+    if (q < nq) mask[q] = ancestor_mask(parent, q / n, q % n, n, err);
+}
+
 template <int D>
 struct KCfg {
     static constexpr int CH = D / 8;                        // 16-byte chunks per token row
@@ -199,9 +207,9 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
         qf[kk][3] = has1 ? ld_u32(q1 + c + 8) : 0u;
     }
     uint64_t tm0 = ~0ull, tm1 = ~0ull;
-    if (a.tree_parent) {
-        if (has0) tm0 = ancestor_mask(a.tree_parent, qt0 / a.n_draft, qt0 % a.n_draft, a.n_draft, a.err);
-        if (has1) tm1 = ancestor_mask(a.tree_parent, qt1 / a.n_draft, qt1 % a.n_draft, a.n_draft, a.err);
+    if (a.tree_mask) {
+        if (has0) tm0 = a.tree_mask[qt0];
+        if (has1) tm1 = a.tree_mask[qt1];
     }
 
     float o[C::NO][4];
@@ -542,6 +550,13 @@ cudaError_t launch_d(const AttnLaunch &a, cudaStream_t stream, cudaEvent_t befor
     Occupancy &occ = occupancy<D>();
     if (!occ.ok) return cudaErrorInvalidDevice;
     if (before && cudaEventRecord(before, stream) != cudaSuccess) return cudaErrorInvalidResourceHandle;
+    if (a.tree_mask && a.nq > 0) {
+        tree_mask_kernel<<<(a.nq + 255) / 256, 256, 0, stream>>>(a.tree_parent, a.nq, a.n_draft, a.tree_mask,
+                                                                 a.err);
+        count_launch();
+        cudaError_t e0 = cudaGetLastError();
+        if (e0 != cudaSuccess) return e0;
+    }
     const bool both = a.n_tc_units > 0 && a.n_units > 0;
     thread_local SideStream side;
     cudaStream_t mma_stream = stream;

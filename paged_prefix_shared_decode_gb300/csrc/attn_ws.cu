@@ -180,21 +180,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-__device__ uint64_t ws_ancestor_mask(const int32_t *parent, int b, int i, int n, int32_t *err) {
-    uint64_t m = 0;
-    int j = i;
-    for (int step = 0; step < 64 && j >= 0; ++step) {
-        m |= 1ull << j;
-        const int p = __ldg(parent + (size_t)b * n + j);
-        if (p >= j || p < -1) {
-            atomicOr(err, 2);
-            break;
-        }
-        j = p;
-    }
-    return m;
-}
-
 template <int D>
 struct WsCfg {
     static constexpr int CH = D / 8;
@@ -317,7 +302,7 @@ __global__ void __launch_bounds__(kWsThreads, WsCfg<D>::MIN_BLOCKS)
         // their descriptors; warps 1-3 follow through the unit slots.
         const bool use_tma = wp.box_rows >= 32 || D == 128;
         const int pt = warp * 32 + lane;   // producer thread 0..127
-        if (pt == 0 && use_tma) {
+        if (lane == 0 && use_tma) {
             asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
             asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
         }
@@ -371,18 +356,21 @@ __global__ void __launch_bounds__(kWsThreads, WsCfg<D>::MIN_BLOCKS)
                 const uint32_t dV = dK + C::TILE_BYTES;
                 const uint32_t fb = bar(C::B_KV_FULL + stage);
                 if (use_tma && ntok == kTileTokens && (kt.tok0 & (wp.box_rows - 1)) == 0) {
-                    if (pt == 0) {
-                        mbar_expect_tx(fb, 2 * C::TILE_BYTES);
-                        const int nbox = kTileTokens / wp.box_rows;
+                    // the tile's (block, 64-column slab) boxes are spread over
+                    // lane 0 of the four producer warps: one issuing thread
+                    // cannot keep enough small boxes in flight
+                    constexpr int NSLAB = D / 64;
+                    const int npair = (kTileTokens / wp.box_rows) * NSLAB;
+                    if (lane == 0) {
+                        const int mine = (npair - warp + kProdWarps - 1) / kProdWarps;
+                        mbar_expect_tx(fb, (uint32_t)(mine * 2 * wp.box_rows * 128));
                         const int yoff = bs > kTileTokens ? (kt.tok0 & (bs - 1)) : 0;
-                        for (int k = 0; k < nbox; ++k) {
+                        for (int pr = warp; pr < npair; pr += kProdWarps) {
+                            const int k = pr / NSLAB, cb = pr % NSLAB;
                             const int y = (row_base_lh + kt.blk[k] * a.Hkv) * bs + yoff;
-#pragma unroll
-                            for (int cb = 0; cb < D / 64; ++cb) {
-                                const uint32_t off = cb * (kTileTokens * 128) + k * wp.box_rows * 128;
-                                tma_load_2d(dK + off, &kmap, cb * 64, y, fb);
-                                tma_load_2d(dV + off, &vmap, cb * 64, y, fb);
-                            }
+                            const uint32_t off = cb * (kTileTokens * 128) + k * wp.box_rows * 128;
+                            tma_load_2d(dK + off, &kmap, cb * 64, y, fb);
+                            tma_load_2d(dV + off, &vmap, cb * 64, y, fb);
                         }
                     } else {
                         mbar_arrive(fb);
@@ -517,8 +505,7 @@ __global__ void __launch_bounds__(kWsThreads, WsCfg<D>::MIN_BLOCKS)
             int qt = 0;
             if (has) qt = __ldg(a.members + it.member_off + mem);
             uint64_t tmask = ~0ull;
-            if (has && a.tree_parent)
-                tmask = ws_ancestor_mask(a.tree_parent, qt / a.n_draft, qt % a.n_draft, a.n_draft, a.err);
+            if (has && a.tree_mask) tmask = a.tree_mask[qt];
             tmask >>= 32 * half;
 
             // Q: half a row per thread (zero for padding rows), once the previous

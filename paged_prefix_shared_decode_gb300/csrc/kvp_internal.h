@@ -63,6 +63,7 @@ struct AttnLaunch {
     float scale_log2;
     const int32_t *tree_parent;   // null for decode
     int32_t n_draft;
+    uint64_t *tree_mask;          // per query token: ancestor-or-self bits (verify only)
     void *out;
     float *lse;
     // workspace views

@@ -123,6 +123,7 @@ struct HostPlan {
     std::vector<MergeDesc> merge;
     std::vector<int32_t> entries;
     int32_t n_row_tiles = 0, n_partial_rows = 0, n_units = 0, n_tc_units = 0;
+    int32_t n_tree_q = 0;   // query tokens with a draft-tree mask (verify)
     int64_t unique_kv_bytes = 0;
 };
 
@@ -365,6 +366,7 @@ int build_verify(const kvp_attn_desc &d, const int32_t *tables, const int32_t *c
     }
     finish(hp, protos, G, B * n, d.num_layers * d.num_kv_heads, sms, attention_ctas_per_sm(d.head_dim),
            tc_usable(d) ? tc_row_threshold(d.head_dim) : INT32_MAX);
+    hp.n_tree_q = B * n;
     return KVP_OK;
 }
 
@@ -387,7 +389,7 @@ int log2_int(int32_t x) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t items, tc_items, tiles, members, merge, entries, part_o, part_lse, total, plan_bytes;
+    size_t items, tc_items, tiles, members, merge, entries, part_o, part_lse, tree_mask, total, plan_bytes;
 };
 
 WsLayout layout(const HostPlan &hp, const kvp_attn_desc &d) {
@@ -403,6 +405,7 @@ WsLayout layout(const HostPlan &hp, const kvp_attn_desc &d) {
     const size_t lh = (size_t)d.num_layers * d.num_kv_heads * (size_t)hp.n_partial_rows;
     w.part_o = off;  off = align256(off + sizeof(float) * lh * d.head_dim);
     w.part_lse = off; off = align256(off + sizeof(float) * lh);
+    w.tree_mask = off; off = align256(off + sizeof(uint64_t) * (size_t)hp.n_tree_q);
     w.total = off;
     return w;
 }
@@ -463,6 +466,7 @@ int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k
     a.entries = (const int32_t *)(base + w.entries);
     a.part_o = (float *)(base + w.part_o);
     a.part_lse = (float *)(base + w.part_lse);
+    a.tree_mask = parent ? (uint64_t *)(base + w.tree_mask) : nullptr;
     a.n_units = hp.n_units;
     a.n_tc_units = hp.n_tc_units;
     a.n_merge_q = hp.n_partial_rows > 0 ? nq : 0;
