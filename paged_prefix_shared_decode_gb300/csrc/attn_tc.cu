@@ -1,0 +1,817 @@
+// Paged attention on the 5th-generation tensor cores (tcgen05 + TMA,
+// sm_103a) for work items with more than 32 query rows: shared-prefix
+// segments read by many sequences, MCTS tree levels and draft-tree
+// verification.
+//
+// One persistent CTA of 13 warps per SM.  A work unit is (item, layer, kv
+// head): up to 128 query rows (the item's members x the GQA group of the kv
+// head) against the item's 64-token KV tiles, taken two at a time as
+// 128-token steps.
+//   warps 0-1   K producers, warps 2-3 V producers.  Each pair fills its own
+//               ring, since K is released as soon as S = Q K^T is computed
+//               and V only once P V is.  Whole tiles whose blocks start on a
+//               box boundary are copied by TMA (cp.async.bulk.tensor, one box
+//               per block and 64-column slab, 128-byte swizzle, issued by
+//               lane 0 of both warps of the pair); ragged tiles by cp.async
+//               (16-byte chunks, same swizzle, zero fill).  Warp 0 claims
+//               units from an atomic counter and stages their tile
+//               descriptors in shared memory; the V pair also loads each
+//               unit's Q as soon as the previous unit's last S is done.
+//   warp 4      MMA issuer (one thread): S_g = Q K^T (M=128, N=128, K=d) into
+//               TMEM buffer g = step parity, and O_g += P_g V (M=128, N=d,
+//               K=128) with P_g read from TMEM.
+//   warps 5-8   softmax group 0 (even steps), warps 9-12 group 1 (odd
+//               steps), one thread per query row.  Each group keeps its own
+//               running max m_g, sum l_g and accumulator O_g, so while one
+//               group turns step t's scores into P the tensor cores run the
+//               other group's P V and next S.  The two groups' (m, l, O) are
+//               merged when the unit ends.
+// P (bf16 pairs) overwrites the S columns it came from, so it never passes
+// through shared memory.  The running max is raised only when a step's max
+// exceeds it by more than 8 (factor 256); O_g is then rescaled in TMEM.
+// Every wait is bounded; on a timeout the CTA sets bit 4 of the workspace
+// error word, all roles leave their loops and TMEM is freed.
+//
+// TMEM columns: S_0 [0, 128), S_1 [128, 256), O_0 [256, 256 + d),
+// O_1 [256 + d, 256 + 2d).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "kvp_internal.h"
+
+namespace kvp {
+namespace {
+
+constexpr int kProdWarps = 4;        // warps 0-1: K, warps 2-3: V
+constexpr int kMmaWarp = 4;
+constexpr int kSoftWarp0 = 5;        // warps 5-8: group 0, 9-12: group 1
+constexpr int kTcThreads = 416;      // 13 warps
+constexpr int kPairThreads = 64;     // threads of one producer pair
+constexpr int kSoftThreads = 256;
+constexpr int kGroupThreads = 128;
+constexpr int kStepTokens = 2 * kTileTokens;
+constexpr int kTmemCols = 512;
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ uint32_t saddr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                 "r"(src_bytes));
+}
+// arrives on the barrier once every earlier cp.async of this thread has landed
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ float exp2_sfu(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ---- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+// adds expected transaction bytes without arriving
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// ---- fences and barriers
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+// Named barrier 1 over the 256 softmax threads with an OR reduction, so that
+// all of them take the same branch.
+__device__ __forceinline__ bool soft_bar_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 q, %1, 0;\nbar.red.or.pred p, 1, 256, q;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+// ---- tcgen05
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;   // descriptor version
+    d |= (uint64_t)2 << 61;   // 128-byte swizzle
+    return d;
+}
+// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, A K-major,
+// B K-major (or MN-major), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// D (TMEM) (+)= A (shared memory) * B (shared memory)
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+// D (TMEM) (+)= A (TMEM) * B (shared memory)
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+        : "memory");
+}
+
+#define KVP_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
+                  "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+#define KVP_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), \
+                  "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : KVP_R8(0), KVP_R8(8), KVP_R8(16), KVP_R8(24)
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+        KVP_W8(0), KVP_W8(8), KVP_W8(16), KVP_W8(24)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
+                 KVP_W8(0)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+template <int D>
+struct TcCfg {
+    static constexpr int NSLAB = D / 64;               // 64-column slabs (128-byte rows)
+    static constexpr int CH = D / 8;                   // 16-byte chunks per row
+    static constexpr int SLAB = kStepTokens * 128;     // one slab of a 128-row operand
+    static constexpr int OPER = NSLAB * SLAB;          // Q, or K (V) of one step
+    static constexpr int NK = D == 64 ? 6 : 3;         // K ring depth (steps)
+    static constexpr int NV = D == 64 ? 6 : 2;         // V ring depth (steps)
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = Q_OFF + OPER;
+    static constexpr int V_OFF = K_OFF + NK * OPER;
+    static constexpr int DESC_OFF = V_OFF + NV * OPER;                                // [2][kMaxItemTiles]
+    static constexpr int ML_OFF = DESC_OFF + 2 * kMaxItemTiles * (int)sizeof(KvTile);  // [2][128] float2
+    static constexpr int UNIT_OFF = ML_OFF + 2 * 128 * 8;                           // [2] ints
+    static constexpr int BAR_OFF = UNIT_OFF + 16;
+    static constexpr int B_UNIT_FULL = 0, B_UNIT_EMPTY = 2, B_K_FULL = 4, B_K_EMPTY = B_K_FULL + NK,
+                         B_V_FULL = B_K_EMPTY + NK, B_V_EMPTY = B_V_FULL + NV, B_S_FULL = B_V_EMPTY + NV,
+                         B_P_FULL = B_S_FULL + 2, B_Q_FULL = B_P_FULL + 2, B_Q_EMPTY = B_Q_FULL + 1,
+                         B_O_FULL = B_Q_EMPTY + 1, B_O_EMPTY = B_O_FULL + 1, N_BARS = B_O_EMPTY + 1;
+    static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;   // tmem address, abort flag
+    static constexpr int SMEM = MISC_OFF + 16 + 1024;       // + slack to align the base to 1024
+    static constexpr int S_COL = 0, O_COL = 2 * kStepTokens;
+};
+static_assert(TcCfg<64>::SMEM <= 227 * 1024 && TcCfg<128>::SMEM <= 227 * 1024, "shared memory");
+
+// byte offset of 16-byte chunk c of row `row` in a 128-row operand
+// ([slab][row][128 B], 128-byte swizzle)
+__device__ __forceinline__ uint32_t swz(int row, int c) {
+    return (uint32_t)((c >> 3) * (kStepTokens * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+}
+
+// Valid columns j0 .. j0+31 of a 64-token tile for one row, as bits: those
+// before the row's valid count nv (0 outside the tile's member interval)
+// and, in a draft-tree tile, ancestors-or-self only.
+__device__ __forceinline__ uint32_t valid_bits(int nv, bool tree, uint64_t tmask, int j0) {
+    uint32_t vm = nv >= j0 + 32 ? 0xffffffffu : (nv <= j0 ? 0u : (1u << (nv - j0)) - 1u);
+    if (tree) vm &= (uint32_t)(tmask >> j0);
+    return vm;
+}
+// Max of the valid scores among 32 (-inf if none).  Masking uses selects, not
+// per-element branches, and is skipped when the whole warp is unmasked.
+__device__ __forceinline__ float max32(const uint32_t (&x)[32], uint32_t vm) {
+    float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+    if (__all_sync(0xffffffffu, vm == 0xffffffffu)) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            a0 = fmaxf(a0, __uint_as_float(x[j]));
+            a1 = fmaxf(a1, __uint_as_float(x[j + 1]));
+            a2 = fmaxf(a2, __uint_as_float(x[j + 2]));
+            a3 = fmaxf(a3, __uint_as_float(x[j + 3]));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            a0 = fmaxf(a0, (vm >> j) & 1u ? __uint_as_float(x[j]) : -INFINITY);
+            a1 = fmaxf(a1, (vm >> (j + 1)) & 1u ? __uint_as_float(x[j + 1]) : -INFINITY);
+            a2 = fmaxf(a2, (vm >> (j + 2)) & 1u ? __uint_as_float(x[j + 2]) : -INFINITY);
+            a3 = fmaxf(a3, (vm >> (j + 3)) & 1u ? __uint_as_float(x[j + 3]) : -INFINITY);
+        }
+    }
+    return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+}
+// p = 2^(s * sc + nm) for scores j0 .. j0+15 (0 where invalid), packed as 8
+// bf16 pairs; adds the sum of p to sum
+__device__ __forceinline__ void exp_pack16(const uint32_t (&x)[32], int j0, float sc, float nm,
+                                           uint32_t vm, uint32_t *p, float &sum) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+        float e0 = exp2_sfu(fmaf(__uint_as_float(x[j0 + j]), sc, nm));
+        float e1 = exp2_sfu(fmaf(__uint_as_float(x[j0 + j + 1]), sc, nm));
+        float e2 = exp2_sfu(fmaf(__uint_as_float(x[j0 + j + 2]), sc, nm));
+        float e3 = exp2_sfu(fmaf(__uint_as_float(x[j0 + j + 3]), sc, nm));
+        e0 = (vm >> (j0 + j)) & 1u ? e0 : 0.f;
+        e1 = (vm >> (j0 + j + 1)) & 1u ? e1 : 0.f;
+        e2 = (vm >> (j0 + j + 2)) & 1u ? e2 : 0.f;
+        e3 = (vm >> (j0 + j + 3)) & 1u ? e3 : 0.f;
+        s0 += e0 + e1;
+        s1 += e2 + e3;
+        p[j / 2] = pack_bf16x2(e0, e1);
+        p[j / 2 + 1] = pack_bf16x2(e2, e3);
+    }
+    sum += s0 + s1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                   const AttnLaunch a, const int box_rows) {
+    using C = TcCfg<D>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    KvTile *s_desc = reinterpret_cast<KvTile *>(smem + C::DESC_OFF);
+    float2 *s_ml = reinterpret_cast<float2 *>(smem + C::ML_OFF);
+    volatile int *s_unit = reinterpret_cast<volatile int *>(smem + C::UNIT_OFF);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+    const uint32_t bar0 = saddr(smem + C::BAR_OFF);
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(C::B_UNIT_FULL + s), 1);
+            // unit slot free: MMA thread + softmax threads + producer warps 1-3
+            mbar_init(bar(C::B_UNIT_EMPTY + s), 1 + kSoftThreads + (kProdWarps - 1));
+            mbar_init(bar(C::B_S_FULL + s), 1);
+            mbar_init(bar(C::B_P_FULL + s), kGroupThreads);
+        }
+        for (int s = 0; s < C::NK; ++s) {
+            mbar_init(bar(C::B_K_FULL + s), kPairThreads);
+            mbar_init(bar(C::B_K_EMPTY + s), 1);
+        }
+        for (int s = 0; s < C::NV; ++s) {
+            mbar_init(bar(C::B_V_FULL + s), kPairThreads);
+            mbar_init(bar(C::B_V_EMPTY + s), 1);
+        }
+        mbar_init(bar(C::B_Q_FULL), kPairThreads);
+        mbar_init(bar(C::B_Q_EMPTY), 1);
+        mbar_init(bar(C::B_O_FULL), 1);
+        mbar_init(bar(C::B_O_EMPTY), kSoftThreads);
+        *s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                         saddr(s_tmem)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem = *s_tmem;
+
+    // bounded wait; on a timeout the whole CTA aborts
+    auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+        for (uint32_t i = 0; i < kWaitLimit; ++i) {
+            if (mbar_try_wait(b, parity)) return true;
+            if ((i & 1023) == 1023 && *s_abort) return false;
+        }
+        *s_abort = 1;
+        atomicOr(a.err, 4);
+        return false;
+    };
+
+    const int n_items = a.n_tc_units / (a.L * a.Hkv);
+    const int G = a.G;
+    const uint32_t q_smem = saddr(smem + C::Q_OFF);
+    const uint32_t k_smem = saddr(smem + C::K_OFF);
+    const uint32_t v_smem = saddr(smem + C::V_OFF);
+    const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(a.q);
+
+    if (warp < kProdWarps) {
+        // ------------------------------------------------------------ producers
+        const bool is_v = warp >= 2;
+        const int pw = warp & 1;                 // warp within the pair
+        const int pt = pw * 32 + lane;           // thread within the pair
+        const __nv_bfloat16 *pool = static_cast<const __nv_bfloat16 *>(is_v ? a.v_pool : a.k_pool);
+        const CUtensorMap *map = is_v ? &vmap : &kmap;
+        const int nring = is_v ? C::NV : C::NK;
+        const int b_full = is_v ? C::B_V_FULL : C::B_K_FULL;
+        const int b_empty = is_v ? C::B_V_EMPTY : C::B_K_EMPTY;
+        const uint32_t ring = is_v ? v_smem : k_smem;
+        const int bs_log2 = a.bs_log2, bs = 1 << bs_log2;
+        const size_t head_stride = (size_t)D << bs_log2;
+        const size_t block_stride = (size_t)a.Hkv * head_stride;
+        // TMA for whole tiles when a box is at least 4 KB (d = 128, or blocks
+        // of 32+ tokens); below that, cp.async moves 2 KB blocks faster
+        const bool use_tma = box_rows >= 32 || D == 128;
+        if (lane == 0 && use_tma)
+            asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+        // lane 0 waits (acquire) and the warp follows it (__syncwarp orders memory)
+        auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
+            int ok = 1;
+            if (lane == 0) ok = wait(b, parity) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();
+            return ok != 0;
+        };
+        uint32_t g = 0;   // steps filled
+        for (int uc = 0;; ++uc) {
+            const int slot = uc & 1;
+            int unit = -1;
+            if (warp == 0) {
+                bool ok = wait_warp(bar(C::B_UNIT_EMPTY + slot), ((uc >> 1) & 1) ^ 1);
+                if (lane == 0) unit = atomicAdd(a.tc_counter, 1);
+                unit = __shfl_sync(0xffffffffu, unit, 0);
+                const bool done = !ok || unit >= a.n_tc_units || __shfl_sync(0xffffffffu, *s_abort, 0);
+                if (!done) {
+                    const WorkItem it = a.tc_items[unit % n_items];
+                    const int ntile = it.tile_end - it.tile_begin;
+                    const int4 *src = reinterpret_cast<const int4 *>(a.tiles + it.tile_begin);
+                    int4 *dst = reinterpret_cast<int4 *>(s_desc + slot * kMaxItemTiles);
+                    for (int i = lane; i < ntile * 2; i += 32) dst[i] = src[i];
+                }
+                if (lane == 0) s_unit[slot] = done ? -1 : unit;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_UNIT_FULL + slot));
+                if (done) break;
+            } else {
+                const bool ok = wait_warp(bar(C::B_UNIT_FULL + slot), (uc >> 1) & 1);
+                unit = ok ? s_unit[slot] : -1;
+                if (unit < 0) break;
+            }
+            const int item_idx = unit % n_items;
+            const int lk = unit / n_items;
+            const int kvh = lk % a.Hkv, l = lk / a.Hkv;
+            const WorkItem it = a.tc_items[item_idx];
+            const int ntile = it.tile_end - it.tile_begin;
+            const int nsteps = (ntile + 1) >> 1;
+            const size_t layer_base = (size_t)l * a.NB * block_stride + (size_t)kvh * head_stride;
+            const int row_base_lh = (l * a.NB) * a.Hkv + kvh;   // row of block b = (row_base_lh + b*Hkv) * bs
+            const KvTile *tiles = s_desc + slot * kMaxItemTiles;
+            bool alive = true;
+            if (is_v) {
+                // Q of this unit, once the previous unit's S MMAs are done with it
+                alive = wait_warp(bar(C::B_Q_EMPTY), (uc & 1) ^ 1);
+                const int rows = it.n_members * G;
+#pragma unroll 4
+                for (int x = pt; x < 128 * C::CH; x += kPairThreads) {
+                    const int r = x / C::CH, c = x % C::CH;
+                    const __nv_bfloat16 *src = qb;
+                    if (r < rows) {
+                        const int qt = __ldg(a.members + it.member_off + r / G);
+                        src = qb + (((size_t)l * a.nq + qt) * a.Hq + kvh * G + r % G) * D + c * 8;
+                    }
+                    cp_async16(q_smem + swz(r, c), src, r < rows ? 16 : 0);
+                }
+                cp_async_arrive(bar(C::B_Q_FULL));
+            }
+            for (int t = 0; alive && t < nsteps; ++t, ++g) {
+                const int st = g % nring;
+                if (!wait_warp(bar(b_empty + st), ((g / nring) & 1) ^ 1)) { alive = false; break; }
+                const uint32_t dst = ring + st * C::OPER;
+                const uint32_t fb = bar(b_full + st);
+                for (int h = 0; h < 2 && 2 * t + h < ntile; ++h) {
+                    const KvTile &kt = tiles[2 * t + h];
+                    const int ntok = kt.ntok_flags & 0xFFFF;
+                    if (use_tma && ntok == kTileTokens && (kt.tok0 & (box_rows - 1)) == 0) {
+                        if (lane == 0) {
+                            // this half's (block, slab) boxes, split over the pair
+                            const int nbox = (kTileTokens / box_rows) * C::NSLAB;
+                            const int mine = (nbox - pw + 1) / 2;
+                            mbar_expect_tx(fb, (uint32_t)(mine * box_rows * 128));
+                            const int yoff = bs > kTileTokens ? (kt.tok0 & (bs - 1)) : 0;
+                            for (int bx = pw; bx < nbox; bx += 2) {
+                                const int k = bx / C::NSLAB, cb = bx % C::NSLAB;
+                                const int y = (row_base_lh + kt.blk[k] * a.Hkv) * bs + yoff;
+                                tma_load_2d(dst + cb * C::SLAB + (h * kTileTokens + k * box_rows) * 128, map,
+                                            cb * 64, y, fb);
+                            }
+                        }
+                        continue;
+                    }
+                    const int jb = kt.tok0 >> bs_log2;
+#pragma unroll 4
+                    for (int x = pt; x < kTileTokens * C::CH; x += kPairThreads) {
+                        const int tok = x / C::CH, c = x % C::CH;
+                        const __nv_bfloat16 *src = pool;
+                        int bytes = 0;
+                        if (tok < ntok) {
+                            const int pos = kt.tok0 + tok;
+                            const int blk = kt.blk[(pos >> bs_log2) - jb];
+                            if ((unsigned)blk < (unsigned)a.NB) {
+                                src = pool + layer_base + (size_t)blk * block_stride +
+                                      (size_t)(pos & (bs - 1)) * D + c * 8;
+                                bytes = 16;
+                            } else if (c == 0) {
+                                atomicOr(a.err, 1);
+                            }
+                        }
+                        cp_async16(dst + swz(h * kTileTokens + tok, c), src, bytes);
+                    }
+                }
+                cp_async_arrive(fb);
+            }
+            if (warp != 0 && lane == 0) mbar_arrive(bar(C::B_UNIT_EMPTY + slot));
+            if (!alive || __shfl_sync(0xffffffffu, *s_abort, 0)) {
+                // let the consumers see the end
+                if (warp == 0 && lane == 0) {
+                    const int s2 = (uc + 1) & 1;
+                    s_unit[s2] = -1;
+                    mbar_arrive(bar(C::B_UNIT_FULL + s2));
+                }
+                break;
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16(128, kStepTokens, false);
+            constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
+            uint32_t gk = 0, gv = 0;        // steps taken from the K / V rings
+            uint32_t np0 = 0, np1 = 0;      // P_FULL phases consumed per group
+            for (int uc = 0;; ++uc) {
+                const int slot = uc & 1;
+                if (!wait(bar(C::B_UNIT_FULL + slot), (uc >> 1) & 1)) break;
+                const int unit = s_unit[slot];
+                if (unit < 0) break;
+                const WorkItem it = a.tc_items[unit % n_items];
+                const int ntile = it.tile_end - it.tile_begin;
+                const int nsteps = (ntile + 1) >> 1;
+                bool ok = wait(bar(C::B_Q_FULL), uc & 1);
+                // Q was written through the generic proxy (cp.async)
+                fence_async_smem();
+                tc_after();
+                auto issue_s = [&](int t) -> bool {
+                    const uint32_t g = gk + t, st = g % C::NK;
+                    if (!wait(bar(C::B_K_FULL + st), (g / C::NK) & 1)) return false;
+                    fence_async_smem();
+                    tc_after();
+                    const uint32_t kst = k_smem + st * C::OPER;
+                    const uint32_t d_tm = tmem + C::S_COL + (t & 1) * kStepTokens;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t o = (uint32_t)(k >> 2) * C::SLAB + (uint32_t)(k & 3) * 32;
+                        umma_ss(d_tm, sdesc(q_smem + o, 16, 1024), sdesc(kst + o, 16, 1024), IDESC_S,
+                                k > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bar(C::B_S_FULL + (t & 1)));
+                    umma_commit(bar(C::B_K_EMPTY + st));
+                    if (t == nsteps - 1) umma_commit(bar(C::B_Q_EMPTY));
+                    return true;
+                };
+                if (ok && nsteps > 0) ok = issue_s(0);
+                if (ok && nsteps > 1) ok = issue_s(1);
+                // the previous unit's epilogue has read O_0 and O_1
+                if (ok) ok = wait(bar(C::B_O_EMPTY), (uc & 1) ^ 1);
+                tc_after();
+                for (int t = 0; ok && t < nsteps; ++t) {
+                    const int grp = t & 1;
+                    if (!wait(bar(C::B_P_FULL + grp), (grp ? np1 : np0) & 1)) { ok = false; break; }
+                    if (grp) ++np1; else ++np0;
+                    const uint32_t g = gv + t, st = g % C::NV;
+                    if (!wait(bar(C::B_V_FULL + st), (g / C::NV) & 1)) { ok = false; break; }
+                    fence_async_smem();
+                    tc_after();
+                    const uint32_t vst = v_smem + st * C::OPER;
+                    // an odd last tile leaves rows 64..127 of V unwritten: skip them
+                    const int ksteps = 2 * t + 1 < ntile ? kStepTokens / 16 : kTileTokens / 16;
+                    for (int k = 0; k < ksteps; ++k)
+                        umma_ts(tmem + C::O_COL + grp * D, tmem + C::S_COL + grp * kStepTokens + k * 8,
+                                sdesc(vst + k * 2048, C::SLAB, 1024), IDESC_PV, (t >= 2 || k > 0) ? 1u : 0u);
+                    umma_commit(bar(C::B_V_EMPTY + st));
+                    if (t + 2 < nsteps && !issue_s(t + 2)) { ok = false; break; }
+                }
+                if (!ok) break;
+                if (nsteps == 0) umma_commit(bar(C::B_Q_EMPTY));
+                gk += nsteps;
+                gv += nsteps;
+                umma_commit(bar(C::B_O_FULL));
+                mbar_arrive(bar(C::B_UNIT_EMPTY + slot));
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int grp = (warp - kSoftWarp0) >> 2;
+        const int quarter = warp & 3;             // TMEM lanes this warp may access
+        const int r = quarter * 32 + lane;        // query row in the unit
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t s_tm = tmem + lane_base + C::S_COL + grp * kStepTokens;
+        const uint32_t o_tm = tmem + lane_base + C::O_COL;
+        const float sc = a.scale_log2;
+        uint32_t ns = 0;   // S_FULL phases consumed by this group
+        for (int uc = 0;; ++uc) {
+            const int slot = uc & 1;
+            bool ok = wait(bar(C::B_UNIT_FULL + slot), (uc >> 1) & 1);
+            const int unit = ok ? s_unit[slot] : -1;
+            if (soft_bar_or(!ok || unit < 0 || *s_abort)) break;
+            const int item_idx = unit % n_items;
+            const int lk = unit / n_items;
+            const int kvh = lk % a.Hkv, l = lk / a.Hkv;
+            const WorkItem it = a.tc_items[item_idx];
+            const int ntile = it.tile_end - it.tile_begin;
+            const int nsteps = (ntile + 1) >> 1;
+            const KvTile *tiles = s_desc + slot * kMaxItemTiles;
+            const int rows = it.n_members * G;
+            const bool has = r < rows;
+            const int mem = r / G;
+            int qt = 0;
+            if (has) qt = __ldg(a.members + it.member_off + mem);
+            const uint64_t tmask = has && a.tree_mask ? a.tree_mask[qt] : ~0ull;
+
+            float m = -INFINITY, lsum = 0.f;
+            for (int t = grp; t < nsteps; t += 2) {
+                ok = wait(bar(C::B_S_FULL + grp), ns & 1) && ok;
+                ns += 1;
+                tc_after();
+                int nv0 = 0, nv1 = 0;
+                bool tr0 = false, tr1 = false;
+                {
+                    const KvTile &k0 = tiles[2 * t];
+                    const int mlo = k0.members & 0xFFFF, mhi = k0.members >> 16;
+                    nv0 = has && mem >= mlo && mem < mhi ? (k0.ntok_flags & 0xFFFF) : 0;
+                    tr0 = (k0.ntok_flags >> 16) & kTileTree;
+                }
+                if (2 * t + 1 < ntile) {
+                    const KvTile &k1 = tiles[2 * t + 1];
+                    const int mlo = k1.members & 0xFFFF, mhi = k1.members >> 16;
+                    nv1 = has && mem >= mlo && mem < mhi ? (k1.ntok_flags & 0xFFFF) : 0;
+                    tr1 = (k1.ntok_flags >> 16) & kTileTree;
+                }
+                uint32_t x[32], y[32];
+                // row max of the low tile's scores, then the high tile's (kept)
+                tmem_ld32(s_tm, x);
+                tmem_ld32(s_tm + 32, y);
+                tmem_wait_ld();
+                float mx = fmaxf(max32(x, valid_bits(nv0, tr0, tmask, 0)), max32(y, valid_bits(nv0, tr0, tmask, 32)));
+                tmem_ld32(s_tm + 64, x);
+                tmem_ld32(s_tm + 96, y);
+                tmem_wait_ld();
+                mx = fmaxf(mx, fmaxf(max32(x, valid_bits(nv1, tr1, tmask, 0)), max32(y, valid_bits(nv1, tr1, tmask, 32))));
+                // scale > 0: max of scaled scores = scale * max of raw scores
+                const float tmx = mx * sc;
+                const bool up = m == -INFINITY ? tmx != -INFINITY : tmx > m + 8.f;
+                const bool resc = up && m != -INFINITY;
+                if (__any_sync(0xffffffffu, resc)) {
+                    // O_g holds P V up to step t-2, complete since S(t) is
+                    const float f = resc ? exp2_sfu(m - tmx) : 1.f;
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        tmem_ld32(o_tm + grp * D + c0, x);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) x[j] = __float_as_uint(__uint_as_float(x[j]) * f);
+                        tmem_st32(o_tm + grp * D + c0, x);
+                    }
+                    tmem_wait_st();
+                    lsum *= f;
+                }
+                if (up) m = tmx;
+                // p = 2^(s * scale - m): one FFMA and one SFU op per score.
+                // P column i holds the pair of scores 2i, 2i + 1; every store
+                // lands on columns whose scores are already in registers.
+                const float nm = m == -INFINITY ? 0.f : -m;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    tmem_ld32(s_tm + 64 * hh, x);
+                    tmem_ld32(s_tm + 64 * hh + 32, y);
+                    tmem_wait_ld();
+                    const uint32_t vx = valid_bits(hh ? nv1 : nv0, hh ? tr1 : tr0, tmask, 0);
+                    const uint32_t vy = valid_bits(hh ? nv1 : nv0, hh ? tr1 : tr0, tmask, 32);
+                    uint32_t pk[8];
+                    exp_pack16(x, 0, sc, nm, vx, pk, lsum);
+                    tmem_st8(s_tm + 32 * hh, pk);
+                    exp_pack16(x, 16, sc, nm, vx, pk, lsum);
+                    tmem_st8(s_tm + 32 * hh + 8, pk);
+                    exp_pack16(y, 0, sc, nm, vy, pk, lsum);
+                    tmem_st8(s_tm + 32 * hh + 16, pk);
+                    exp_pack16(y, 16, sc, nm, vy, pk, lsum);
+                    tmem_st8(s_tm + 32 * hh + 24, pk);
+                }
+                tmem_wait_st();
+                tc_before();
+                mbar_arrive(bar(C::B_P_FULL + grp));
+            }
+            // epilogue: merge the two groups' (m, l, O) and write
+            ok = wait(bar(C::B_O_FULL), uc & 1) && ok;
+            tc_after();
+            s_ml[grp * 128 + r] = make_float2(m, lsum);
+            if (soft_bar_or(!ok || *s_abort)) break;
+            const float2 a0 = s_ml[r], a1 = s_ml[128 + r];
+            const float c = fmaxf(a0.x, a1.x);
+            const float f0 = a0.x == -INFINITY ? 0.f : exp2_sfu(a0.x - c);
+            const float f1 = a1.x == -INFINITY ? 0.f : exp2_sfu(a1.x - c);
+            const float ltot = a0.y * f0 + a1.y * f1;
+            const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
+            const float lse2 = ltot > 0.f ? c + __log2f(ltot) : -INFINITY;
+            const float w0 = f0 * inv, w1 = f1 * inv;
+            const bool write = has && nsteps > 0;
+#pragma unroll
+            for (int c0 = grp * (D / 2); c0 < (grp + 1) * (D / 2); c0 += 32) {
+                uint32_t x[32], y[32];
+                tmem_ld32(o_tm + c0, x);
+                tmem_ld32(o_tm + D + c0, y);
+                tmem_wait_ld();
+                if (!write) continue;
+                // a group with no steps (or no valid key) has weight 0 and an
+                // O that was never written: select, do not multiply
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float v0 = w0 != 0.f ? __uint_as_float(x[j]) * w0 : 0.f;
+                    const float v1 = w1 != 0.f ? __uint_as_float(y[j]) * w1 : 0.f;
+                    x[j] = __float_as_uint(v0 + v1);
+                }
+                if (it.out_base < 0) {
+                    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
+                                         (((size_t)l * a.nq + qt) * a.Hq + kvh * G + r % G) * D + c0;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(x[j]), __uint_as_float(x[j + 1]));
+                        v.y = pack_bf16x2(__uint_as_float(x[j + 2]), __uint_as_float(x[j + 3]));
+                        v.z = pack_bf16x2(__uint_as_float(x[j + 4]), __uint_as_float(x[j + 5]));
+                        v.w = pack_bf16x2(__uint_as_float(x[j + 6]), __uint_as_float(x[j + 7]));
+                        *reinterpret_cast<uint4 *>(dst + j) = v;
+                    }
+                } else {
+                    float *dst = a.part_o + (((size_t)l * a.Hkv + kvh) * a.P + it.out_base + r) * D + c0;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(dst + j) =
+                            make_float4(__uint_as_float(x[j]), __uint_as_float(x[j + 1]),
+                                        __uint_as_float(x[j + 2]), __uint_as_float(x[j + 3]));
+                }
+            }
+            if (write && grp == 0) {
+                if (it.out_base < 0) {
+                    if (a.lse) a.lse[((size_t)l * a.nq + qt) * a.Hq + kvh * G + r % G] = lse2 * 0.6931471805599453f;
+                } else {
+                    a.part_lse[((size_t)l * a.Hkv + kvh) * a.P + it.out_base + r] = lse2;
+                }
+            }
+            tc_before();
+            mbar_arrive(bar(C::B_O_EMPTY));
+            mbar_arrive(bar(C::B_UNIT_EMPTY + slot));
+        }
+    }
+    tc_before();
+    __syncthreads();
+    tc_after();
+    if (warp == kMmaWarp)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+}
+
+// ------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D view of a pool: rows = L*NB*Hkv*bs token rows of d bf16; box = 64
+// columns x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *pool, int D, long long rows, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides, box,
+                    es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct TcOcc {
+    int sms = 0;
+    bool ok = false;
+};
+
+template <int D>
+TcOcc &tc_occ() {
+    static TcOcc occ;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return;
+        if (cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 TcCfg<D>::SMEM) != cudaSuccess)
+            return;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return;
+        occ.sms = sms;
+        occ.ok = true;
+    });
+    return occ;
+}
+
+template <int D>
+cudaError_t launch_tc_d(const AttnLaunch &a, cudaStream_t stream) {
+    TcOcc &occ = tc_occ<D>();
+    if (!occ.ok) return cudaErrorInvalidDevice;
+    const int bs = 1 << a.bs_log2;
+    const int box_rows = bs < kTileTokens ? bs : kTileTokens;
+    const long long rows = (long long)a.L * a.NB * a.Hkv * bs;
+    alignas(64) CUtensorMap km, vm;
+    if (!make_map(&km, a.k_pool, D, rows, box_rows) || !make_map(&vm, a.v_pool, D, rows, box_rows))
+        return cudaErrorInvalidValue;
+    // one CTA per SM (its shared memory and TMEM allow no more)
+    const int grid = a.n_tc_units < occ.sms ? a.n_tc_units : occ.sms;
+    attn_tc_kernel<D><<<grid, kTcThreads, TcCfg<D>::SMEM, stream>>>(km, vm, a, box_rows);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_path_supported(int L, int NB, int Hkv, int bs) {
+    // TMA row coordinates are 32-bit
+    return (long long)L * NB * Hkv * bs < (1LL << 31);
+}
+
+cudaError_t launch_attention_tc(const AttnLaunch &a, cudaStream_t stream, int ctas_per_sm) {
+    (void)ctas_per_sm;
+    if (a.n_tc_units <= 0) return cudaSuccess;
+    if (a.D == 64) return launch_tc_d<64>(a, stream);
+    if (a.D == 128) return launch_tc_d<128>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kvp
