@@ -47,16 +47,17 @@
 namespace kvp {
 namespace {
 
-constexpr int kProdWarps = 4;        // warps 0-1: K, warps 2-3: V
-constexpr int kMmaWarp = 4;
-constexpr int kSoftWarp0 = 5;        // warps 5-8: group 0, 9-12: group 1
-constexpr int kTcThreads = 416;      // 13 warps
-constexpr int kPairThreads = 64;     // threads of one producer pair
+constexpr int kProdWarps = 2;        // warp 0: K, warp 1: V
+constexpr int kVWarp = 1;
+constexpr int kMmaWarp = 2;
+constexpr int kSoftWarp0 = 3;        // warps 3-6: group 0, 7-10: group 1
+constexpr int kTcThreads = 352;      // 11 warps: at most 3 per SM sub-partition
 constexpr int kSoftThreads = 256;
 constexpr int kGroupThreads = 128;
 constexpr int kStepTokens = 2 * kTileTokens;
 constexpr int kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr float kMaxSlack = 32.f;    // log2 headroom of p above the running max
 
 __device__ __forceinline__ uint32_t saddr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -260,26 +261,57 @@ __device__ __forceinline__ float max32(const uint32_t (&x)[32], uint32_t vm) {
     return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
 }
 // p = 2^(s * sc + nm) for scores j0 .. j0+15 (0 where invalid), packed as 8
-// bf16 pairs; adds the sum of p to sum
+// bf16 pairs; adds the sum of p to sum and folds the valid scores into mx
 __device__ __forceinline__ void exp_pack16(const uint32_t (&x)[32], int j0, float sc, float nm,
-                                           uint32_t vm, uint32_t *p, float &sum) {
+                                           uint32_t vm, uint32_t *p, float &sum, float &mx) {
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
     for (int j = 0; j < 16; j += 4) {
-        float e0 = exp2_sfu(fmaf(__uint_as_float(x[j0 + j]), sc, nm));
-        float e1 = exp2_sfu(fmaf(__uint_as_float(x[j0 + j + 1]), sc, nm));
-        float e2 = exp2_sfu(fmaf(__uint_as_float(x[j0 + j + 2]), sc, nm));
-        float e3 = exp2_sfu(fmaf(__uint_as_float(x[j0 + j + 3]), sc, nm));
-        e0 = (vm >> (j0 + j)) & 1u ? e0 : 0.f;
-        e1 = (vm >> (j0 + j + 1)) & 1u ? e1 : 0.f;
-        e2 = (vm >> (j0 + j + 2)) & 1u ? e2 : 0.f;
-        e3 = (vm >> (j0 + j + 3)) & 1u ? e3 : 0.f;
-        s0 += e0 + e1;
-        s1 += e2 + e3;
-        p[j / 2] = pack_bf16x2(e0, e1);
-        p[j / 2 + 1] = pack_bf16x2(e2, e3);
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[i] = (vm >> (j0 + j + i)) & 1u ? __uint_as_float(x[j0 + j + i]) : -INFINITY;
+            mx = fmaxf(mx, v[i]);
+            v[i] = exp2_sfu(fmaf(v[i], sc, nm));
+        }
+        s0 += v[0] + v[1];
+        s1 += v[2] + v[3];
+        p[j / 2] = pack_bf16x2(v[0], v[1]);
+        p[j / 2 + 1] = pack_bf16x2(v[2], v[3]);
     }
     sum += s0 + s1;
+}
+
+// P = 2^(s * sc + nm) of one step into the S columns it came from (P column
+// i holds scores 2i, 2i + 1; every store lands on columns whose scores are
+// already in registers); adds the sum of P to ls and folds the step's valid
+// raw scores into mx.
+__device__ __forceinline__ void p_pass(uint32_t s_tm, float nm, float sc, int nv0, bool tr0, int nv1, bool tr1,
+                                       uint64_t tmask, float &ls, float &mx) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        uint32_t x[32], y[32];
+        tmem_ld32(s_tm + 64 * hh, x);
+        tmem_ld32(s_tm + 64 * hh + 32, y);
+        tmem_wait_ld();
+        const uint32_t vx = valid_bits(hh ? nv1 : nv0, hh ? tr1 : tr0, tmask, 0);
+        const uint32_t vy = valid_bits(hh ? nv1 : nv0, hh ? tr1 : tr0, tmask, 32);
+        uint32_t pk[8];
+        exp_pack16(x, 0, sc, nm, vx, pk, ls, mx);
+        tmem_st8(s_tm + 32 * hh, pk);
+        exp_pack16(x, 16, sc, nm, vx, pk, ls, mx);
+        tmem_st8(s_tm + 32 * hh + 8, pk);
+        exp_pack16(y, 0, sc, nm, vy, pk, ls, mx);
+        tmem_st8(s_tm + 32 * hh + 16, pk);
+        exp_pack16(y, 16, sc, nm, vy, pk, ls, mx);
+        tmem_st8(s_tm + 32 * hh + 24, pk);
+    }
+}
+// the same, kept out of line for the rare recomputation so that its
+// registers do not add to the common path's
+__device__ __noinline__ void p_pass_slow(uint32_t s_tm, float nm, float sc, int nv0, bool tr0, int nv1, bool tr1,
+                                         uint64_t tmask, float &ls, float &mx) {
+    p_pass(s_tm, nm, sc, nv0, tr0, nv1, tr1, tmask, ls, mx);
 }
 
 template <int D>
@@ -303,20 +335,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(C::B_UNIT_FULL + s), 1);
-            // unit slot free: MMA thread + softmax threads + producer warps 1-3
-            mbar_init(bar(C::B_UNIT_EMPTY + s), 1 + kSoftThreads + (kProdWarps - 1));
+            // unit slot free: MMA thread + softmax threads + V warp
+            mbar_init(bar(C::B_UNIT_EMPTY + s), 1 + kSoftThreads + 1);
             mbar_init(bar(C::B_S_FULL + s), 1);
             mbar_init(bar(C::B_P_FULL + s), kGroupThreads);
         }
         for (int s = 0; s < C::NK; ++s) {
-            mbar_init(bar(C::B_K_FULL + s), kPairThreads);
+            mbar_init(bar(C::B_K_FULL + s), 32);
             mbar_init(bar(C::B_K_EMPTY + s), 1);
         }
         for (int s = 0; s < C::NV; ++s) {
-            mbar_init(bar(C::B_V_FULL + s), kPairThreads);
+            mbar_init(bar(C::B_V_FULL + s), 32);
             mbar_init(bar(C::B_V_EMPTY + s), 1);
         }
-        mbar_init(bar(C::B_Q_FULL), kPairThreads);
+        mbar_init(bar(C::B_Q_FULL), 32);
         mbar_init(bar(C::B_Q_EMPTY), 1);
         mbar_init(bar(C::B_O_FULL), 1);
         mbar_init(bar(C::B_O_EMPTY), kSoftThreads);
@@ -355,9 +387,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp < kProdWarps) {
         // ------------------------------------------------------------ producers
-        const bool is_v = warp >= 2;
-        const int pw = warp & 1;                 // warp within the pair
-        const int pt = pw * 32 + lane;           // thread within the pair
+        const bool is_v = warp == kVWarp;
         const __nv_bfloat16 *pool = static_cast<const __nv_bfloat16 *>(is_v ? a.v_pool : a.k_pool);
         const CUtensorMap *map = is_v ? &vmap : &kmap;
         const int nring = is_v ? C::NV : C::NK;
@@ -367,10 +397,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int bs_log2 = a.bs_log2, bs = 1 << bs_log2;
         const size_t head_stride = (size_t)D << bs_log2;
         const size_t block_stride = (size_t)a.Hkv * head_stride;
-        // TMA for whole tiles when a box is at least 4 KB (d = 128, or blocks
-        // of 32+ tokens); below that, cp.async moves 2 KB blocks faster
-        const bool use_tma = box_rows >= 32 || D == 128;
-        if (lane == 0 && use_tma)
+        // (block, 64-column slab) boxes of one 64-token tile
+        const int nbox = (kTileTokens / box_rows) * C::NSLAB;
+        if (lane == 0)
             asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
         // lane 0 waits (acquire) and the warp follows it (__syncwarp orders memory)
         auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
@@ -384,7 +413,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int uc = 0;; ++uc) {
             const int slot = uc & 1;
             int unit = -1;
-            if (warp == 0) {
+            if (!is_v) {
                 bool ok = wait_warp(bar(C::B_UNIT_EMPTY + slot), ((uc >> 1) & 1) ^ 1);
                 if (lane == 0) unit = atomicAdd(a.tc_counter, 1);
                 unit = __shfl_sync(0xffffffffu, unit, 0);
@@ -416,18 +445,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const KvTile *tiles = s_desc + slot * kMaxItemTiles;
             bool alive = true;
             if (is_v) {
-                // Q of this unit, once the previous unit's S MMAs are done with it
+                // Q of this unit, once the previous unit's S MMAs are done with
+                // it: rows lane + 32 i, whose member indices are loaded first
                 alive = wait_warp(bar(C::B_Q_EMPTY), (uc & 1) ^ 1);
                 const int rows = it.n_members * G;
-#pragma unroll 4
-                for (int x = pt; x < 128 * C::CH; x += kPairThreads) {
-                    const int r = x / C::CH, c = x % C::CH;
-                    const __nv_bfloat16 *src = qb;
-                    if (r < rows) {
-                        const int qt = __ldg(a.members + it.member_off + r / G);
-                        src = qb + (((size_t)l * a.nq + qt) * a.Hq + kvh * G + r % G) * D + c * 8;
-                    }
-                    cp_async16(q_smem + swz(r, c), src, r < rows ? 16 : 0);
+                int qt[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = lane + 32 * i;
+                    qt[i] = r < rows ? __ldg(a.members + it.member_off + r / G) : 0;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = lane + 32 * i;
+                    const __nv_bfloat16 *qrow = qb + (((size_t)l * a.nq + qt[i]) * a.Hq + kvh * G + r % G) * D;
+#pragma unroll
+                    for (int c = 0; c < C::CH; ++c)
+                        cp_async16(q_smem + swz(r, c), r < rows ? qrow + c * 8 : qb, r < rows ? 16 : 0);
                 }
                 cp_async_arrive(bar(C::B_Q_FULL));
             }
@@ -436,28 +470,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!wait_warp(bar(b_empty + st), ((g / nring) & 1) ^ 1)) { alive = false; break; }
                 const uint32_t dst = ring + st * C::OPER;
                 const uint32_t fb = bar(b_full + st);
+                // whole tiles by TMA, one box per lane; ragged ones by cp.async
+                // with zero fill past the tile's end
+                bool tma[2] = {false, false};
+                for (int h = 0; h < 2 && 2 * t + h < ntile; ++h) {
+                    const KvTile &kt = tiles[2 * t + h];
+                    tma[h] = (kt.ntok_flags & 0xFFFF) == kTileTokens && (kt.tok0 & (box_rows - 1)) == 0;
+                }
+                if (lane == 0 && (tma[0] || tma[1]))
+                    mbar_expect_tx(fb, (uint32_t)(((tma[0] ? 1 : 0) + (tma[1] ? 1 : 0)) * nbox * box_rows * 128));
+                __syncwarp();
                 for (int h = 0; h < 2 && 2 * t + h < ntile; ++h) {
                     const KvTile &kt = tiles[2 * t + h];
                     const int ntok = kt.ntok_flags & 0xFFFF;
-                    if (use_tma && ntok == kTileTokens && (kt.tok0 & (box_rows - 1)) == 0) {
-                        if (lane == 0) {
-                            // this half's (block, slab) boxes, split over the pair
-                            const int nbox = (kTileTokens / box_rows) * C::NSLAB;
-                            const int mine = (nbox - pw + 1) / 2;
-                            mbar_expect_tx(fb, (uint32_t)(mine * box_rows * 128));
+                    if (tma[h]) {
+                        if (lane < nbox) {
+                            const int k = lane / C::NSLAB, cb = lane % C::NSLAB;
                             const int yoff = bs > kTileTokens ? (kt.tok0 & (bs - 1)) : 0;
-                            for (int bx = pw; bx < nbox; bx += 2) {
-                                const int k = bx / C::NSLAB, cb = bx % C::NSLAB;
-                                const int y = (row_base_lh + kt.blk[k] * a.Hkv) * bs + yoff;
-                                tma_load_2d(dst + cb * C::SLAB + (h * kTileTokens + k * box_rows) * 128, map,
-                                            cb * 64, y, fb);
-                            }
+                            const int y = (row_base_lh + kt.blk[k] * a.Hkv) * bs + yoff;
+                            tma_load_2d(dst + cb * C::SLAB + (h * kTileTokens + k * box_rows) * 128, map, cb * 64,
+                                        y, fb);
                         }
                         continue;
                     }
                     const int jb = kt.tok0 >> bs_log2;
 #pragma unroll 4
-                    for (int x = pt; x < kTileTokens * C::CH; x += kPairThreads) {
+                    for (int x = lane; x < kTileTokens * C::CH; x += 32) {
                         const int tok = x / C::CH, c = x % C::CH;
                         const __nv_bfloat16 *src = pool;
                         int bytes = 0;
@@ -477,10 +515,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 cp_async_arrive(fb);
             }
-            if (warp != 0 && lane == 0) mbar_arrive(bar(C::B_UNIT_EMPTY + slot));
+            if (is_v && lane == 0) mbar_arrive(bar(C::B_UNIT_EMPTY + slot));
             if (!alive || __shfl_sync(0xffffffffu, *s_abort, 0)) {
                 // let the consumers see the end
-                if (warp == 0 && lane == 0) {
+                if (!is_v && lane == 0) {
                     const int s2 = (uc + 1) & 1;
                     s_unit[s2] = -1;
                     mbar_arrive(bar(C::B_UNIT_FULL + s2));
@@ -604,56 +642,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     nv1 = has && mem >= mlo && mem < mhi ? (k1.ntok_flags & 0xFFFF) : 0;
                     tr1 = (k1.ntok_flags >> 16) & kTileTree;
                 }
-                uint32_t x[32], y[32];
-                // row max of the low tile's scores, then the high tile's (kept)
-                tmem_ld32(s_tm, x);
-                tmem_ld32(s_tm + 32, y);
-                tmem_wait_ld();
-                float mx = fmaxf(max32(x, valid_bits(nv0, tr0, tmask, 0)), max32(y, valid_bits(nv0, tr0, tmask, 32)));
-                tmem_ld32(s_tm + 64, x);
-                tmem_ld32(s_tm + 96, y);
-                tmem_wait_ld();
-                mx = fmaxf(mx, fmaxf(max32(x, valid_bits(nv1, tr1, tmask, 0)), max32(y, valid_bits(nv1, tr1, tmask, 32))));
-                // scale > 0: max of scaled scores = scale * max of raw scores
-                const float tmx = mx * sc;
-                const bool up = m == -INFINITY ? tmx != -INFINITY : tmx > m + 8.f;
-                const bool resc = up && m != -INFINITY;
-                if (__any_sync(0xffffffffu, resc)) {
-                    // O_g holds P V up to step t-2, complete since S(t) is
-                    const float f = resc ? exp2_sfu(m - tmx) : 1.f;
-#pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        tmem_ld32(o_tm + grp * D + c0, x);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) x[j] = __float_as_uint(__uint_as_float(x[j]) * f);
-                        tmem_st32(o_tm + grp * D + c0, x);
-                    }
-                    tmem_wait_st();
-                    lsum *= f;
-                }
-                if (up) m = tmx;
-                // p = 2^(s * scale - m): one FFMA and one SFU op per score.
-                // P column i holds the pair of scores 2i, 2i + 1; every store
-                // lands on columns whose scores are already in registers.
-                const float nm = m == -INFINITY ? 0.f : -m;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    tmem_ld32(s_tm + 64 * hh, x);
-                    tmem_ld32(s_tm + 64 * hh + 32, y);
+                // A row's running max m is raised only when a step's scaled max
+                // exceeds it by more than kMaxSlack, so p <= 2^kMaxSlack, well
+                // inside bf16 and the fp32 sums.  A step therefore reads S once
+                // and forms P with the current m while it tracks the step's max;
+                // only a row whose max breaks the bound, or that has no m yet,
+                // takes the slow path: rescale O_g and l, form P again.
+                if (__all_sync(0xffffffffu, m == -INFINITY)) {
+                    // this group's first step of the unit: find m first
+                    uint32_t x[32], y[32];
+                    tmem_ld32(s_tm, x);
+                    tmem_ld32(s_tm + 32, y);
                     tmem_wait_ld();
-                    const uint32_t vx = valid_bits(hh ? nv1 : nv0, hh ? tr1 : tr0, tmask, 0);
-                    const uint32_t vy = valid_bits(hh ? nv1 : nv0, hh ? tr1 : tr0, tmask, 32);
-                    uint32_t pk[8];
-                    exp_pack16(x, 0, sc, nm, vx, pk, lsum);
-                    tmem_st8(s_tm + 32 * hh, pk);
-                    exp_pack16(x, 16, sc, nm, vx, pk, lsum);
-                    tmem_st8(s_tm + 32 * hh + 8, pk);
-                    exp_pack16(y, 0, sc, nm, vy, pk, lsum);
-                    tmem_st8(s_tm + 32 * hh + 16, pk);
-                    exp_pack16(y, 16, sc, nm, vy, pk, lsum);
-                    tmem_st8(s_tm + 32 * hh + 24, pk);
+                    float mx = fmaxf(max32(x, valid_bits(nv0, tr0, tmask, 0)), max32(y, valid_bits(nv0, tr0, tmask, 32)));
+                    tmem_ld32(s_tm + 64, x);
+                    tmem_ld32(s_tm + 96, y);
+                    tmem_wait_ld();
+                    mx = fmaxf(mx, fmaxf(max32(x, valid_bits(nv1, tr1, tmask, 0)), max32(y, valid_bits(nv1, tr1, tmask, 32))));
+                    m = mx * sc;   // scale > 0: max of scaled scores = scale * max of raw scores
                 }
+                float ls = 0.f, mx = -INFINITY;
+                p_pass(s_tm, m == -INFINITY ? 0.f : -m, sc, nv0, tr0, nv1, tr1, tmask, ls, mx);
+                const float tmx = mx * sc;
+                const bool bad = tmx != -INFINITY && (m == -INFINITY || tmx > m + kMaxSlack);
+                if (__any_sync(0xffffffffu, bad)) {
+                    const bool resc = bad && m != -INFINITY;
+                    if (__any_sync(0xffffffffu, resc)) {
+                        // O_g holds P V up to step t-2, complete since S(t) is
+                        const float f = resc ? exp2_sfu(m - tmx) : 1.f;
+#pragma unroll
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t x[32];
+                            tmem_ld32(o_tm + grp * D + c0, x);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) x[j] = __float_as_uint(__uint_as_float(x[j]) * f);
+                            tmem_st32(o_tm + grp * D + c0, x);
+                        }
+                        lsum *= f;
+                    }
+                    if (bad) m = tmx;
+                    ls = 0.f;
+                    p_pass_slow(s_tm, m == -INFINITY ? 0.f : -m, sc, nv0, tr0, nv1, tr1, tmask, ls, mx);
+                }
+                lsum += ls;
                 tmem_wait_st();
                 tc_before();
                 mbar_arrive(bar(C::B_P_FULL + grp));
