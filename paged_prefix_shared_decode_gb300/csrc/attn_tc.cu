@@ -3,24 +3,23 @@
 // segments read by many sequences, MCTS tree levels and draft-tree
 // verification.
 //
-// One persistent CTA of 13 warps per SM.  A work unit is (item, layer, kv
+// One persistent CTA of 12 warps per SM.  A work unit is (item, layer, kv
 // head): up to 128 query rows (the item's members x the GQA group of the kv
 // head) against the item's 64-token KV tiles, taken two at a time as
 // 128-token steps.
-//   warps 0-1   K producers, warps 2-3 V producers.  Each pair fills its own
-//               ring, since K is released as soon as S = Q K^T is computed
-//               and V only once P V is.  Whole tiles whose blocks start on a
-//               box boundary are copied by TMA (cp.async.bulk.tensor, one box
-//               per block and 64-column slab, 128-byte swizzle, issued by
-//               lane 0 of both warps of the pair); ragged tiles by cp.async
-//               (16-byte chunks, same swizzle, zero fill).  Warp 0 claims
-//               units from an atomic counter and stages their tile
-//               descriptors in shared memory; the V pair also loads each
-//               unit's Q as soon as the previous unit's last S is done.
-//   warp 4      MMA issuer (one thread): S_g = Q K^T (M=128, N=128, K=d) into
+//   warp 0      K producer, warp 1 V producer.  Each fills its own ring, since
+//               K is released as soon as S = Q K^T is computed and V only once
+//               P V is.  Whole tiles whose blocks start on a box boundary are
+//               copied by TMA (cp.async.bulk.tensor, one box per block and
+//               64-column slab, 128-byte swizzle, one lane per box); ragged
+//               tiles by cp.async (16-byte chunks, same swizzle, zero fill).
+//   warp 2      MMA issuer (one thread): S_g = Q K^T (M=128, N=128, K=d) into
 //               TMEM buffer g = step parity, and O_g += P_g V (M=128, N=d,
 //               K=128) with P_g read from TMEM.
-//   warps 5-8   softmax group 0 (even steps), warps 9-12 group 1 (odd
+//   warp 3      claims units from an atomic counter, stages their tile
+//               descriptors in shared memory (two slots), and loads each
+//               unit's Q as soon as the previous unit's last S is done.
+//   warps 4-7   softmax group 0 (even steps), warps 8-11 group 1 (odd
 //               steps), one thread per query row.  Each group keeps its own
 //               running max m_g, sum l_g and accumulator O_g, so while one
 //               group turns step t's scores into P the tensor cores run the
@@ -28,7 +27,7 @@
 //               merged when the unit ends.
 // P (bf16 pairs) overwrites the S columns it came from, so it never passes
 // through shared memory.  The running max is raised only when a step's max
-// exceeds it by more than 8 (factor 256); O_g is then rescaled in TMEM.
+// exceeds it by more than 32, so p < 2^32; O_g is then rescaled in TMEM.
 // Every wait is bounded; on a timeout the CTA sets bit 4 of the workspace
 // error word, all roles leave their loops and TMEM is freed.
 //
@@ -50,14 +49,15 @@ namespace {
 constexpr int kProdWarps = 2;        // warp 0: K, warp 1: V
 constexpr int kVWarp = 1;
 constexpr int kMmaWarp = 2;
-constexpr int kSoftWarp0 = 3;        // warps 3-6: group 0, 7-10: group 1
-constexpr int kTcThreads = 352;      // 11 warps: at most 3 per SM sub-partition
+constexpr int kUnitWarp = 3;         // claims units, stages descriptors and Q
+constexpr int kSoftWarp0 = 4;        // warps 4-7: group 0, 8-11: group 1
+constexpr int kTcThreads = 384;      // 12 warps: 3 per SM sub-partition
 constexpr int kSoftThreads = 256;
 constexpr int kGroupThreads = 128;
 constexpr int kStepTokens = 2 * kTileTokens;
 constexpr int kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr float kMaxSlack = 32.f;    // log2 headroom of p above the running max
+constexpr float kSlackSum = 4294967296.f;   // 2^32: bound on a step's sum of p
 
 __device__ __forceinline__ uint32_t saddr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -181,11 +181,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         KVP_W8(0), KVP_W8(8), KVP_W8(16), KVP_W8(24)
         : "memory");
 }
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
-                 KVP_W8(0)
-                 : "memory");
-}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
@@ -260,18 +255,19 @@ __device__ __forceinline__ float max32(const uint32_t (&x)[32], uint32_t vm) {
     }
     return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
 }
-// p = 2^(s * sc + nm) for scores j0 .. j0+15 (0 where invalid), packed as 8
-// bf16 pairs; adds the sum of p to sum and folds the valid scores into mx
+// p = 2^(s * sc + nm) for scores j0 .. j0+15, packed as 8 bf16 pairs; with
+// MASKED the invalid ones (bits of vm) give 0.  Adds the sum of p to sum.
+template <bool MASKED>
 __device__ __forceinline__ void exp_pack16(const uint32_t (&x)[32], int j0, float sc, float nm,
-                                           uint32_t vm, uint32_t *p, float &sum, float &mx) {
+                                           uint32_t vm, uint32_t *p, float &sum) {
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
     for (int j = 0; j < 16; j += 4) {
         float v[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            v[i] = (vm >> (j0 + j + i)) & 1u ? __uint_as_float(x[j0 + j + i]) : -INFINITY;
-            mx = fmaxf(mx, v[i]);
+            v[i] = __uint_as_float(x[j0 + j + i]);
+            if (MASKED) v[i] = (vm >> (j0 + j + i)) & 1u ? v[i] : -INFINITY;
             v[i] = exp2_sfu(fmaf(v[i], sc, nm));
         }
         s0 += v[0] + v[1];
@@ -282,12 +278,10 @@ __device__ __forceinline__ void exp_pack16(const uint32_t (&x)[32], int j0, floa
     sum += s0 + s1;
 }
 
-// P = 2^(s * sc + nm) of one step into the S columns it came from (P column
-// i holds scores 2i, 2i + 1; every store lands on columns whose scores are
-// already in registers); adds the sum of P to ls and folds the step's valid
-// raw scores into mx.
+// P = 2^(s * sc + nm) of one step, packed into pk (word i holds scores 2i,
+// 2i + 1); adds the sum of P to ls.  S is only read.
 __device__ __forceinline__ void p_pass(uint32_t s_tm, float nm, float sc, int nv0, bool tr0, int nv1, bool tr1,
-                                       uint64_t tmask, float &ls, float &mx) {
+                                       uint64_t tmask, uint32_t (&pk)[64], float &ls) {
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         uint32_t x[32], y[32];
@@ -296,22 +290,49 @@ __device__ __forceinline__ void p_pass(uint32_t s_tm, float nm, float sc, int nv
         tmem_wait_ld();
         const uint32_t vx = valid_bits(hh ? nv1 : nv0, hh ? tr1 : tr0, tmask, 0);
         const uint32_t vy = valid_bits(hh ? nv1 : nv0, hh ? tr1 : tr0, tmask, 32);
-        uint32_t pk[8];
-        exp_pack16(x, 0, sc, nm, vx, pk, ls, mx);
-        tmem_st8(s_tm + 32 * hh, pk);
-        exp_pack16(x, 16, sc, nm, vx, pk, ls, mx);
-        tmem_st8(s_tm + 32 * hh + 8, pk);
-        exp_pack16(y, 0, sc, nm, vy, pk, ls, mx);
-        tmem_st8(s_tm + 32 * hh + 16, pk);
-        exp_pack16(y, 16, sc, nm, vy, pk, ls, mx);
-        tmem_st8(s_tm + 32 * hh + 24, pk);
+        uint32_t *q = pk + 32 * hh;
+        if (__all_sync(0xffffffffu, (vx & vy) == 0xffffffffu)) {
+            exp_pack16<false>(x, 0, sc, nm, vx, q, ls);
+            exp_pack16<false>(x, 16, sc, nm, vx, q + 8, ls);
+            exp_pack16<false>(y, 0, sc, nm, vy, q + 16, ls);
+            exp_pack16<false>(y, 16, sc, nm, vy, q + 24, ls);
+        } else {
+            exp_pack16<true>(x, 0, sc, nm, vx, q, ls);
+            exp_pack16<true>(x, 16, sc, nm, vx, q + 8, ls);
+            exp_pack16<true>(y, 0, sc, nm, vy, q + 16, ls);
+            exp_pack16<true>(y, 16, sc, nm, vy, q + 24, ls);
+        }
     }
 }
-// the same, kept out of line for the rare recomputation so that its
-// registers do not add to the common path's
-__device__ __noinline__ void p_pass_slow(uint32_t s_tm, float nm, float sc, int nv0, bool tr0, int nv1, bool tr1,
-                                         uint64_t tmask, float &ls, float &mx) {
-    p_pass(s_tm, nm, sc, nv0, tr0, nv1, tr1, tmask, ls, mx);
+// P overwrites the first 64 S columns (all scores are read by then)
+__device__ __forceinline__ void p_store(uint32_t s_tm, const uint32_t (&pk)[64]) {
+    tmem_st32(s_tm, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+    tmem_st32(s_tm + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+}
+// Row max of one step's valid raw scores (-inf if none).
+__device__ __forceinline__ float step_max(uint32_t s_tm, int nv0, bool tr0, int nv1, bool tr1, uint64_t tmask) {
+    uint32_t x[32], y[32];
+    tmem_ld32(s_tm, x);
+    tmem_ld32(s_tm + 32, y);
+    tmem_wait_ld();
+    float mx = fmaxf(max32(x, valid_bits(nv0, tr0, tmask, 0)), max32(y, valid_bits(nv0, tr0, tmask, 32)));
+    tmem_ld32(s_tm + 64, x);
+    tmem_ld32(s_tm + 96, y);
+    tmem_wait_ld();
+    return fmaxf(mx, fmaxf(max32(x, valid_bits(nv1, tr1, tmask, 0)), max32(y, valid_bits(nv1, tr1, tmask, 32))));
+}
+// The slow path, kept out of line so that its registers do not add to the
+// common path's: the step's max, the new running max (raised for the rows
+// marked bad), P again, stored.  Returns (new m, sum of P).
+__device__ __noinline__ float2 recompute_step(uint32_t s_tm, float m, float sc, int nv0, bool tr0, int nv1, bool tr1,
+                                              uint64_t tmask, bool bad) {
+    const float tmx = step_max(s_tm, nv0, tr0, nv1, tr1, tmask) * sc;
+    const float m_new = bad ? fmaxf(m, tmx) : m;
+    float ls = 0.f;
+    uint32_t pk[64];
+    p_pass(s_tm, m_new == -INFINITY ? 0.f : -m_new, sc, nv0, tr0, nv1, tr1, tmask, pk, ls);
+    p_store(s_tm, pk);
+    return make_float2(m_new, ls);
 }
 
 template <int D>
@@ -335,8 +356,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(C::B_UNIT_FULL + s), 1);
-            // unit slot free: MMA thread + softmax threads + V warp
-            mbar_init(bar(C::B_UNIT_EMPTY + s), 1 + kSoftThreads + 1);
+            // unit slot free: MMA thread + softmax threads + K and V warps
+            mbar_init(bar(C::B_UNIT_EMPTY + s), 1 + kSoftThreads + kProdWarps);
             mbar_init(bar(C::B_S_FULL + s), 1);
             mbar_init(bar(C::B_P_FULL + s), kGroupThreads);
         }
@@ -412,28 +433,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t g = 0;   // steps filled
         for (int uc = 0;; ++uc) {
             const int slot = uc & 1;
-            int unit = -1;
-            if (!is_v) {
-                bool ok = wait_warp(bar(C::B_UNIT_EMPTY + slot), ((uc >> 1) & 1) ^ 1);
-                if (lane == 0) unit = atomicAdd(a.tc_counter, 1);
-                unit = __shfl_sync(0xffffffffu, unit, 0);
-                const bool done = !ok || unit >= a.n_tc_units || __shfl_sync(0xffffffffu, *s_abort, 0);
-                if (!done) {
-                    const WorkItem it = a.tc_items[unit % n_items];
-                    const int ntile = it.tile_end - it.tile_begin;
-                    const int4 *src = reinterpret_cast<const int4 *>(a.tiles + it.tile_begin);
-                    int4 *dst = reinterpret_cast<int4 *>(s_desc + slot * kMaxItemTiles);
-                    for (int i = lane; i < ntile * 2; i += 32) dst[i] = src[i];
-                }
-                if (lane == 0) s_unit[slot] = done ? -1 : unit;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::B_UNIT_FULL + slot));
-                if (done) break;
-            } else {
-                const bool ok = wait_warp(bar(C::B_UNIT_FULL + slot), (uc >> 1) & 1);
-                unit = ok ? s_unit[slot] : -1;
-                if (unit < 0) break;
-            }
+            const bool okw = wait_warp(bar(C::B_UNIT_FULL + slot), (uc >> 1) & 1);
+            const int unit = okw ? s_unit[slot] : -1;
+            if (unit < 0) break;
             const int item_idx = unit % n_items;
             const int lk = unit / n_items;
             const int kvh = lk % a.Hkv, l = lk / a.Hkv;
@@ -444,27 +446,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int row_base_lh = (l * a.NB) * a.Hkv + kvh;   // row of block b = (row_base_lh + b*Hkv) * bs
             const KvTile *tiles = s_desc + slot * kMaxItemTiles;
             bool alive = true;
-            if (is_v) {
-                // Q of this unit, once the previous unit's S MMAs are done with
-                // it: rows lane + 32 i, whose member indices are loaded first
-                alive = wait_warp(bar(C::B_Q_EMPTY), (uc & 1) ^ 1);
-                const int rows = it.n_members * G;
-                int qt[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = lane + 32 * i;
-                    qt[i] = r < rows ? __ldg(a.members + it.member_off + r / G) : 0;
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = lane + 32 * i;
-                    const __nv_bfloat16 *qrow = qb + (((size_t)l * a.nq + qt[i]) * a.Hq + kvh * G + r % G) * D;
-#pragma unroll
-                    for (int c = 0; c < C::CH; ++c)
-                        cp_async16(q_smem + swz(r, c), r < rows ? qrow + c * 8 : qb, r < rows ? 16 : 0);
-                }
-                cp_async_arrive(bar(C::B_Q_FULL));
-            }
             for (int t = 0; alive && t < nsteps; ++t, ++g) {
                 const int st = g % nring;
                 if (!wait_warp(bar(b_empty + st), ((g / nring) & 1) ^ 1)) { alive = false; break; }
@@ -515,16 +496,59 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 cp_async_arrive(fb);
             }
-            if (is_v && lane == 0) mbar_arrive(bar(C::B_UNIT_EMPTY + slot));
-            if (!alive || __shfl_sync(0xffffffffu, *s_abort, 0)) {
-                // let the consumers see the end
-                if (!is_v && lane == 0) {
-                    const int s2 = (uc + 1) & 1;
-                    s_unit[s2] = -1;
-                    mbar_arrive(bar(C::B_UNIT_FULL + s2));
-                }
-                break;
+            if (lane == 0) mbar_arrive(bar(C::B_UNIT_EMPTY + slot));
+            if (!alive || __shfl_sync(0xffffffffu, *s_abort, 0)) break;
+        }
+    } else if (warp == kUnitWarp) {
+        // ------------------------------------------------------------ units and Q
+        auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
+            int ok = 1;
+            if (lane == 0) ok = wait(b, parity) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();
+            return ok != 0;
+        };
+        for (int uc = 0;; ++uc) {
+            const int slot = uc & 1;
+            bool ok = wait_warp(bar(C::B_UNIT_EMPTY + slot), ((uc >> 1) & 1) ^ 1);
+            int unit = -1;
+            if (lane == 0) unit = atomicAdd(a.tc_counter, 1);
+            unit = __shfl_sync(0xffffffffu, unit, 0);
+            const bool done = !ok || unit >= a.n_tc_units || __shfl_sync(0xffffffffu, *s_abort, 0);
+            WorkItem it{};
+            if (!done) {
+                it = a.tc_items[unit % n_items];
+                const int ntile = it.tile_end - it.tile_begin;
+                const int4 *src = reinterpret_cast<const int4 *>(a.tiles + it.tile_begin);
+                int4 *dst = reinterpret_cast<int4 *>(s_desc + slot * kMaxItemTiles);
+                for (int i = lane; i < ntile * 2; i += 32) dst[i] = src[i];
             }
+            if (lane == 0) s_unit[slot] = done ? -1 : unit;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_UNIT_FULL + slot));
+            if (done) break;
+            // Q of this unit, once the previous unit's S MMAs are done with
+            // it: rows lane + 32 i, whose member indices are loaded first
+            ok = wait_warp(bar(C::B_Q_EMPTY), (uc & 1) ^ 1);
+            const int lk = unit / n_items;
+            const int kvh = lk % a.Hkv, l = lk / a.Hkv;
+            const int rows = it.n_members * G;
+            int qt[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = lane + 32 * i;
+                qt[i] = r < rows ? __ldg(a.members + it.member_off + r / G) : 0;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = lane + 32 * i;
+                const __nv_bfloat16 *qrow = qb + (((size_t)l * a.nq + qt[i]) * a.Hq + kvh * G + r % G) * D;
+#pragma unroll
+                for (int c = 0; c < C::CH; ++c)
+                    cp_async16(q_smem + swz(r, c), r < rows ? qrow + c * 8 : qb, r < rows ? 16 : 0);
+            }
+            cp_async_arrive(bar(C::B_Q_FULL));
+            if (!ok) break;
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -642,34 +666,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     nv1 = has && mem >= mlo && mem < mhi ? (k1.ntok_flags & 0xFFFF) : 0;
                     tr1 = (k1.ntok_flags >> 16) & kTileTree;
                 }
-                // A row's running max m is raised only when a step's scaled max
-                // exceeds it by more than kMaxSlack, so p <= 2^kMaxSlack, well
-                // inside bf16 and the fp32 sums.  A step therefore reads S once
-                // and forms P with the current m while it tracks the step's max;
-                // only a row whose max breaks the bound, or that has no m yet,
-                // takes the slow path: rescale O_g and l, form P again.
+                // A row's running max m is raised only when the step's P would
+                // sum to more than 2^32, so every p <= 2^32, well inside bf16
+                // and the fp32 sums.  A step therefore reads S once and forms P
+                // with the current m, in registers; only a row whose sum breaks
+                // the bound, or that has valid scores but no m yet, takes the
+                // slow path (the step's max, O_g and l rescaled, P again)
+                // before P overwrites S.
                 if (__all_sync(0xffffffffu, m == -INFINITY)) {
                     // this group's first step of the unit: find m first
-                    uint32_t x[32], y[32];
-                    tmem_ld32(s_tm, x);
-                    tmem_ld32(s_tm + 32, y);
-                    tmem_wait_ld();
-                    float mx = fmaxf(max32(x, valid_bits(nv0, tr0, tmask, 0)), max32(y, valid_bits(nv0, tr0, tmask, 32)));
-                    tmem_ld32(s_tm + 64, x);
-                    tmem_ld32(s_tm + 96, y);
-                    tmem_wait_ld();
-                    mx = fmaxf(mx, fmaxf(max32(x, valid_bits(nv1, tr1, tmask, 0)), max32(y, valid_bits(nv1, tr1, tmask, 32))));
-                    m = mx * sc;   // scale > 0: max of scaled scores = scale * max of raw scores
+                    // (scale > 0: max of scaled scores = scale * max of raw scores)
+                    m = step_max(s_tm, nv0, tr0, nv1, tr1, tmask) * sc;
                 }
-                float ls = 0.f, mx = -INFINITY;
-                p_pass(s_tm, m == -INFINITY ? 0.f : -m, sc, nv0, tr0, nv1, tr1, tmask, ls, mx);
-                const float tmx = mx * sc;
-                const bool bad = tmx != -INFINITY && (m == -INFINITY || tmx > m + kMaxSlack);
-                if (__any_sync(0xffffffffu, bad)) {
-                    const bool resc = bad && m != -INFINITY;
+                float ls = 0.f;
+                uint32_t pk[64];
+                p_pass(s_tm, m == -INFINITY ? 0.f : -m, sc, nv0, tr0, nv1, tr1, tmask, pk, ls);
+                const bool bad = m == -INFINITY ? (nv0 > 0 || nv1 > 0) : !(ls <= kSlackSum);
+                if (!__any_sync(0xffffffffu, bad)) {
+                    p_store(s_tm, pk);
+                } else {
+                    const float2 r2 = recompute_step(s_tm, m, sc, nv0, tr0, nv1, tr1, tmask, bad);
+                    const bool resc = r2.x != m && m != -INFINITY;
                     if (__any_sync(0xffffffffu, resc)) {
                         // O_g holds P V up to step t-2, complete since S(t) is
-                        const float f = resc ? exp2_sfu(m - tmx) : 1.f;
+                        const float f = resc ? exp2_sfu(m - r2.x) : 1.f;
 #pragma unroll
                         for (int c0 = 0; c0 < D; c0 += 32) {
                             uint32_t x[32];
@@ -681,9 +701,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         lsum *= f;
                     }
-                    if (bad) m = tmx;
-                    ls = 0.f;
-                    p_pass_slow(s_tm, m == -INFINITY ? 0.f : -m, sc, nv0, tr0, nv1, tr1, tmask, ls, mx);
+                    m = r2.x;
+                    ls = r2.y;
                 }
                 lsum += ls;
                 tmem_wait_st();

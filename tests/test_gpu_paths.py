@@ -16,7 +16,7 @@ if not torch.cuda.is_available():
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUBSET = ("tiny_fork or dendrite_full or trellis or mcts_tree or ragged or cow or gqa or "
-          "verify_B1 or verify_tree_shapes or short_draft")
+          "verify_B1 or verify_tree_shapes or short_draft or growing_scores")
 
 
 @pytest.mark.parametrize("path", ["tc", "mma"])

@@ -97,3 +97,33 @@ def test_verify_bad_parent_sets_error_word():
     call = VerifyCall(r)
     call(bf16_tensor(W.verify_q(w)))
     assert kvp.kvp_device_error(call.ws) == 2
+
+
+def growing_kv(w, i):
+    """Keys of the context's second half scaled 30x: a later step's scores
+    exceed the running max of the earlier steps by far more than the kernel's
+    headroom (p would overflow fp32), so its rescale-and-recompute path runs."""
+    k, v = W.append_kv(w, i)
+    ntok = w.ops[i][2]
+    if ntok > w.info["n_draft"]:
+        kf = W.bf16_bits_to_f32(k)
+        kf[:, ntok // 2:] *= 30.0
+        k = W.f32_to_bf16_bits(kf)
+    return k, v
+
+
+def test_verify_growing_scores():
+    w = W.verify_tree(1, layers=1)
+    r = PoolRunner(w, alloc_seed=1)
+    r.run_ops(kv_fn=growing_kv)
+    call = VerifyCall(r)
+    q = W.verify_q(w)
+    call(bf16_tensor(q))
+    torch.cuda.synchronize()
+    rw = oracle.replay(w, alloc_seed=1, kv_fn=growing_kv)
+    t, ln = rw.tables(w.batch, w.max_blocks_per_seq)
+    ctx = ln - w.info["n_draft"]
+    want_o, want_l = oracle.verify_attention(q, rw.k_pool, rw.v_pool, t, ctx, w.info["parents"])
+    check_close(to_f64(call.out), want_o, max_abs_tol=peaked_max_abs(want_o, bf16_absmax(rw.v_pool)))
+    check_lse(to_f64(call.lse), want_l)
+    assert kvp.kvp_device_error(call.ws) == 0
