@@ -199,10 +199,10 @@ struct TcCfg {
     static constexpr int CH = D / 8;                   // 16-byte chunks per row
     static constexpr int SLAB = kStepTokens * 128;     // one slab of a 128-row operand
     static constexpr int OPER = NSLAB * SLAB;          // Q, or K (V) of one step
-    static constexpr int NK = D == 64 ? 6 : 3;         // K ring depth (steps)
-    static constexpr int NV = D == 64 ? 6 : 2;         // V ring depth (steps)
-    static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + OPER;
+    static constexpr int NK = D == 64 ? 5 : 2;         // K ring depth (steps)
+    static constexpr int NV = D == 64 ? 5 : 2;         // V ring depth (steps)
+    static constexpr int Q_OFF = 0;                    // two 128-row Q tiles
+    static constexpr int K_OFF = Q_OFF + 2 * OPER;
     static constexpr int V_OFF = K_OFF + NK * OPER;
     static constexpr int DESC_OFF = V_OFF + NV * OPER;                                // [2][kMaxItemTiles]
     static constexpr int ML_OFF = DESC_OFF + 2 * kMaxItemTiles * (int)sizeof(KvTile);  // [2][128] float2
@@ -532,20 +532,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = wait_warp(bar(C::B_Q_EMPTY), (uc & 1) ^ 1);
             const int lk = unit / n_items;
             const int kvh = lk % a.Hkv, l = lk / a.Hkv;
+            // (one 128-row tile, or two for a pair unit)
             const int rows = it.n_members * G;
-            int qt[4];
+            const int ntq = rows > 128 ? 2 : 1;
+            for (int tq = 0; tq < ntq; ++tq) {
+                int qt[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = lane + 32 * i;
-                qt[i] = r < rows ? __ldg(a.members + it.member_off + r / G) : 0;
-            }
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 128 * tq + lane + 32 * i;
+                    qt[i] = r < rows ? __ldg(a.members + it.member_off + r / G) : 0;
+                }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = lane + 32 * i;
-                const __nv_bfloat16 *qrow = qb + (((size_t)l * a.nq + qt[i]) * a.Hq + kvh * G + r % G) * D;
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 128 * tq + lane + 32 * i;
+                    const __nv_bfloat16 *qrow = qb + (((size_t)l * a.nq + qt[i]) * a.Hq + kvh * G + r % G) * D;
 #pragma unroll
-                for (int c = 0; c < C::CH; ++c)
-                    cp_async16(q_smem + swz(r, c), r < rows ? qrow + c * 8 : qb, r < rows ? 16 : 0);
+                    for (int c = 0; c < C::CH; ++c)
+                        cp_async16(q_smem + tq * C::OPER + swz(r & 127, c), r < rows ? qrow + c * 8 : qb,
+                                   r < rows ? 16 : 0);
+                }
             }
             cp_async_arrive(bar(C::B_Q_FULL));
             if (!ok) break;
@@ -565,6 +570,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const WorkItem it = a.tc_items[unit % n_items];
                 const int ntile = it.tile_end - it.tile_begin;
                 const int nsteps = (ntile + 1) >> 1;
+                const bool pair = it.n_members * G > 128;
                 bool ok = wait(bar(C::B_Q_FULL), uc & 1);
                 // Q was written through the generic proxy (cp.async)
                 fence_async_smem();
@@ -587,6 +593,62 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (t == nsteps - 1) umma_commit(bar(C::B_Q_EMPTY));
                     return true;
                 };
+                if (pair) {
+                    // Two 128-row tiles over the same K/V: each step serves both,
+                    // S_g and O_g belong to tile g, and group g takes every step.
+                    auto wait_k = [&](int t) -> bool {
+                        const uint32_t g = gk + t, st = g % C::NK;
+                        if (!wait(bar(C::B_K_FULL + st), (g / C::NK) & 1)) return false;
+                        fence_async_smem();
+                        tc_after();
+                        return true;
+                    };
+                    auto issue_sp = [&](int t, int tq) {
+                        const uint32_t st = (gk + t) % C::NK;
+                        const uint32_t kst = k_smem + st * C::OPER, qs = q_smem + tq * C::OPER;
+                        const uint32_t d_tm = tmem + C::S_COL + tq * kStepTokens;
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k) {
+                            const uint32_t o = (uint32_t)(k >> 2) * C::SLAB + (uint32_t)(k & 3) * 32;
+                            umma_ss(d_tm, sdesc(qs + o, 16, 1024), sdesc(kst + o, 16, 1024), IDESC_S,
+                                    k > 0 ? 1u : 0u);
+                        }
+                        umma_commit(bar(C::B_S_FULL + tq));
+                        if (tq == 1) {
+                            umma_commit(bar(C::B_K_EMPTY + st));
+                            if (t == nsteps - 1) umma_commit(bar(C::B_Q_EMPTY));
+                        }
+                    };
+                    if (ok && nsteps > 0) {
+                        ok = wait_k(0);
+                        if (ok) {
+                            issue_sp(0, 0);
+                            issue_sp(0, 1);
+                        }
+                    }
+                    if (ok) ok = wait(bar(C::B_O_EMPTY), (uc & 1) ^ 1);
+                    tc_after();
+                    for (int t = 0; ok && t < nsteps; ++t) {
+                        const uint32_t g = gv + t, st = g % C::NV;
+                        const uint32_t vst = v_smem + st * C::OPER;
+                        const int ksteps = 2 * t + 1 < ntile ? kStepTokens / 16 : kTileTokens / 16;
+                        for (int tq = 0; ok && tq < 2; ++tq) {
+                            if (!wait(bar(C::B_P_FULL + tq), (tq ? np1 : np0) & 1)) { ok = false; break; }
+                            if (tq) ++np1; else ++np0;
+                            if (tq == 0 && !wait(bar(C::B_V_FULL + st), (g / C::NV) & 1)) { ok = false; break; }
+                            if (tq == 0) fence_async_smem();
+                            tc_after();
+                            for (int k = 0; k < ksteps; ++k)
+                                umma_ts(tmem + C::O_COL + tq * D, tmem + C::S_COL + tq * kStepTokens + k * 8,
+                                        sdesc(vst + k * 2048, C::SLAB, 1024), IDESC_PV, (t > 0 || k > 0) ? 1u : 0u);
+                            if (tq == 1) umma_commit(bar(C::B_V_EMPTY + st));
+                            if (t + 1 < nsteps) {
+                                if (tq == 0 && !wait_k(t + 1)) { ok = false; break; }
+                                issue_sp(t + 1, tq);
+                            }
+                        }
+                    }
+                } else {
                 if (ok && nsteps > 0) ok = issue_s(0);
                 if (ok && nsteps > 1) ok = issue_s(1);
                 // the previous unit's epilogue has read O_0 and O_1
@@ -608,6 +670,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 sdesc(vst + k * 2048, C::SLAB, 1024), IDESC_PV, (t >= 2 || k > 0) ? 1u : 0u);
                     umma_commit(bar(C::B_V_EMPTY + st));
                     if (t + 2 < nsteps && !issue_s(t + 2)) { ok = false; break; }
+                }
                 }
                 if (!ok) break;
                 if (nsteps == 0) umma_commit(bar(C::B_Q_EMPTY));
@@ -641,14 +704,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int nsteps = (ntile + 1) >> 1;
             const KvTile *tiles = s_desc + slot * kMaxItemTiles;
             const int rows = it.n_members * G;
-            const bool has = r < rows;
-            const int mem = r / G;
+            // one tile: the groups split the steps over the same rows; a pair
+            // unit: group g takes every step for the rows of tile g
+            const bool pair = rows > 128;
+            const int rr = pair ? 128 * grp + r : r;
+            const bool has = rr < rows;
+            const int mem = rr / G;
             int qt = 0;
             if (has) qt = __ldg(a.members + it.member_off + mem);
             const uint64_t tmask = has && a.tree_mask ? a.tree_mask[qt] : ~0ull;
 
             float m = -INFINITY, lsum = 0.f;
-            for (int t = grp; t < nsteps; t += 2) {
+            for (int t = pair ? 0 : grp; t < nsteps; t += pair ? 1 : 2) {
                 ok = wait(bar(C::B_S_FULL + grp), ns & 1) && ok;
                 ns += 1;
                 tc_after();
@@ -709,29 +776,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_before();
                 mbar_arrive(bar(C::B_P_FULL + grp));
             }
-            // epilogue: merge the two groups' (m, l, O) and write
+            // epilogue: one tile merges the two groups' (m, l, O) and each
+            // group writes half of the columns; in a pair unit each group
+            // writes its own tile's rows from its own O
             ok = wait(bar(C::B_O_FULL), uc & 1) && ok;
             tc_after();
             s_ml[grp * 128 + r] = make_float2(m, lsum);
             if (soft_bar_or(!ok || *s_abort)) break;
-            const float2 a0 = s_ml[r], a1 = s_ml[128 + r];
-            const float c = fmaxf(a0.x, a1.x);
-            const float f0 = a0.x == -INFINITY ? 0.f : exp2_sfu(a0.x - c);
-            const float f1 = a1.x == -INFINITY ? 0.f : exp2_sfu(a1.x - c);
-            const float ltot = a0.y * f0 + a1.y * f1;
-            const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
-            const float lse2 = ltot > 0.f ? c + __log2f(ltot) : -INFINITY;
-            const float w0 = f0 * inv, w1 = f1 * inv;
+            float w0, w1, lse2;
+            int ca, cb;
+            if (!pair) {
+                const float2 a0 = s_ml[r], a1 = s_ml[128 + r];
+                const float c = fmaxf(a0.x, a1.x);
+                const float f0 = a0.x == -INFINITY ? 0.f : exp2_sfu(a0.x - c);
+                const float f1 = a1.x == -INFINITY ? 0.f : exp2_sfu(a1.x - c);
+                const float ltot = a0.y * f0 + a1.y * f1;
+                const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
+                lse2 = ltot > 0.f ? c + __log2f(ltot) : -INFINITY;
+                w0 = f0 * inv;
+                w1 = f1 * inv;
+                ca = grp * (D / 2);
+                cb = ca + D / 2;
+            } else {
+                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                lse2 = lsum > 0.f ? m + __log2f(lsum) : -INFINITY;
+                w0 = grp == 0 ? inv : 0.f;
+                w1 = grp == 1 ? inv : 0.f;
+                ca = 0;
+                cb = D;
+            }
             const bool write = has && nsteps > 0;
-#pragma unroll
-            for (int c0 = grp * (D / 2); c0 < (grp + 1) * (D / 2); c0 += 32) {
+            for (int c0 = ca; c0 < cb; c0 += 32) {
                 uint32_t x[32], y[32];
                 tmem_ld32(o_tm + c0, x);
                 tmem_ld32(o_tm + D + c0, y);
                 tmem_wait_ld();
                 if (!write) continue;
-                // a group with no steps (or no valid key) has weight 0 and an
-                // O that was never written: select, do not multiply
+                // an O with weight 0 may never have been written (a group with
+                // no steps or no valid key): select, do not multiply
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const float v0 = w0 != 0.f ? __uint_as_float(x[j]) * w0 : 0.f;
@@ -740,7 +822,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (it.out_base < 0) {
                     __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
-                                         (((size_t)l * a.nq + qt) * a.Hq + kvh * G + r % G) * D + c0;
+                                         (((size_t)l * a.nq + qt) * a.Hq + kvh * G + rr % G) * D + c0;
 #pragma unroll
                     for (int j = 0; j < 32; j += 8) {
                         uint4 v;
@@ -751,7 +833,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         *reinterpret_cast<uint4 *>(dst + j) = v;
                     }
                 } else {
-                    float *dst = a.part_o + (((size_t)l * a.Hkv + kvh) * a.P + it.out_base + r) * D + c0;
+                    float *dst = a.part_o + (((size_t)l * a.Hkv + kvh) * a.P + it.out_base + rr) * D + c0;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
                         *reinterpret_cast<float4 *>(dst + j) =
@@ -759,11 +841,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                         __uint_as_float(x[j + 2]), __uint_as_float(x[j + 3]));
                 }
             }
-            if (write && grp == 0) {
+            if (write && (pair || grp == 0)) {
                 if (it.out_base < 0) {
-                    if (a.lse) a.lse[((size_t)l * a.nq + qt) * a.Hq + kvh * G + r % G] = lse2 * 0.6931471805599453f;
+                    if (a.lse) a.lse[((size_t)l * a.nq + qt) * a.Hq + kvh * G + rr % G] = lse2 * 0.6931471805599453f;
                 } else {
-                    a.part_lse[((size_t)l * a.Hkv + kvh) * a.P + it.out_base + r] = lse2;
+                    a.part_lse[((size_t)l * a.Hkv + kvh) * a.P + it.out_base + rr] = lse2;
                 }
             }
             tc_before();

@@ -13,7 +13,7 @@ constexpr int kTileBlocks = 5;     // blocks a 64-token tile can touch when bs >
 constexpr int kMaxItemTiles = 128; // KV tiles per work item (descriptors staged in smem)
 constexpr int kTileTree = 1;       // tile flag: draft tokens under a tree mask
 constexpr int kMmaMaxRows = 64;    // rows of an mma.sync unit (4 warps x 16)
-constexpr int kTcRows = 128;       // rows of a tcgen05 unit (one thread per row)
+constexpr int kTcRows = 256;       // rows of a tcgen05 unit: one 128-row tile or a pair
 
 // One KV tile of a work item: tokens [tok0, tok0 + ntok) of one sequence,
 // whose physical blocks (in order) are blk[0..]: token t of the tile lives in
