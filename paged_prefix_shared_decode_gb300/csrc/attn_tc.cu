@@ -255,6 +255,18 @@ __device__ __forceinline__ float max32(const uint32_t (&x)[32], uint32_t vm) {
     }
     return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
 }
+// (d0, d1) = (a0, a1) * b + c in one packed instruction
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b, float c) {
+    asm("{\n.reg .b64 ra, rb, rc, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %4};\nmov.b64 rc, {%5, %5};\n"
+        "fma.rn.f32x2 rd, ra, rb, rc;\nmov.b64 {%0, %1}, rd;\n}\n"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (s0, s1) += (a0, a1) in one packed instruction
+__device__ __forceinline__ void fadd2(float &s0, float &s1, float a0, float a1) {
+    asm("{\n.reg .b64 ra, rs;\nmov.b64 ra, {%2, %3};\nmov.b64 rs, {%0, %1};\nadd.f32x2 rs, rs, ra;\n"
+        "mov.b64 {%0, %1}, rs;\n}\n"
+        : "+f"(s0), "+f"(s1) : "f"(a0), "f"(a1));
+}
 // p = 2^(s * sc + nm) for scores j0 .. j0+15, packed as 8 bf16 pairs; with
 // MASKED the invalid ones (bits of vm) give 0.  Adds the sum of p to sum.
 template <bool MASKED>
@@ -262,18 +274,16 @@ __device__ __forceinline__ void exp_pack16(const uint32_t (&x)[32], int j0, floa
                                            uint32_t vm, uint32_t *p, float &sum) {
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; j += 4) {
-        float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[i] = __uint_as_float(x[j0 + j + i]);
-            if (MASKED) v[i] = (vm >> (j0 + j + i)) & 1u ? v[i] : -INFINITY;
-            v[i] = exp2_sfu(fmaf(v[i], sc, nm));
+    for (int j = 0; j < 16; j += 2) {
+        float y0, y1;
+        ffma2(y0, y1, __uint_as_float(x[j0 + j]), __uint_as_float(x[j0 + j + 1]), sc, nm);
+        if (MASKED) {
+            y0 = (vm >> (j0 + j)) & 1u ? y0 : -INFINITY;
+            y1 = (vm >> (j0 + j + 1)) & 1u ? y1 : -INFINITY;
         }
-        s0 += v[0] + v[1];
-        s1 += v[2] + v[3];
-        p[j / 2] = pack_bf16x2(v[0], v[1]);
-        p[j / 2 + 1] = pack_bf16x2(v[2], v[3]);
+        const float e0 = exp2_sfu(y0), e1 = exp2_sfu(y1);
+        fadd2(s0, s1, e0, e1);
+        p[j / 2] = pack_bf16x2(e0, e1);
     }
     sum += s0 + s1;
 }
