@@ -41,7 +41,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "decode attention tokens/s and achieved HBM GB/s (% of GB300 peak) vs φ/branches"
 KERNEL_SRC = os.path.join(ROOT, "paged_prefix_shared_decode_gb300", "csrc", "attn_kernels.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_item_kernel_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_item_kernel_dendrite_traffic.md")
 
 
 def parse():
@@ -183,15 +183,20 @@ def peaks():
 
 
 def traffic_for_current_kernel():
-    """DRAM bytes per launch from the committed ncu capture, if the kernel
-    source has not changed since; else None."""
+    """DRAM bytes per launch from the committed ncu summary ("key: value"
+    lines), if the kernel source has not changed since; else None."""
     try:
+        t = {}
         with open(TRAFFIC_FILE) as f:
-            t = json.load(f)
+            for line in f:
+                k, sep, v = line.partition(":")
+                if sep and k.strip() in ("kernel", "workload", "source_sha256", "dram_bytes_per_launch"):
+                    t[k.strip()] = v.strip()
         h = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
         if t.get("source_sha256") == h:
+            t["dram_bytes_per_launch"] = float(t["dram_bytes_per_launch"])
             return t
-    except (OSError, ValueError):
+    except (OSError, ValueError, KeyError):
         pass
     return None
 
@@ -437,10 +442,11 @@ def run_verify_bench(a, w, rank, world, dev):
         "config": {"workload": describe(w), "name": w.name, "query_tokens_per_step": B * n,
                    "l2": "flushed between timed steps, outside the timed region"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "attn_item_kernel",
+                     "frac": achieved / peak, "traffic": None, "kernel": "attn_tc_kernel",
                      "algorithmic_bytes_per_launch": ub, "kernel_ms": kern_ms,
                      "tensor_tflops": flops / (kern_ms / 1e3) / 1e12, "tensor_peak_tflops": tpk,
-                     "peak_kind": f"{kind} hbm_gbs (copy)"},
+                     "tensor_frac": flops / (kern_ms / 1e3) / 1e12 / tpk,
+                     "peak_kind": f"{kind} hbm_gbs (copy); tensor: measured bf16_tflops (burst)"},
         "e2e": None, "gpu_launches": int(launches), "clocks": clk,
     }
     return res, w
@@ -466,7 +472,8 @@ def run_sweep(a, dev):
             out.append({"workload": name, "tokens_per_s": res["value"], "ms_per_step": res["ms_per_step"],
                         "kernel_ms": res["roofline"]["kernel_ms"],
                         "unique_gb_per_s": res["roofline"]["achieved"], "frac": res["roofline"]["frac"],
-                        "tensor_tflops": res["roofline"]["tensor_tflops"]})
+                        "tensor_tflops": res["roofline"]["tensor_tflops"],
+                        "tensor_frac": res["roofline"]["tensor_frac"]})
             continue
         w = workload(name, 16)
         s = w.shapes
