@@ -1,11 +1,11 @@
 // Paged attention work-item kernel and log-sum-exp merge (sm_103a).
 //
-// A persistent grid (one to three CTAs of 4 warps per SM) pulls work units --
+// A persistent grid (up to four CTAs of 4 warps per SM) pulls work units --
 // (work item, layer, kv head) -- from an atomic counter, longest first.  A
 // unit is up to 64 query rows (sequences or draft nodes x the GQA group that
 // shares this kv head) against a list of 64-token KV tiles.  The tiles'
 // descriptors, which carry the physical block ids, are staged in shared
-// memory first; then each tile's K and V are copied into a 3-4 deep shared
+// memory first; then each tile's K and V are copied into a 3-deep shared
 // memory ring (cp.async, 16-byte chunks, XOR-swizzled rows) and used by every
 // row of the unit.  This is how a block shared by several sequences is read
 // from HBM once for all of them.
@@ -114,11 +114,13 @@ template <int D>
 struct KCfg {
     static constexpr int CH = D / 8;                        // 16-byte chunks per token row
     static constexpr int TILE_BYTES = kTileTokens * D * 2;  // one K (or V) tile
-    static constexpr int NSTAGE = D == 64 ? 4 : 3;
+    // three stages and (d 64) four CTAs per SM: more resident warps hide the
+    // mma.sync / SFU latencies better than a deeper ring (measured)
+    static constexpr int NSTAGE = 3;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int DESC_OFF = NSTAGE * STAGE_BYTES;
     static constexpr int SMEM = DESC_OFF + kMaxItemTiles * (int)sizeof(KvTile);
-    static constexpr int MIN_BLOCKS = D == 64 ? 3 : 2;
+    static constexpr int MIN_BLOCKS = D == 64 ? 4 : 2;
     static constexpr int NO = D / 8;    // n-tiles of O
     static constexpr int KS = D / 16;   // k-steps of Q K^T
 };
