@@ -201,8 +201,44 @@ void push_range(std::vector<KvTile> &kv, const TileSrc &src, int32_t row, int32_
 // Chunk items into work items, lay out partial rows and merge lists.  Items
 // with more than `thr` rows go to the tcgen05 kernel (one CTA per SM), the
 // rest to the mma.sync kernel (`mma_ctas` CTAs per SM).
+// Items of at most 16 rows and a few tiles cost more in per-unit start-up
+// than in work; pack them into items of up to 64 rows, each tile keeping the
+// member interval of the item it came from.
+void pack_small(std::vector<ProtoItem> &protos, int32_t G, int thr) {
+    // stay on the mma.sync kernel: at most 64 rows and at most the threshold
+    const int kPackRows = thr < 64 ? thr : 64;
+    constexpr int kPackTiles = 4, kPackMaxTiles = 64;
+    std::vector<ProtoItem> out;
+    ProtoItem cur;
+    auto flush = [&]() {
+        if (!cur.members.empty()) out.push_back(std::move(cur));
+        cur = ProtoItem{};
+    };
+    for (auto &p : protos) {
+        const int rows = (int)p.members.size() * G;
+        const bool small = rows <= 16 && rows <= thr && (int)p.kv.size() <= kPackTiles;
+        if (!small) {
+            out.push_back(std::move(p));
+            continue;
+        }
+        if ((int)(cur.members.size() + p.members.size()) * G > kPackRows ||
+            (int)(cur.kv.size() + p.kv.size()) > kPackMaxTiles)
+            flush();
+        const int32_t off = (int32_t)cur.members.size();
+        cur.members.insert(cur.members.end(), p.members.begin(), p.members.end());
+        for (KvTile t : p.kv) {
+            const int32_t lo = (t.members & 0xFFFF) + off, hi = (t.members >> 16) + off;
+            t.members = lo | (hi << 16);
+            cur.kv.push_back(t);
+        }
+    }
+    flush();
+    protos.swap(out);
+}
+
 void finish(HostPlan &hp, std::vector<ProtoItem> &protos, int32_t G, int32_t nq,
             int32_t layers_heads, int32_t sms, int32_t mma_ctas, int thr) {
+    pack_small(protos, G, thr);
     struct Chunked {
         WorkItem it;
         int64_t cost;
