@@ -22,7 +22,11 @@ namespace {
 
 constexpr int kMaxSlots = 4096;   // tokens per launch (16 KB of parameters)
 constexpr int kMaxCow = 256;      // copy-on-write triples per launch
+// Decode appends are a few tokens: a small parameter block for those, since
+// every launch passes the whole block.
+constexpr int kSmallSlots = 64, kSmallCow = 16;
 
+template <int NS, int NC>
 struct KvWriteArgs {
     uint4 *k_pool;
     uint4 *v_pool;
@@ -33,11 +37,12 @@ struct KvWriteArgs {
     int32_t tok_begin, ntok;          // this launch's tokens
     int32_t ncow;
     int64_t cow_chunks;               // sum over triples of L*Hkv*used*CH
-    int32_t cow[3 * kMaxCow];
-    int32_t slots[kMaxSlots];
+    int32_t cow[3 * NC];
+    int32_t slots[NS];
 };
 
-__global__ void __launch_bounds__(256) kv_write_kernel(const __grid_constant__ KvWriteArgs a) {
+template <int NS, int NC>
+__global__ void __launch_bounds__(256) kv_write_kernel(const __grid_constant__ KvWriteArgs<NS, NC> a) {
     const int64_t tok_chunks = (int64_t)a.L * a.ntok * a.Hkv * a.CH;
     const int64_t total = 2 * (a.cow_chunks + tok_chunks);
     const int64_t tile = (int64_t)a.bs * a.CH;     // chunks per (block, head) tile
@@ -79,44 +84,62 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const __grid_constant__ K
     }
 }
 
+
+int sm_count() {
+    static int sms = [] {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        return n;
+    }();
+    return sms;
+}
+
+// One launch over tokens [tok_done, tok_done + ntok) and triples
+// [cow_done, cow_done + ncow) with a parameter block of NS slots / NC triples.
+template <int NS, int NC>
+cudaError_t launch_part(const KvWrite &w, int cow_done, int ncow, int tok_done, int ntok, cudaStream_t stream) {
+    static KvWriteArgs<NS, NC> args;   // filled per launch (host code is not reentrant per pool)
+    KvWriteArgs<NS, NC> &a = args;
+    a.k_pool = static_cast<uint4 *>(w.k_pool);
+    a.v_pool = static_cast<uint4 *>(w.v_pool);
+    a.k = static_cast<const uint4 *>(w.k);
+    a.v = static_cast<const uint4 *>(w.v);
+    a.L = w.L; a.NB = w.NB; a.Hkv = w.Hkv; a.bs = w.bs; a.CH = w.d / 8;
+    a.ntok_total = w.ntok;
+    a.ncow = ncow;
+    a.cow_chunks = 0;
+    for (int i = 0; i < ncow; ++i) {
+        a.cow[3 * i] = w.cow[3 * (cow_done + i)];
+        a.cow[3 * i + 1] = w.cow[3 * (cow_done + i) + 1];
+        a.cow[3 * i + 2] = w.cow[3 * (cow_done + i) + 2];
+        a.cow_chunks += (int64_t)w.L * w.Hkv * a.cow[3 * i + 2] * a.CH;
+    }
+    a.tok_begin = tok_done;
+    a.ntok = ntok;
+    for (int i = 0; i < ntok; ++i) a.slots[i] = w.slots[tok_done + i];
+    const int64_t total = 2 * (a.cow_chunks + (int64_t)w.L * ntok * w.Hkv * a.CH);
+    const int64_t want = (total + 255) / 256;
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 16));
+    kv_write_kernel<NS, NC><<<blocks, 256, 0, stream>>>(a);
+    count_launch();
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_kv_write(const KvWrite &w, cudaStream_t stream) {
-    static KvWriteArgs args;   // large; filled per launch (host code is not reentrant per pool)
-    int cow_done = 0, tok_done = 0;
-    int sms = 0, dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 152;
     if (w.ncow == 0 && w.ntok == 0) return cudaSuccess;
+    if (w.ntok <= kSmallSlots && w.ncow <= kSmallCow)
+        return launch_part<kSmallSlots, kSmallCow>(w, 0, w.ncow, 0, w.ntok, stream);
+    int cow_done = 0, tok_done = 0;
     while (cow_done < w.ncow || tok_done < w.ntok) {
-        KvWriteArgs &a = args;
-        a.k_pool = static_cast<uint4 *>(w.k_pool);
-        a.v_pool = static_cast<uint4 *>(w.v_pool);
-        a.k = static_cast<const uint4 *>(w.k);
-        a.v = static_cast<const uint4 *>(w.v);
-        a.L = w.L; a.NB = w.NB; a.Hkv = w.Hkv; a.bs = w.bs; a.CH = w.d / 8;
-        a.ntok_total = w.ntok;
-        a.ncow = std::min(kMaxCow, w.ncow - cow_done);
-        a.cow_chunks = 0;
-        for (int i = 0; i < a.ncow; ++i) {
-            a.cow[3 * i] = w.cow[3 * (cow_done + i)];
-            a.cow[3 * i + 1] = w.cow[3 * (cow_done + i) + 1];
-            a.cow[3 * i + 2] = w.cow[3 * (cow_done + i) + 2];
-            a.cow_chunks += (int64_t)w.L * w.Hkv * a.cow[3 * i + 2] * a.CH;
-        }
-        a.tok_begin = tok_done;
-        a.ntok = std::min(kMaxSlots, w.ntok - tok_done);
-        for (int i = 0; i < a.ntok; ++i) a.slots[i] = w.slots[tok_done + i];
-        const int64_t total = 2 * (a.cow_chunks + (int64_t)w.L * a.ntok * w.Hkv * a.CH);
-        const int64_t want = (total + 255) / 256;
-        const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * 16));
-        kv_write_kernel<<<blocks, 256, 0, stream>>>(a);
-        count_launch();
-        cudaError_t e = cudaGetLastError();
+        const int ncow = std::min(kMaxCow, w.ncow - cow_done), ntok = std::min(kMaxSlots, w.ntok - tok_done);
+        cudaError_t e = launch_part<kMaxSlots, kMaxCow>(w, cow_done, ncow, tok_done, ntok, stream);
         if (e != cudaSuccess) return e;
-        cow_done += a.ncow;
-        tok_done += a.ntok;
+        cow_done += ncow;
+        tok_done += ntok;
     }
     return cudaSuccess;
 }
