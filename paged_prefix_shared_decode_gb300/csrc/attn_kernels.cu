@@ -13,18 +13,22 @@
 // accumulate) with an online softmax in fp32 (base-2 exponent, scale * log2 e
 // folded into the scores).  Rows outside a tile's member interval, tokens past
 // the tile's end and draft tokens that are not ancestors-or-self of a node
-// are masked.  With at most 16 (32) rows the four warps split each tile's
-// tokens four (two) ways and combine their (m, l, o) through shared memory.
+// are masked.  With at most 16 rows the four warps split each tile's tokens
+// four ways (with at most 32 rows at head dim 128, two ways) and combine
+// their (m, l, o) through shared memory.
 //
 // A unit writes out (bf16) and lse (fp32, natural log) directly, or -- when
 // its rows' keys are split over several units -- normalised partial o and a
-// base-2 lse per row, which merge_kernel combines:
+// base-2 lse per row, which the merge kernels combine (one warp per query
+// head, or per kv head's group of query heads when there are many queries):
 //   out = sum_c w_c o_c / sum_c w_c,  w_c = 2^(lse_c - max lse),
 //   lse = max lse + log2(sum w)   (converted to natural log).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "kvp_internal.h"
@@ -447,8 +451,11 @@ __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kerne
         for (int i = threadIdx.x; i < ntile * 2; i += kThreads) dst[i] = src[i];
         __syncthreads();
         const int rows = it.n_members * a.G;
+        // The two-way split pays at head dim 128 (two CTAs per SM leave few
+        // warps to hide latency); at head dim 64 the extra copy of the tile
+        // loop costs more in instruction fetch than the split gains.
         if (rows <= 16) run_unit<D, 4>(a, it, l, kvh, ntile, smem, s_tiles);
-        else if (rows <= 32) run_unit<D, 2>(a, it, l, kvh, ntile, smem, s_tiles);
+        else if (D == 128 && rows <= 32) run_unit<D, 2>(a, it, l, kvh, ntile, smem, s_tiles);
         else run_unit<D, 1>(a, it, l, kvh, ntile, smem, s_tiles);
         __syncthreads();
     }
@@ -504,6 +511,139 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const AttnLaunch a) {
     if (a.lse && lane == 0)
         a.lse[((size_t)l * a.nq + qt) * a.Hq + h] =
             (wsum > 0.f ? Mb + __log2f(wsum) : -INFINITY) * 0.6931471805599453f;
+}
+
+// One warp per (layer, query token, kv head).  The G query heads of a kv
+// head share the query's merge entries, and one entry's partial rows for
+// those heads are G * D contiguous floats, so the warp loads the entry list
+// once and reads each entry as one coalesced block.  Lane p of a chunk of
+// 32 / G entries holds the weight of (entry p / G, head p % G).
+constexpr int kMergeWarps = 2;
+constexpr int kMergeCached = 4;             // entry chunks kept in registers from the max pass
+constexpr long long kMergeGroupMin = 2048;   // group warps over all layers
+
+template <int D, int G>
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_group_kernel(const AttnLaunch a) {
+    constexpr int NF4 = G * D / 4;        // float4s per entry
+    constexpr int K = (NF4 + 31) / 32;    // float4s per lane
+    constexpr int E = 32 / G;             // entries per chunk
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * kMergeWarps + warp;
+    const int qt = gw / a.Hkv, kvh = gw % a.Hkv, l = blockIdx.y;
+    if (qt >= a.nq) return;
+    const MergeDesc md = a.merge[qt];
+    if (md.cnt == 0) return;
+    const size_t rb = ((size_t)l * a.Hkv + kvh) * a.P;
+    const int32_t *ent = a.entries + md.off;
+    const int g = lane % G, c0 = lane / G;
+    int ec[kMergeCached];
+    float lc[kMergeCached];
+#pragma unroll
+    for (int i = 0; i < kMergeCached; ++i) {
+        ec[i] = 0;
+        if (c0 + i * E < md.cnt) ec[i] = __ldg(ent + c0 + i * E);
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMergeCached; ++i) {
+        lc[i] = -INFINITY;
+        if (c0 + i * E < md.cnt) lc[i] = a.part_lse[rb + ec[i] + g];
+        M = fmaxf(M, lc[i]);
+    }
+    for (int c = c0 + kMergeCached * E; c < md.cnt; c += E) M = fmaxf(M, a.part_lse[rb + __ldg(ent + c) + g]);
+#pragma unroll
+    for (int off = 16; off >= G; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float Mb = M == -INFINITY ? 0.f : M;   // lane's head g
+
+    float4 acc[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    auto chunk = [&](int base, int e, float lv) {
+        const float w = exp2_sfu(lv - Mb);   // 0 for pairs past the end
+        wsum += w;
+        const int n = min(E, md.cnt - base);
+#pragma unroll 4
+        for (int j = 0; j < n; ++j) {
+            const int ej = __shfl_sync(0xffffffffu, e, j * G);
+            const float4 *src = reinterpret_cast<const float4 *>(a.part_o + (rb + ej) * D);
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int f = lane + 32 * k;
+                const float wj = __shfl_sync(0xffffffffu, w, j * G + f / (D / 4));
+                if (NF4 % 32 == 0 || f < NF4) {
+                    const float4 x = src[f];
+                    acc[k].x += wj * x.x;
+                    acc[k].y += wj * x.y;
+                    acc[k].z += wj * x.z;
+                    acc[k].w += wj * x.w;
+                }
+            }
+        }
+    };
+#pragma unroll
+    for (int i = 0; i < kMergeCached; ++i)
+        if (i * E < md.cnt) chunk(i * E, ec[i], lc[i]);
+    for (int base = kMergeCached * E; base < md.cnt; base += E) {
+        int e = 0;
+        float lv = -INFINITY;
+        if (base + c0 < md.cnt) {
+            e = __ldg(ent + base + c0);
+            lv = a.part_lse[rb + e + g];
+        }
+        chunk(base, e, lv);
+    }
+#pragma unroll
+    for (int off = 16; off >= G; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+
+    const size_t ob = ((size_t)l * a.nq + qt) * a.Hq + (size_t)kvh * G;   // first output row
+    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) + ob * D;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int f = lane + 32 * k;
+        const float ws = __shfl_sync(0xffffffffu, wsum, f / (D / 4));
+        const float inv = ws > 0.f ? 1.f / ws : 0.f;
+        if (NF4 % 32 == 0 || f < NF4) {
+            uint2 v;
+            v.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
+            v.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
+            *reinterpret_cast<uint2 *>(dst + 4 * f) = v;
+        }
+    }
+    if (a.lse && lane < G)
+        a.lse[ob + lane] = (wsum > 0.f ? Mb + __log2f(wsum) : -INFINITY) * 0.6931471805599453f;
+}
+
+// KVP_MERGE=group / =head in the environment forces one merge kernel (tests,
+// ablations); by default the grouped kernel runs when there are many groups.
+int merge_mode() {
+    static int mode = [] {
+        const char *e = std::getenv("KVP_MERGE");
+        if (e && std::strcmp(e, "group") == 0) return 1;
+        if (e && std::strcmp(e, "head") == 0) return 2;
+        return 0;
+    }();
+    return mode;
+}
+
+template <int D>
+void launch_merge(const AttnLaunch &a, cudaStream_t stream) {
+    const long long groups = (long long)a.nq * a.Hkv;
+    dim3 grid((unsigned)((groups + kMergeWarps - 1) / kMergeWarps), a.L);
+    // with few groups, one warp per head keeps more loads in flight
+    const int mode = merge_mode();
+    const bool grouped = mode == 1 || (mode == 0 && groups * a.L >= kMergeGroupMin);
+    switch (grouped ? a.G : 0) {
+        case 1: merge_group_kernel<D, 1><<<grid, 32 * kMergeWarps, 0, stream>>>(a); return;
+        case 2: merge_group_kernel<D, 2><<<grid, 32 * kMergeWarps, 0, stream>>>(a); return;
+        case 4: merge_group_kernel<D, 4><<<grid, 32 * kMergeWarps, 0, stream>>>(a); return;
+        case 8: merge_group_kernel<D, 8><<<grid, 32 * kMergeWarps, 0, stream>>>(a); return;
+        case 16: merge_group_kernel<D, 16><<<grid, 32 * kMergeWarps, 0, stream>>>(a); return;
+        default: break;
+    }
+    const long long warps = (long long)a.nq * a.Hq;
+    dim3 g1((unsigned)((warps + kThreads / 32 - 1) / (kThreads / 32)), a.L);
+    merge_kernel<D><<<g1, kThreads, 0, stream>>>(a);
 }
 
 struct Occupancy {
@@ -586,9 +726,7 @@ cudaError_t launch_d(const AttnLaunch &a, cudaStream_t stream, cudaEvent_t befor
     }
     if (after && cudaEventRecord(after, stream) != cudaSuccess) return cudaErrorInvalidResourceHandle;
     if (a.P == 0) return cudaSuccess;
-    const long long warps = (long long)a.nq * a.Hq;
-    dim3 grid((unsigned)((warps + kThreads / 32 - 1) / (kThreads / 32)), a.L);
-    merge_kernel<D><<<grid, kThreads, 0, stream>>>(a);
+    launch_merge<D>(a, stream);
     count_launch();
     return cudaGetLastError();
 }

@@ -146,6 +146,15 @@ def test_gqa_group_16_and_single_sequence():
     run_decode(w)
 
 
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 8, 64), (8, 4, 128), (12, 2, 64), (32, 2, 128), (24, 8, 128)])
+def test_gqa_groups_with_split_prefix(Hq, Hkv, d):
+    """Query-head groups of 1, 2 and 16 (merged a whole group per warp) and of
+    6 and 3 (merged one head per warp), with a prefix long enough to be split
+    into many key ranges, so a query merges many partial rows."""
+    w = _custom([5, 0, 77], prefix=3000, Hq=Hq, Hkv=Hkv, d=d, layers=1)
+    run_decode(w)
+
+
 def test_fork_child_without_private_tokens_equals_parent():
     w = _custom([0, 0], prefix=300, step_tokens=0)
     w.batch = [0, 1, 2]
