@@ -43,8 +43,9 @@ enum {
 
 /* Device error word bits (kvp_device_error). */
 enum {
-    KVP_DEVERR_BLOCK_ID = 1,    /* a planned block id outside [0, NB): those tokens read as 0 */
-    KVP_DEVERR_TREE_PARENT = 2  /* a parent pointer not in [-1, i): treated as a root       */
+    KVP_DEVERR_BLOCK_ID = 1,     /* a planned block id outside [0, NB): those tokens read as 0 */
+    KVP_DEVERR_TREE_PARENT = 2,  /* a parent pointer not in [-1, i): treated as a root       */
+    KVP_DEVERR_WAIT_TIMEOUT = 4  /* a tcgen05 pipeline wait ran out: that CTA stopped early  */
 };
 
 /* ------------------------------------------------------------------ pool */

@@ -41,6 +41,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "../../include/kvp.h"
 #include "kvp_internal.h"
 
 namespace kvp {
@@ -405,7 +406,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if ((i & 1023) == 1023 && *s_abort) return false;
         }
         *s_abort = 1;
-        atomicOr(a.err, 4);
+        atomicOr(a.err, KVP_DEVERR_WAIT_TIMEOUT);
         return false;
     };
 
