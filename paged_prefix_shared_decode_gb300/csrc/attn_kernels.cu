@@ -433,16 +433,18 @@ __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kerne
     extern __shared__ __align__(128) unsigned char smem[];
     KvTile *s_tiles = reinterpret_cast<KvTile *>(smem + C::DESC_OFF);
     __shared__ int s_unit;
-    const int n_items = a.n_units / (a.L * a.Hkv);
     for (;;) {
         if (threadIdx.x == 0) s_unit = atomicAdd(a.counter, 1);
         __syncthreads();
         const int unit = s_unit;
         if (unit >= a.n_units) break;
-        // item-minor order: the items of one (layer, kv head) run together, so
-        // row tiles that read the same shared blocks meet in L2
-        const int item_idx = unit % n_items;
-        const int lk = unit / n_items;
+        // item-major order: items are sorted longest first, so the longest
+        // units start first (over every layer and kv head) and the shortest
+        // fill the tail; row tiles of one item, adjacent in the list, are
+        // L * Hkv units apart, well within the units in flight, so they still
+        // read their shared blocks from L2
+        const int item_idx = unit / (a.L * a.Hkv);
+        const int lk = unit % (a.L * a.Hkv);
         const int kvh = lk % a.Hkv, l = lk / a.Hkv;
         const WorkItem it = a.items[item_idx];
         const int ntile = it.tile_end - it.tile_begin;
