@@ -9,6 +9,7 @@ Contents:
   attention.c    -- fp64 definition of decode and tree-verify attention (C,
                     OpenMP over (layer, query, head)), built into liboracle.so
   pool_model.py  -- the block pool / fork / copy-on-write bookkeeping model
+  radix_model.py -- the radix-tree prefix cache over the pool's blocks
   this file      -- ctypes wrappers and a helper that replays a workload's
                     op trace through the model into the oracle's own host pool
 
@@ -26,6 +27,7 @@ import threading
 import numpy as np
 
 from .pool_model import PoolModel, PoolError, initial_free_list, splitmix64_stream  # noqa: F401
+from .radix_model import RadixModel  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attention.c")

@@ -189,3 +189,38 @@ class PoolModel:
                 self.free.appendleft(b)
         del self.tables[s]
         del self.lens[s]
+
+    # -- holders other than sequences (the prefix cache) and sequences that
+    #    start from blocks someone already holds ("Trellis", section
+    #    "RadixAttention in Trellis": a session acquires existing prefix
+    #    blocks by raising their refcount instead of allocating)
+    def hold_block(self, b):
+        """One more reference to a live block."""
+        if not 0 <= b < self.NB or self.ref[b] <= 0:
+            raise PoolError("invalid", f"block {b} is not in use")
+        self.ref[b] += 1
+
+    def drop_block(self, b) -> bool:
+        """One reference fewer; True when the block went back to the pool."""
+        if not 0 <= b < self.NB or self.ref[b] <= 0:
+            raise PoolError("invalid", f"block {b} is not in use")
+        self.ref[b] -= 1
+        if self.ref[b] == 0:
+            self.free.appendleft(b)
+            return True
+        return False
+
+    def alloc_prefix(self, blocks):
+        """A new sequence whose table is `blocks` (one more reference each),
+        holding len(blocks) full blocks of tokens."""
+        if len(blocks) > self.MB:
+            raise PoolError("invalid", "block table capacity exceeded")
+        for b in blocks:
+            if not 0 <= b < self.NB or self.ref[b] <= 0:
+                raise PoolError("invalid", f"block {b} is not in use")
+        s = self._new_id()
+        self.tables[s] = list(blocks)
+        self.lens[s] = len(blocks) * self.bs
+        for b in blocks:
+            self.ref[b] += 1
+        return s
