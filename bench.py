@@ -461,10 +461,13 @@ def run_sweep(a, dev):
     out = []
     peak, _ = peaks()
     names = ["trellis0.0", "trellis0.25", "trellis0.5", "trellis0.75", "trellis0.9", "mcts",
-             "verify1", "verify8", "verify32"]
+             "verify1", "verify8", "verify32", "radix0.5", "radix0.9"]
     if a.sweep_set:
         names = [n for n in a.sweep_set.split(",") if n]
     for name in names:
+        if name.startswith("radix"):
+            out.append(prefix_cache_bench(kvp, float(name[len("radix"):]), with_oracle=not a.no_cpu_baseline))
+            continue
         sub = argparse.Namespace(**vars(a))
         sub.steps, sub.warmup = 5, 3
         if name.startswith("verify"):
@@ -530,6 +533,106 @@ def run_sweep(a, dev):
             del ws, flush
             torch.cuda.empty_cache()
     return out
+
+
+# ---------------------------------------------------- prefix cache (host)
+
+def _prefix_cache_op(api, system, prompts, fulls, bs):
+    """One pass of the Trellis session pattern through a prefix cache: warm
+    the system prompt, then per session match its prompt, start from the
+    cached blocks, take blocks for the rest of the prompt and the decoded
+    tokens, cache the finished session (fulls: prompt + decoded tokens),
+    unlock, free.  Returns (seconds, matched tokens)."""
+    pool, cache = api["new"]()
+    s = api["alloc"](pool)
+    api["reserve"](pool, s, len(system))
+    api["insert"](cache, system, api["table"](pool, s))
+    api["free"](pool, s)
+    matched = 0
+    t0 = time.perf_counter()
+    for prompt, full in zip(prompts, fulls):
+        got, lock = api["match"](cache, prompt)
+        matched += len(got) * bs
+        s = api["alloc_prefix"](pool, got)
+        api["reserve"](pool, s, len(full) - len(got) * bs)
+        api["insert"](cache, full, api["table"](pool, s))
+        api["unlock"](cache, lock)
+        api["free"](pool, s)
+    dt = time.perf_counter() - t0
+    api["close"](pool, cache)
+    return dt, matched
+
+
+def prefix_cache_bench(kvp, phi: float, with_oracle: bool, reps: int = 5):
+    """Host cost per session of the radix prefix cache through the public
+    API (bookkeeping pool, no device K/V), on the Trellis benchmark's session
+    pattern (64 sessions, 512-token prompts sharing 32 * round(phi * 512 / 32)
+    tokens, 64 decoded tokens each, 32-token blocks); the oracle beside it."""
+    import workloads as W
+    bs, sessions = 32, 64
+    system, prompts, generated = W.prefix_cache_sessions(phi, sessions=sessions)
+    nb = sessions * (len(prompts[0]) + len(generated[0])) // bs + 64
+    mb = (len(prompts[0]) + len(generated[0])) // bs + 2
+
+    def lib_new():
+        pool = kvp.kv_pool_create(kvp.PoolDesc(1, nb, bs, 1, 64, sessions + 2, mb, 1))
+        return pool, kvp.kvp_radix_create(pool)
+
+    def lib_close(pool, cache):
+        kvp.kvp_radix_destroy(cache)
+        kvp.kv_pool_destroy(pool)
+
+    lib = {"new": lib_new, "close": lib_close, "alloc": kvp.seq_alloc, "free": kvp.seq_free,
+           "reserve": lambda p, s, n: kvp.seq_reserve(p, s, n), "table": kvp.seq_block_table,
+           "insert": kvp.kvp_radix_insert, "alloc_prefix": kvp.seq_alloc_prefix,
+           "match": lambda c, t: kvp.kvp_radix_match(c, t, bs), "unlock": kvp.kvp_radix_unlock}
+    np_sys = np.asarray(system, np.int32)
+    np_prompts = [np.asarray(p, np.int32) for p in prompts]
+    np_fulls = [np.asarray(p + g, np.int32) for p, g in zip(prompts, generated)]
+    runs = [_prefix_cache_op(lib, np_sys, np_prompts, np_fulls, bs) for _ in range(reps)]
+    dt = float(np.median([r[0] for r in runs]))
+    # one match + unlock through ctypes on preallocated buffers (the C call
+    # itself, without the binding's array handling)
+    import ctypes
+    lib_ = kvp.load()
+    pool, cache = lib_new()
+    s = kvp.seq_alloc(pool)
+    kvp.seq_reserve(pool, s, len(system))
+    kvp.kvp_radix_insert(cache, np_sys, kvp.seq_block_table(pool, s))
+    q = np_prompts[0]
+    buf = np.zeros(len(q) // bs, np.int32)
+    nb_, lk = ctypes.c_int32(), ctypes.c_int32()
+    qp, bp = q.ctypes.data_as(ctypes.c_void_p), buf.ctypes.data_as(ctypes.c_void_p)
+    t0 = time.perf_counter()
+    for _ in range(2000):
+        lib_.kvp_radix_match(cache, qp, len(q), bp, len(buf), ctypes.byref(nb_), ctypes.byref(lk))
+        lib_.kvp_radix_unlock(cache, lk.value)
+    match_us = (time.perf_counter() - t0) / 2000 * 1e6
+    lib_close(pool, cache)
+    res = {"workload": f"radix{phi}", "sessions": sessions, "block": bs,
+           "match_unlock_us": match_us,
+           "host_us_per_session": dt / sessions * 1e6,
+           "hit_frac": runs[0][1] / sum(len(p) for p in prompts),
+           "api": "Python binding over the C ABI, int32 token arrays (match, seq_alloc_prefix, "
+                  "seq_reserve, insert, unlock, seq_free per session)"}
+    if with_oracle:
+        import oracle
+
+        def or_new():
+            m = oracle.PoolModel(nb, bs, sessions + 2, mb, alloc_seed=1)
+            return m, oracle.RadixModel(m)
+
+        orc = {"new": or_new, "close": lambda p, c: None, "alloc": lambda p: p.alloc(),
+               "free": lambda p, s: p.free_seq(s), "reserve": lambda p, s, n: p.append(s, n),
+               "table": lambda p, s: p.table(s), "insert": lambda c, t, b: c.insert(t, list(b)),
+               "alloc_prefix": lambda p, b: p.alloc_prefix(b), "match": lambda c, t: c.match(t),
+               "unlock": lambda c, lk: c.unlock(lk)}
+        fulls = [p + g for p, g in zip(prompts, generated)]
+        oruns = [_prefix_cache_op(orc, system, prompts, fulls, bs) for _ in range(2)]
+        assert oruns[0][1] == runs[0][1]
+        res["cpu_baseline"] = {"kind": "oracle", "cores": 1,
+                               "host_us_per_session": float(np.median([r[0] for r in oruns])) / sessions * 1e6}
+    return res
 
 
 # -------------------------------------------------------- oracle timing

@@ -94,6 +94,16 @@ int seq_fork(kvp_pool *pool, int32_t parent, int32_t *child_out);
  * reclaimed). */
 int seq_free(kvp_pool *pool, int32_t seq);
 
+/* A new sequence that starts from blocks someone already holds (a prefix
+ * found in the prefix cache below): its table is blocks[0..n_blocks), one
+ * more reference on each, and its length n_blocks * block_size ("Trellis",
+ * section "RadixAttention in Trellis": a session acquires the existing
+ * prefix blocks, raising their refcount, instead of allocating and
+ * recomputing them).  Every block must be in use (refcount > 0), else
+ * KVP_ERR_INVALID and nothing changes; KVP_ERR_OOM when no sequence slot is
+ * free. */
+int seq_alloc_prefix(kvp_pool *pool, const int32_t *blocks, int32_t n_blocks, int32_t *seq_out);
+
 /* Append ntok tokens' K and V (device, [L][ntok][Hkv][d] bf16 each) to a
  * sequence.  Copy-on-write ("Dendrite", section details: data is shared until
  * modified and copied only on write): if the last block is partially filled
@@ -135,6 +145,68 @@ int kvp_gather_tables(const kvp_pool *pool, const int32_t *seqs, int32_t n, int3
  * may be NULL) with an asynchronous host-to-device copy on `stream`. */
 int kvp_export_tables(kvp_pool *pool, const int32_t *seqs, int32_t n, int32_t width,
                       int32_t *d_tables, int32_t *d_lens, void *stream);
+
+/* ---------------------------------------------------------- prefix cache */
+
+/*
+ * A radix-tree prefix cache over a pool's blocks ("SGLang RadixAttention",
+ * sections on the node and edge structure, on the three operations match /
+ * split / insert, and on reference counting with LRU eviction; "Trellis",
+ * section "RadixAttention in Trellis").  The root is the empty sequence; the
+ * edge into a node holds a run of token ids and the ids of the blocks that
+ * store them.  Everything is in whole blocks of block_size tokens: a run is
+ * a whole number of blocks, a match is rounded down to whole agreeing
+ * blocks, and edges split on block boundaries.  The cache holds one pool
+ * reference on every block in the tree, so a block goes back to the pool
+ * only when neither the cache nor a sequence holds it.  "Last used" is a
+ * logical clock advanced by every match and insert and stamped on every node
+ * of the path it used.  Not thread-safe; destroy the cache before its pool.
+ */
+typedef struct kvp_radix kvp_radix;
+
+/* KVP_ERR_INVALID on a null pool; KVP_ERR_OOM if memory runs out. */
+int kvp_radix_create(kvp_pool *pool, kvp_radix **out);
+
+/* Drops the cache's references (each node's blocks last to first, children
+ * before parents) and frees the cache. */
+int kvp_radix_destroy(kvp_radix *cache);
+
+/* Longest cached prefix of tokens[0..n_tokens) in whole blocks: its block
+ * ids go to blocks_out (cap >= n_tokens / block_size) and their count to
+ * *n_blocks_out.  Every node whose blocks were returned (including one whose
+ * edge agreed only in part) is locked, i.e. not evictable, until
+ * kvp_radix_unlock(cache, *lock_out); *lock_out = -1 when nothing matched. */
+int kvp_radix_match(kvp_radix *cache, const int32_t *tokens, int32_t n_tokens, int32_t *blocks_out,
+                    int32_t cap, int32_t *n_blocks_out, int32_t *lock_out);
+
+/* Releases a lock from kvp_radix_match (-1: nothing to release).
+ * KVP_ERR_STATE, with nothing changed, if that path is not locked. */
+int kvp_radix_unlock(kvp_radix *cache, int32_t lock);
+
+/* Caches a sequence's whole blocks: tokens[0..n_tokens) are stored in
+ * blocks[0..n_blocks) (block j holds tokens [j*bs, (j+1)*bs)); only the
+ * first min(n_tokens / bs, n_blocks) blocks count.  The tree is walked as in
+ * match, splitting an edge that agrees for only part of its run (the upper
+ * part inherits the lower part's locks); what is not cached yet becomes a
+ * new leaf on which the cache takes one reference per block.  Blocks already
+ * cached for an equal prefix are kept.  Every new block must be in use, else
+ * KVP_ERR_INVALID and nothing changes. */
+int kvp_radix_insert(kvp_radix *cache, const int32_t *tokens, int32_t n_tokens, const int32_t *blocks,
+                     int32_t n_blocks);
+
+/* Until the pool has need_free free blocks: the unlocked leaf used longest
+ * ago gives its blocks back (last to first) and leaves the tree; a parent
+ * left childless and unlocked is then a leaf like any other.  *freed_out =
+ * blocks that went back to the pool.  KVP_OK when met, KVP_ERR_OOM when
+ * nothing more is evictable. */
+int kvp_radix_evict(kvp_radix *cache, int32_t need_free, int32_t *freed_out);
+
+/* Canonical dump for tests and tools: depth first from the root, children
+ * in increasing order of their first block's tokens; per node the int32
+ * words depth, locks, stamp, n_tokens, tokens..., n_blocks, blocks...
+ * *n_out = words needed; KVP_ERR_INVALID (nothing written) when cap is too
+ * small. */
+int kvp_radix_dump(const kvp_radix *cache, int32_t *out, int64_t cap, int64_t *n_out);
 
 /* ------------------------------------------------------------- attention */
 

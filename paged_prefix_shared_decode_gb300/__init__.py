@@ -99,6 +99,14 @@ _SIGS = {
     "paged_decode_attention_noalloc": ([_P, _P, _P, _P, _P, _I32, _I32, ctypes.POINTER(AttnDesc), _P, _P,
                                         _P], ctypes.c_int),
     "kvp_kernel_launches": ([ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+    "seq_alloc_prefix": ([_P, _P, _I32, _I32P], ctypes.c_int),
+    "kvp_radix_create": ([_P, ctypes.POINTER(_P)], ctypes.c_int),
+    "kvp_radix_destroy": ([_P], ctypes.c_int),
+    "kvp_radix_match": ([_P, _P, _I32, _P, _I32, _I32P, _I32P], ctypes.c_int),
+    "kvp_radix_unlock": ([_P, _I32], ctypes.c_int),
+    "kvp_radix_insert": ([_P, _P, _I32, _P, _I32], ctypes.c_int),
+    "kvp_radix_evict": ([_P, _I32, _I32P], ctypes.c_int),
+    "kvp_radix_dump": ([_P, _P, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
 }
 
 
@@ -197,6 +205,15 @@ def seq_reserve(pool, seq: int, ntok: int):
     _check(load().seq_reserve(pool, seq, ntok, slots.ctypes.data_as(_P), cow.ctypes.data_as(_P)),
            "seq_reserve")
     return slots[:ntok], cow
+
+
+def seq_alloc_prefix(pool, blocks) -> int:
+    """A new sequence whose table is `blocks` (already held elsewhere, e.g. a
+    prefix cache match) and whose length is len(blocks) * block_size."""
+    b, bp = _host_i32(blocks)
+    s = _I32()
+    _check(load().seq_alloc_prefix(pool, bp, len(b), ctypes.byref(s)), "seq_alloc_prefix")
+    return s.value
 
 
 def seq_block_table(pool, seq: int) -> np.ndarray:
@@ -342,3 +359,63 @@ def kvp_kernel_launches() -> int:
 
 def kvp_strerror(code: int) -> str:
     return load().kvp_strerror(code).decode()
+
+
+# ---------------------------------------------------------- prefix cache
+
+def kvp_radix_create(pool):
+    h = _P()
+    _check(load().kvp_radix_create(pool, ctypes.byref(h)), "kvp_radix_create")
+    return h.value
+
+
+def kvp_radix_destroy(cache):
+    _check(load().kvp_radix_destroy(cache), "kvp_radix_destroy")
+
+
+def kvp_radix_match(cache, tokens, block_size: int):
+    """(block ids of the longest cached prefix, lock); lock -1 when none."""
+    t, tp = _host_i32(tokens)
+    out = np.zeros(max(len(t) // block_size, 1), np.int32)
+    n, lock = _I32(), _I32()
+    _check(load().kvp_radix_match(cache, tp, len(t), out.ctypes.data_as(_P), len(out), ctypes.byref(n),
+                                  ctypes.byref(lock)), "kvp_radix_match")
+    return out[:n.value], lock.value
+
+
+def kvp_radix_unlock(cache, lock: int):
+    _check(load().kvp_radix_unlock(cache, lock), "kvp_radix_unlock")
+
+
+def kvp_radix_insert(cache, tokens, blocks):
+    t, tp = _host_i32(tokens)
+    b, bp = _host_i32(blocks)
+    _check(load().kvp_radix_insert(cache, tp, len(t), bp, len(b)), "kvp_radix_insert")
+
+
+def kvp_radix_evict(cache, need_free: int):
+    """(met, blocks returned to the pool)."""
+    freed = _I32()
+    rc = load().kvp_radix_evict(cache, need_free, ctypes.byref(freed))
+    if rc not in (KVP_OK, KVP_ERR_OOM):
+        _check(rc, "kvp_radix_evict")
+    return rc == KVP_OK, freed.value
+
+
+def kvp_radix_dump(cache):
+    """Canonical tree: [(depth, tokens, blocks, locks, stamp)] depth first,
+    children in increasing order of their first block's tokens."""
+    n = ctypes.c_int64()
+    load().kvp_radix_dump(cache, None, 0, ctypes.byref(n))   # sizes the buffer
+    w = np.zeros(max(n.value, 1), np.int32)
+    _check(load().kvp_radix_dump(cache, w.ctypes.data_as(_P), len(w), ctypes.byref(n)), "kvp_radix_dump")
+    out, i = [], 0
+    w = w[:n.value].tolist()
+    while i < len(w):
+        depth, locks, stamp, nt = w[i:i + 4]
+        toks = tuple(w[i + 4:i + 4 + nt])
+        nb = w[i + 4 + nt]
+        blks = tuple(w[i + 5 + nt:i + 5 + nt + nb])
+        out.append((depth, toks, blks, locks, stamp))
+        i += 5 + nt + nb
+    return out

@@ -6,6 +6,8 @@
 
 #include <cuda_runtime.h>
 
+struct kvp_pool;
+
 namespace kvp {
 
 constexpr int kTileTokens = 64;    // tokens per KV tile (one pipeline stage)
@@ -94,6 +96,16 @@ int attention_ctas_per_sm(int D);
 // Rows above which items of head dim D run on the tcgen05 kernel
 // (INT32_MAX: never).
 int tc_row_threshold(int head_dim);
+
+// Pool access for other holders of blocks (the prefix cache).  b must be
+// in use (refcount > 0) for hold and drop; drop returns true when the block
+// went back to the front of the free list.
+int32_t pool_block_size(const kvp_pool *p);
+int32_t pool_num_blocks(const kvp_pool *p);
+int32_t pool_free_count(const kvp_pool *p);
+bool pool_block_in_use(const kvp_pool *p, int32_t b);
+void pool_hold_block(kvp_pool *p, int32_t b);
+bool pool_drop_block(kvp_pool *p, int32_t b);
 
 // Counts every kernel launch the library makes.
 void count_launch();

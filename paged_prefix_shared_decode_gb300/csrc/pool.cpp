@@ -214,6 +214,22 @@ int seq_fork(kvp_pool *p, int32_t parent, int32_t *child_out) {
     return KVP_OK;
 }
 
+int seq_alloc_prefix(kvp_pool *p, const int32_t *blocks, int32_t n_blocks, int32_t *seq_out) {
+    if (!p || !seq_out || n_blocks < 0 || (n_blocks > 0 && !blocks)) return KVP_ERR_INVALID;
+    if (n_blocks > p->desc.max_blocks_per_seq) return KVP_ERR_INVALID;
+    for (int32_t i = 0; i < n_blocks; ++i)
+        if (blocks[i] < 0 || blocks[i] >= p->desc.num_blocks || p->ref[blocks[i]] <= 0) return KVP_ERR_INVALID;
+    if (p->free_ids.empty()) return KVP_ERR_OOM;
+    int32_t s = *p->free_ids.begin();
+    p->free_ids.erase(p->free_ids.begin());
+    p->live[s] = 1;
+    p->tables[s].assign(blocks, blocks + n_blocks);
+    p->lens[s] = n_blocks * p->desc.block_size;
+    for (int32_t i = 0; i < n_blocks; ++i) p->ref[blocks[i]] += 1;
+    *seq_out = s;
+    return KVP_OK;
+}
+
 int seq_free(kvp_pool *p, int32_t seq) {
     if (!is_live(p, seq)) return KVP_ERR_INVALID;
     auto &t = p->tables[seq];
@@ -372,3 +388,20 @@ const char *kvp_strerror(int code) {
 }
 
 }  // extern "C"
+
+namespace kvp {
+
+int32_t pool_block_size(const kvp_pool *p) { return p->desc.block_size; }
+int32_t pool_num_blocks(const kvp_pool *p) { return p->desc.num_blocks; }
+int32_t pool_free_count(const kvp_pool *p) { return (int32_t)p->free_.size(); }
+bool pool_block_in_use(const kvp_pool *p, int32_t b) {
+    return b >= 0 && b < p->desc.num_blocks && p->ref[b] > 0;
+}
+void pool_hold_block(kvp_pool *p, int32_t b) { p->ref[b] += 1; }
+bool pool_drop_block(kvp_pool *p, int32_t b) {
+    if (--p->ref[b] != 0) return false;
+    p->free_.push_back(b);   // the front of the free list
+    return true;
+}
+
+}  // namespace kvp

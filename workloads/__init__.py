@@ -24,7 +24,7 @@ import numpy as np
 __all__ = [
     "Shapes", "Workload", "normal_bf16", "f32_to_bf16_bits", "bf16_bits_to_f32",
     "tiny_fork", "dendrite", "trellis", "mcts", "verify_tree", "random_trace",
-    "append_kv", "step_kv", "step_q", "verify_q", "TINYLLAMA", "LLAMA3_8B",
+    "append_kv", "step_kv", "step_q", "verify_q", "TINYLLAMA", "LLAMA3_8B", "prefix_cache_sessions",
 ]
 
 
@@ -249,6 +249,25 @@ def trellis(phi: float, seed: int = 0, layers: int = 22, sessions: int = 64,
     w = Workload(f"trellis_phi{phi}", sh, ops, batch=list(range(1, sessions + 1)), seed=seed,
                  info=dict(phi=phi, prefix_blocks=p, realised_phi=32 * p / L_prompt))
     return _finish(w, extra_blocks=sessions * 4)
+
+
+def prefix_cache_sessions(phi: float, seed: int = 0, sessions: int = 64, L_prompt: int = 512,
+                          decode: int = 64, vocab: int = 32000):
+    """Token ids for the Trellis benchmark's session pattern: one shared
+    system prompt of 32 * prefixBlocks tokens, then per session a distinct
+    user suffix up to L_prompt tokens and `decode` generated tokens.
+    Returns (system, prompts, generated) as lists of int lists."""
+    p = trellis_prefix_blocks(phi, L_prompt, 32)
+    g = _philox(seed, 999_004, 0)
+    system = g.integers(0, vocab, 32 * p).tolist()
+    prompts, generated = [], []
+    for _ in range(sessions):
+        # a suffix that differs from every other one in its first token
+        suffix = g.integers(0, vocab, L_prompt - 32 * p).tolist()
+        suffix[0] = len(prompts) % vocab
+        prompts.append(system + suffix)
+        generated.append(g.integers(0, vocab, decode).tolist())
+    return system, prompts, generated
 
 
 def mcts(seed: int = 0, layers: int = 32, root: int = 2048, branching: int = 4,
