@@ -224,3 +224,57 @@ class PoolModel:
         for b in blocks:
             self.ref[b] += 1
         return s
+
+    def accept_draft(self, s, ctx_len, parent, accepted):
+        """Speculative accept after tree verify: keep the draft path from a
+        root of the draft tree down to node `accepted` (-1: keep none) and
+        drop the rest ("CAST", section on speculative decoding: the target
+        accepts a path of the draft tree).  Draft node i sits at position
+        ctx_len + i.  The path's tokens move to positions ctx_len, ctx_len+1,
+        ... in order; the length becomes ctx_len + len(path); blocks past the
+        new end are released (last to first).  A block that receives a moved
+        token and is shared with another sequence is copied first (copy on
+        write, in increasing block order, before anything is released).
+        Returns the path."""
+        self._live(s)
+        n = len(parent)
+        if ctx_len < 0 or ctx_len + n != self.lens[s] or not -1 <= accepted < n:
+            raise PoolError("invalid", "draft region does not match the sequence")
+        for i, p in enumerate(parent):
+            if not -1 <= p < i:
+                raise PoolError("invalid", f"parent of draft node {i}")
+        path = []
+        j = accepted
+        while j >= 0:
+            path.append(j)
+            j = parent[j]
+        path.reverse()
+        bs = self.bs
+        t = self.tables[s]
+        written = sorted({(ctx_len + i) // bs for i, node in enumerate(path) if node != i})
+        shared = [j for j in written if self.ref[t[j]] > 1]
+        if len(shared) > len(self.free):
+            raise PoolError("oom", "copy-on-write blocks")
+        for j in shared:
+            old, new = t[j], self._pop()
+            self.ref[old] -= 1
+            t[j] = new
+            self.cow_copies += 1
+            if self.store is not None:
+                for arr in self.store:
+                    arr[:, new] = arr[:, old]
+        if self.store is not None:
+            for arr in self.store:
+                kept = [arr[:, t[(ctx_len + node) // bs], :, (ctx_len + node) % bs, :].copy() for node in path]
+                for i, row in enumerate(kept):
+                    dp = ctx_len + i
+                    arr[:, t[dp // bs], :, dp % bs, :] = row
+        new_len = ctx_len + len(path)
+        keep = -(-new_len // bs)
+        for b in reversed(t[keep:]):
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.free.appendleft(b)
+        del t[keep:]
+        self.lens[s] = new_len
+        return path

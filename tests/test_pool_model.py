@@ -219,3 +219,103 @@ def test_alloc_seed_changes_ids_not_results():
         np.testing.assert_array_equal(out, res[0][1])
         np.testing.assert_array_equal(lse, res[0][2])
     np.testing.assert_array_equal(res[0][1][:, 4], res[0][1][:, 0])
+
+
+# -- speculative accept after tree verify ("CAST", section on speculative
+#    decoding: the target model accepts one path of the draft tree)
+
+def _draft_pool(bs=4, ctx=6, n=9, seed=1, L=2, Hkv=2, d=3, NB=40):
+    kp = np.zeros((L, NB, Hkv, bs, d), np.uint16)
+    vp = np.zeros_like(kp)
+    m = PoolModel(NB, bs, 8, 64, alloc_seed=seed, store=(kp, vp))
+    s = m.alloc()
+    tot = ctx + n
+    k = (np.arange(L * tot * Hkv * d, dtype=np.uint16) + 1).reshape(L, tot, Hkv, d)
+    m.append(s, tot, k, k + 5000)
+    return m, s, kp, vp
+
+
+def _rows(m, kp, s, lo, hi):
+    bs = m.bs
+    t = m.table(s)
+    return np.stack([kp[:, t[p // bs], :, p % bs, :] for p in range(lo, hi)], 1)
+
+
+def test_accept_on_a_chain_keeps_the_first_tokens_in_place():
+    m, s, kp, vp = _draft_pool()
+    before = _rows(m, kp, s, 0, 15)
+    free0 = m.free_count()
+    path = m.accept_draft(s, 6, [-1, 0, 1, 2, 3, 4, 5, 6, 7], 3)
+    assert path == [0, 1, 2, 3]
+    assert m.length(s) == 10 and len(m.table(s)) == 3
+    assert m.free_count() == free0 + 1          # 15 -> 10 tokens: 4 -> 3 blocks
+    assert np.array_equal(_rows(m, kp, s, 0, 10), before[:, :10])
+
+
+def test_accept_on_a_star_moves_one_token():
+    m, s, kp, vp = _draft_pool()
+    before_k, before_v = _rows(m, kp, s, 0, 15), _rows(m, vp, s, 0, 15)
+    path = m.accept_draft(s, 6, [-1] * 9, 5)
+    assert path == [5] and m.length(s) == 7
+    assert np.array_equal(_rows(m, kp, s, 0, 6), before_k[:, :6])
+    assert np.array_equal(_rows(m, kp, s, 6, 7)[:, 0], before_k[:, 6 + 5])
+    assert np.array_equal(_rows(m, vp, s, 6, 7)[:, 0], before_v[:, 6 + 5])
+
+
+def test_accept_none_drops_the_draft():
+    m, s, kp, vp = _draft_pool()
+    assert m.accept_draft(s, 6, [-1, 0, 0, 1, 1, 2, 2, 3, 3], -1) == []
+    assert m.length(s) == 6 and len(m.table(s)) == 2
+
+
+def test_accept_random_trees_against_brute_force():
+    rng = np.random.default_rng(4)
+    for trial in range(40):
+        bs = int(rng.choice([1, 2, 4, 16]))
+        ctx, n = int(rng.integers(0, 20)), int(rng.integers(1, 20))
+        m, s, kp, vp = _draft_pool(bs=bs, ctx=ctx, n=n, NB=200, seed=trial)
+        parent = [-1] + [int(rng.integers(-1, i)) for i in range(1, n)]
+        a = int(rng.integers(-1, n))
+        before = _rows(m, kp, s, 0, ctx + n)
+        # ancestors-or-self of a, found by marking rather than walking
+        anc = set()
+        for j in range(n):
+            x = a
+            while x > j:
+                x = parent[x]
+            if x == j and a >= 0:
+                anc.add(j)
+        path = m.accept_draft(s, ctx, parent, a)
+        assert path == sorted(anc)
+        assert m.length(s) == ctx + len(path)
+        assert len(m.table(s)) == -(-(ctx + len(path)) // bs)
+        got = _rows(m, kp, s, 0, ctx + len(path))
+        want = np.concatenate([before[:, :ctx], before[:, [ctx + j for j in path]]], 1)
+        assert np.array_equal(got, want)
+        assert m.free_count() == sum(1 for b in range(m.NB) if m.refcount(b) == 0)
+
+
+def test_accept_copies_a_shared_block_before_moving_into_it():
+    m, s, kp, vp = _draft_pool(bs=4, ctx=6, n=9)
+    sib = m.fork(s)                              # every block shared
+    sib_before = _rows(m, kp, sib, 0, 15)
+    cow0 = m.cow_copies
+    path = m.accept_draft(s, 6, [-1] * 9, 8)     # token 14 moves to 6: block 1 written
+    assert path == [8] and m.cow_copies == cow0 + 1
+    assert m.table(s)[0] == m.table(sib)[0] and m.table(s)[1] != m.table(sib)[1]
+    assert np.array_equal(_rows(m, kp, sib, 0, 15), sib_before)
+    assert np.array_equal(_rows(m, kp, s, 6, 7)[:, 0], sib_before[:, 14])
+    for b in range(m.NB):
+        want = sum(m.table(x).count(b) for x in m.live())
+        assert m.refcount(b) == want
+
+
+def test_accept_rejects_bad_input_without_change():
+    m, s, kp, vp = _draft_pool()
+    t0, n0 = m.table(s), m.length(s)
+    for ctx, parent, a in [(6, [-1, 0, 5, 0, 0, 0, 0, 0, 0], 2),   # parent after child
+                           (5, [-1] * 9, 0),                        # draft region mismatch
+                           (6, [-1] * 9, 9)]:                       # node out of range
+        with pytest.raises(PoolError):
+            m.accept_draft(s, ctx, parent, a)
+        assert m.table(s) == t0 and m.length(s) == n0
