@@ -94,6 +94,25 @@ int seq_fork(kvp_pool *pool, int32_t parent, int32_t *child_out);
  * reclaimed). */
 int seq_free(kvp_pool *pool, int32_t seq);
 
+/* Speculative accept after tree verify ("CAST", section on speculative
+ * decoding: the target model accepts one path of the draft tree).  The
+ * sequence holds ctx_len context tokens followed by n_draft draft tokens,
+ * draft node i at position ctx_len + i with parent[i] in [-1, i) (-1: a
+ * root), n_draft <= 64.  The path from a root down to node `accepted` (-1:
+ * none) is kept: its tokens move, in order, to positions ctx_len,
+ * ctx_len + 1, ... (K and V, every layer and kv head); the length becomes
+ * ctx_len + path length and the blocks past the new end are released, last
+ * first.  A block that receives a moved token and is shared with another
+ * sequence is copied first (copy-on-write).  Device work is one
+ * kv_move_kernel launch on `stream` (none when nothing moves; a pool without
+ * K/V storage updates its bookkeeping only).  path_out (n_draft entries,
+ * may be NULL) receives the kept node ids, root first, *n_path_out their
+ * count.  KVP_ERR_INVALID (bad sequence, lengths or parents) or
+ * KVP_ERR_OOM (no block to copy into) change nothing; KVP_ERR_CUDA: the
+ * bookkeeping is done but the launch failed. */
+int seq_accept_draft(kvp_pool *pool, int32_t seq, int32_t ctx_len, const int32_t *parent, int32_t n_draft,
+                     int32_t accepted, int32_t *path_out, int32_t *n_path_out, void *stream);
+
 /* A new sequence that starts from blocks someone already holds (a prefix
  * found in the prefix cache below): its table is blocks[0..n_blocks), one
  * more reference on each, and its length n_blocks * block_size ("Trellis",

@@ -100,6 +100,7 @@ _SIGS = {
                                         _P], ctypes.c_int),
     "kvp_kernel_launches": ([ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
     "seq_alloc_prefix": ([_P, _P, _I32, _I32P], ctypes.c_int),
+    "seq_accept_draft": ([_P, _I32, _I32, _P, _I32, _I32, _P, _I32P, _P], ctypes.c_int),
     "kvp_radix_create": ([_P, ctypes.POINTER(_P)], ctypes.c_int),
     "kvp_radix_destroy": ([_P], ctypes.c_int),
     "kvp_radix_match": ([_P, _P, _I32, _P, _I32, _I32P, _I32P], ctypes.c_int),
@@ -205,6 +206,17 @@ def seq_reserve(pool, seq: int, ntok: int):
     _check(load().seq_reserve(pool, seq, ntok, slots.ctypes.data_as(_P), cow.ctypes.data_as(_P)),
            "seq_reserve")
     return slots[:ntok], cow
+
+
+def seq_accept_draft(pool, seq: int, ctx_len: int, parent, accepted: int, stream=None) -> np.ndarray:
+    """Keep the draft path from a root to `accepted` (-1: none) right after
+    the context; returns the kept node ids, root first."""
+    par, pp = _host_i32(parent)
+    out = np.zeros(max(len(par), 1), np.int32)
+    n = _I32()
+    _check(load().seq_accept_draft(pool, seq, ctx_len, pp, len(par), accepted, out.ctypes.data_as(_P),
+                                   ctypes.byref(n), _stream(stream)), "seq_accept_draft")
+    return out[:n.value]
 
 
 def seq_alloc_prefix(pool, blocks) -> int:

@@ -25,6 +25,8 @@ constexpr int kMaxCow = 256;      // copy-on-write triples per launch
 // Decode appends are a few tokens: a small parameter block for those, since
 // every launch passes the whole block.
 constexpr int kSmallSlots = 64, kSmallCow = 16;
+constexpr int kMaxMoves = kMaxDraft;   // kept draft tokens per accept
+constexpr int kMaxMoveCow = kMaxDraft; // blocks copied before the moves (bs 1: one per token)
 
 template <int NS, int NC>
 struct KvWriteArgs {
@@ -85,6 +87,45 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const __grid_constant__ K
 }
 
 
+// Speculative accept: move the kept draft tokens down to the positions right
+// after the context.  One thread per (layer, kv head, 16-byte chunk of a
+// token row), K and V.  It first copies its chunk of every copy-on-write
+// block (all bs slots), then moves its chunk of each kept token in order.
+// The i-th kept draft node has index >= i, so a token's source slot is never
+// a slot that an earlier move of the same thread wrote: doing the moves in
+// order needs no synchronisation, and threads touch disjoint memory.
+struct KvMoveArgs {
+    uint4 *k_pool;
+    uint4 *v_pool;
+    int32_t L, NB, Hkv, bs, CH;
+    int32_t ncow, nmove;
+    int32_t cow[2 * kMaxMoveCow];   // (source block, copy block)
+    int32_t src[kMaxMoves];         // slots: block * bs + slot
+    int32_t dst[kMaxMoves];
+};
+
+__global__ void __launch_bounds__(256) kv_move_kernel(const __grid_constant__ KvMoveArgs a) {
+    const int64_t n = 2LL * a.L * a.Hkv * a.CH;
+    const int64_t tile = (int64_t)a.bs * a.CH;     // chunks per (block, head) tile
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (int64_t)gridDim.x * blockDim.x) {
+        uint4 *pool = (x & 1) ? a.v_pool : a.k_pool;
+        const int64_t y = x >> 1;
+        const int64_t c = y % a.CH, lh = y / a.CH;
+        const int64_t h = lh % a.Hkv, l = lh / a.Hkv;
+        const int64_t head = (l * a.NB * a.Hkv + h) * tile + c;    // + block * Hkv * tile + slot * CH
+        const int64_t blk_stride = (int64_t)a.Hkv * tile;
+        for (int i = 0; i < a.ncow; ++i)
+            for (int sl = 0; sl < a.bs; ++sl)
+                pool[head + a.cow[2 * i + 1] * blk_stride + sl * a.CH] =
+                    pool[head + a.cow[2 * i] * blk_stride + sl * a.CH];
+        for (int i = 0; i < a.nmove; ++i) {
+            const int32_t s = a.src[i], d = a.dst[i];
+            pool[head + (int64_t)(d / a.bs) * blk_stride + (d % a.bs) * a.CH] =
+                pool[head + (int64_t)(s / a.bs) * blk_stride + (s % a.bs) * a.CH];
+        }
+    }
+}
+
 int sm_count() {
     static int sms = [] {
         int dev = 0, n = 0;
@@ -128,6 +169,27 @@ cudaError_t launch_part(const KvWrite &w, int cow_done, int ncow, int tok_done, 
 }
 
 }  // namespace
+
+cudaError_t launch_kv_move(const KvMove &m, cudaStream_t stream) {
+    if (m.ncow == 0 && m.nmove == 0) return cudaSuccess;
+    if (m.ncow > kMaxMoveCow || m.nmove > kMaxMoves || m.d % 8 != 0) return cudaErrorInvalidValue;
+    KvMoveArgs a{};
+    a.k_pool = static_cast<uint4 *>(m.k_pool);
+    a.v_pool = static_cast<uint4 *>(m.v_pool);
+    a.L = m.L; a.NB = m.NB; a.Hkv = m.Hkv; a.bs = m.bs; a.CH = m.d / 8;
+    a.ncow = m.ncow;
+    a.nmove = m.nmove;
+    for (int i = 0; i < 2 * m.ncow; ++i) a.cow[i] = m.cow[i];
+    for (int i = 0; i < m.nmove; ++i) {
+        a.src[i] = m.src[i];
+        a.dst[i] = m.dst[i];
+    }
+    const int64_t n = 2LL * m.L * m.Hkv * a.CH;
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 16));
+    kv_move_kernel<<<blocks, 256, 0, stream>>>(a);
+    count_launch();
+    return cudaGetLastError();
+}
 
 cudaError_t launch_kv_write(const KvWrite &w, cudaStream_t stream) {
     if (w.ncow == 0 && w.ntok == 0) return cudaSuccess;

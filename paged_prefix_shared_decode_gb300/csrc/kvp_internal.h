@@ -16,6 +16,7 @@ constexpr int kMaxItemTiles = 128; // KV tiles per work item (descriptors staged
 constexpr int kTileTree = 1;       // tile flag: draft tokens under a tree mask
 constexpr int kMmaMaxRows = 64;    // rows of an mma.sync unit (4 warps x 16)
 constexpr int kTcRows = 256;       // rows of a tcgen05 unit: one 128-row tile or a pair
+constexpr int kMaxDraft = 64;      // draft tokens per sequence (64-bit ancestor masks)
 
 // One KV tile of a work item: tokens [tok0, tok0 + ntok) of one sequence,
 // whose physical blocks (in order) are blk[0..]: token t of the tile lives in
@@ -125,5 +126,20 @@ struct KvWrite {
 };
 
 cudaError_t launch_kv_write(const KvWrite &w, cudaStream_t stream);
+
+// Speculative accept on the device: copy-on-write block copies (all slots),
+// then kept draft tokens moved from src to dst slots in order.
+struct KvMove {
+    void *k_pool;
+    void *v_pool;
+    int32_t L, NB, Hkv, bs, d;
+    int32_t ncow;
+    const int32_t *cow;    // host: (source block, copy block) pairs
+    int32_t nmove;
+    const int32_t *src;    // host: block*bs + slot per kept token
+    const int32_t *dst;
+};
+
+cudaError_t launch_kv_move(const KvMove &m, cudaStream_t stream);
 
 }  // namespace kvp

@@ -375,7 +375,7 @@ int build_decode(const kvp_attn_desc &d, const int32_t *tables, const int32_t *l
 int build_verify(const kvp_attn_desc &d, const int32_t *tables, const int32_t *ctx, int32_t B,
                  int32_t n, int32_t MB, int sms, HostPlan &hp) {
     const int32_t bs = d.block_size, G = d.num_q_heads / d.num_kv_heads;
-    if (n <= 0 || n > 64) return KVP_ERR_INVALID;
+    if (n <= 0 || n > kMaxDraft) return KVP_ERR_INVALID;
     const int64_t tok_bytes = 2LL * d.num_kv_heads * d.head_dim * 2 * d.num_layers;
     TileSrc src{tables, MB, bs};
     std::vector<ProtoItem> protos;

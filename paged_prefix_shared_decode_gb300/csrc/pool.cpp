@@ -214,6 +214,74 @@ int seq_fork(kvp_pool *p, int32_t parent, int32_t *child_out) {
     return KVP_OK;
 }
 
+int seq_accept_draft(kvp_pool *p, int32_t seq, int32_t ctx_len, const int32_t *parent, int32_t n_draft,
+                     int32_t accepted, int32_t *path_out, int32_t *n_path_out, void *stream) {
+    if (!is_live(p, seq) || ctx_len < 0 || n_draft < 0 || n_draft > kvp::kMaxDraft) return KVP_ERR_INVALID;
+    if ((int64_t)ctx_len + n_draft != p->lens[seq] || accepted < -1 || accepted >= n_draft) return KVP_ERR_INVALID;
+    if (n_draft > 0 && !parent) return KVP_ERR_INVALID;
+    for (int32_t i = 0; i < n_draft; ++i)
+        if (parent[i] < -1 || parent[i] >= i) return KVP_ERR_INVALID;
+    // the accepted path, root first
+    int32_t path[kvp::kMaxDraft];
+    int32_t np = 0;
+    for (int32_t j = accepted; j >= 0; j = parent[j]) path[np++] = j;
+    std::reverse(path, path + np);
+    const int32_t bs = p->desc.block_size;
+    auto &t = p->tables[seq];
+    // blocks that receive a moved token and are shared: copied first
+    std::vector<int32_t> shared;
+    for (int32_t i = 0; i < np; ++i) {
+        if (path[i] == i) continue;
+        const int32_t j = (ctx_len + i) / bs;
+        if (p->ref[t[j]] > 1 && (shared.empty() || shared.back() != j)) shared.push_back(j);
+    }
+    if ((int64_t)shared.size() > (int64_t)p->free_.size()) return KVP_ERR_OOM;
+    p->cow.clear();
+    for (int32_t j : shared) {
+        const int32_t old = t[j], fresh = pop_block(p);
+        p->ref[old] -= 1;
+        t[j] = fresh;
+        p->cow_count += 1;
+        p->cow.push_back(old);
+        p->cow.push_back(fresh);
+    }
+    p->slots.clear();   // source slots
+    p->stage.clear();   // destination slots
+    for (int32_t i = 0; i < np; ++i) {
+        if (path[i] == i) continue;
+        const int32_t sp = ctx_len + path[i], dp = ctx_len + i;
+        p->slots.push_back(t[sp / bs] * bs + sp % bs);
+        p->stage.push_back(t[dp / bs] * bs + dp % bs);
+    }
+    int rc = KVP_OK;
+    if (p->k && (!p->cow.empty() || !p->slots.empty())) {
+        kvp::KvMove m{};
+        m.k_pool = p->k;
+        m.v_pool = p->v;
+        m.L = p->desc.num_layers;
+        m.NB = p->desc.num_blocks;
+        m.Hkv = p->desc.num_kv_heads;
+        m.bs = bs;
+        m.d = p->desc.head_dim;
+        m.ncow = (int32_t)shared.size();
+        m.cow = p->cow.data();
+        m.nmove = (int32_t)p->slots.size();
+        m.src = p->slots.data();
+        m.dst = p->stage.data();
+        if (kvp::launch_kv_move(m, (cudaStream_t)stream) != cudaSuccess) rc = KVP_ERR_CUDA;
+    }
+    // release the blocks past the new end, last first
+    const int32_t new_len = ctx_len + np;
+    const size_t keep = (size_t)((new_len + bs - 1) / bs);
+    for (size_t j = t.size(); j-- > keep;)
+        if (--p->ref[t[j]] == 0) p->free_.push_back(t[j]);
+    t.resize(keep);
+    p->lens[seq] = new_len;
+    if (path_out) std::copy(path, path + np, path_out);
+    if (n_path_out) *n_path_out = np;
+    return rc;
+}
+
 int seq_alloc_prefix(kvp_pool *p, const int32_t *blocks, int32_t n_blocks, int32_t *seq_out) {
     if (!p || !seq_out || n_blocks < 0 || (n_blocks > 0 && !blocks)) return KVP_ERR_INVALID;
     if (n_blocks > p->desc.max_blocks_per_seq) return KVP_ERR_INVALID;
