@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--no-sharing", action="store_true", help="ablation: every sequence reads its own blocks")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cost-table", action="store_true",
+                    help="print the verify cost table f(B, c, n) (one JSON line) and exit")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -535,6 +537,32 @@ def run_sweep(a, dev):
     return out
 
 
+# ------------------------------------------------- verify cost table (CAST)
+
+def cost_table(a, dev):
+    """Tree-verify cost f(B, c, n) on this GPU, the table CAST's tree-size
+    choice consumes ("CAST", section on the verification cost model: the
+    cost of verifying n draft tokens grows with batch size B, context c and
+    n).  Llama-3-8B shapes, 32 layers, block 16, random draft trees of depth
+    <= 8; per point the event-timed verify call (plan upload, tree masks,
+    attention, merge) with L2 flushed between calls."""
+    rows = []
+    for B in (1, 4, 16, 32):
+        for c in (512, 2048, 8192):
+            for n in (16, 32, 64):
+                sub = argparse.Namespace(**vars(a))
+                sub.steps, sub.warmup = 5, 3
+                w = W.verify_tree(B, layers=32, ctx=c, n_draft=n)
+                res, _ = run_verify_bench(sub, w, 0, 1, dev)
+                rows.append({"B": B, "c": c, "n": n, "ms": res["ms_per_step"],
+                             "kernel_ms": res["roofline"]["kernel_ms"],
+                             "tensor_tflops": res["roofline"]["tensor_tflops"],
+                             "hbm_frac": res["roofline"]["frac"]})
+                import torch
+                torch.cuda.empty_cache()
+    return rows
+
+
 # ---------------------------------------------------- prefix cache (host)
 
 def _prefix_cache_op(api, system, prompts, fulls, bs):
@@ -705,6 +733,12 @@ def main():
         res = run_reference(a, rank, world)
         if res is not None:
             print(json.dumps(res), flush=True)
+        return 0
+    if a.cost_table:
+        if rank == 0:
+            import torch
+            print(json.dumps({"cost_table": cost_table(a, torch.device("cuda", local)),
+                              "unit": "ms per verify call"}), flush=True)
         return 0
     res, w = run_ours(a, rank, world, local)
     if rank == 0:
