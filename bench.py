@@ -613,7 +613,7 @@ def prefix_cache_bench(kvp, phi: float, with_oracle: bool, reps: int = 5):
     lib = {"new": lib_new, "close": lib_close, "alloc": kvp.seq_alloc, "free": kvp.seq_free,
            "reserve": lambda p, s, n: kvp.seq_reserve(p, s, n), "table": kvp.seq_block_table,
            "insert": kvp.kvp_radix_insert, "alloc_prefix": kvp.seq_alloc_prefix,
-           "match": lambda c, t: kvp.kvp_radix_match(c, t, bs), "unlock": kvp.kvp_radix_unlock}
+           "match": lambda c, t: kvp.kvp_radix_match(c, t), "unlock": kvp.kvp_radix_unlock}
     np_sys = np.asarray(system, np.int32)
     np_prompts = [np.asarray(p, np.int32) for p in prompts]
     np_fulls = [np.asarray(p + g, np.int32) for p, g in zip(prompts, generated)]

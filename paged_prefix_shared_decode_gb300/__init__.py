@@ -385,10 +385,10 @@ def kvp_radix_destroy(cache):
     _check(load().kvp_radix_destroy(cache), "kvp_radix_destroy")
 
 
-def kvp_radix_match(cache, tokens, block_size: int):
+def kvp_radix_match(cache, tokens):
     """(block ids of the longest cached prefix, lock); lock -1 when none."""
     t, tp = _host_i32(tokens)
-    out = np.zeros(max(len(t) // block_size, 1), np.int32)
+    out = np.zeros(max(len(t), 1), np.int32)   # at least n_tokens / block_size
     n, lock = _I32(), _I32()
     _check(load().kvp_radix_match(cache, tp, len(t), out.ctypes.data_as(_P), len(out), ctypes.byref(n),
                                   ctypes.byref(lock)), "kvp_radix_match")

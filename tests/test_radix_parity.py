@@ -43,7 +43,7 @@ def test_agentic_traffic_bit_exact(bs, seed, steps):
             base = rng.choice([system, *branches, []])
             q = base[:rng.randrange(0, len(base) + 1)] + [rng.randrange(1000) for _ in range(rng.randrange(1, 4 * bs))]
             got_m, lock_m = r.match(q)
-            got_l, lock_l = kvp.kvp_radix_match(c, q, bs)
+            got_l, lock_l = kvp.kvp_radix_match(c, q)
             assert list(got_l) == got_m
             assert (lock_m is None) == (lock_l == -1)
             locks.append((lock_m, lock_l))
@@ -132,14 +132,14 @@ def test_errors_change_nothing():
         kvp.seq_alloc_prefix(p, [free_blk])
     assert kvp.kvp_radix_dump(c) == before
     # unlocking a path that is not locked
-    _, lock = kvp.kvp_radix_match(c, list(range(8)), 4)
+    _, lock = kvp.kvp_radix_match(c, list(range(8)))
     kvp.kvp_radix_unlock(c, lock)
     with pytest.raises(kvp.KvpError) as e:
         kvp.kvp_radix_unlock(c, lock)
     assert e.value.code == kvp.KVP_ERR_STATE
     kvp.kvp_radix_unlock(c, -1)
     # everything locked: eviction reports that it could not free enough
-    _, lock = kvp.kvp_radix_match(c, list(range(12)), 4)
+    _, lock = kvp.kvp_radix_match(c, list(range(12)))
     kvp.seq_free(p, s)
     assert kvp.kvp_radix_evict(c, 32) == (False, 0)
     kvp.kvp_radix_unlock(c, lock)
@@ -150,7 +150,7 @@ def test_errors_change_nothing():
 
 def test_match_and_insert_take_microseconds():
     # host cost of the cache on a 4096-token system prompt shared by 256
-    # sessions, bs 16 (the paper's agentic setting, synthetic tokens)
+    # sessions, bs 16 (an agentic setting, synthetic tokens)
     rng = np.random.default_rng(0)
     bs, nb = 16, 8192
     p = kvp.kv_pool_create(kvp.PoolDesc(1, nb, bs, 1, 64, 300, 512, 1))
@@ -164,7 +164,7 @@ def test_match_and_insert_take_microseconds():
     t0 = time.perf_counter()
     for i in range(256):
         q = system + rng.integers(0, 32000, 64).tolist()
-        got, lock = kvp.kvp_radix_match(c, q, bs)
+        got, lock = kvp.kvp_radix_match(c, q)
         assert len(got) == 4096 // bs
         kvp.kvp_radix_unlock(c, lock)
     dt = (time.perf_counter() - t0) / 256
