@@ -10,6 +10,7 @@ Contents:
                     OpenMP over (layer, query, head)), built into liboracle.so
   pool_model.py  -- the block pool / fork / copy-on-write bookkeeping model
   radix_model.py -- the radix-tree prefix cache over the pool's blocks
+  kv4.py         -- a 4-bit KV page format (codes and per-row scales)
   this file      -- ctypes wrappers and a helper that replays a workload's
                     op trace through the model into the oracle's own host pool
 
