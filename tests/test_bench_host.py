@@ -56,3 +56,13 @@ def test_max_over_ranks_gloo_world2():
     assert all(p.exitcode == 0 for p in ps)
     assert out[0] == out[1] == 15.0
     assert bench.max_over_ranks(3.0, 1) == 3.0
+
+
+@pytest.mark.parametrize("phi,frac", [(0.0, 0.0), (0.5, 0.5), (0.9, 0.875)])
+def test_prefix_cache_bench_runs_on_the_host(phi, frac):
+    # the radix-cache sweep entry needs no GPU; it also checks that the
+    # library and the oracle served the same number of prompt tokens
+    import paged_prefix_shared_decode_gb300 as kvp
+    r = bench.prefix_cache_bench(kvp, phi, with_oracle=True, reps=1)
+    assert r["hit_frac"] == frac
+    assert r["host_us_per_session"] > 0 and r["cpu_baseline"]["host_us_per_session"] > 0
