@@ -64,6 +64,19 @@ struct Builder {
         return ((int64_t)tables[(size_t)s * MB + j] << 24) | (int64_t)valid(s, j);
     }
 
+    // First block index >= from where rows s0 and s1 differ in block id or
+    // valid tokens, or where either row ends.  Below the shorter row's last
+    // block both hold full blocks, so only that block's valid count needs
+    // comparing.
+    int32_t agree(int32_t s0, int32_t s1, int32_t from) const {
+        const int32_t lim = std::min(nblk[s0], nblk[s1]);
+        const int32_t *r0 = tables + (size_t)s0 * MB, *r1 = tables + (size_t)s1 * MB;
+        int32_t x = from;
+        while (x < lim && r0[x] == r1[x]) ++x;
+        if (x == lim && lim > from && valid(s0, lim - 1) != valid(s1, lim - 1)) x = lim - 1;
+        return x;
+    }
+
     // `members` share blocks [0, j); emit their subtree
     void build(const std::vector<int32_t> &members, int32_t j) {
         std::vector<int32_t> rest;
@@ -71,26 +84,42 @@ struct Builder {
             if (nblk[s] <= j) order.push_back(s);   // path ends here: first in order
             else rest.push_back(s);
         }
+        // group by the key of block j, groups in order of first appearance
+        // (a linear scan while there are few distinct keys, a hash map after)
         std::vector<std::vector<int32_t>> groups;
+        std::vector<int64_t> gkeys;
         std::unordered_map<int64_t, size_t> gi;
         for (int32_t s : rest) {
-            auto ins = gi.emplace(key(s, j), groups.size());
-            if (ins.second) groups.emplace_back();
-            groups[ins.first->second].push_back(s);
+            const int64_t k = key(s, j);
+            size_t g = groups.size();
+            if (gi.empty()) {
+                for (size_t i = 0; i < gkeys.size(); ++i)
+                    if (gkeys[i] == k) { g = i; break; }
+                if (g == groups.size() && gkeys.size() == 16)
+                    for (size_t i = 0; i < gkeys.size(); ++i) gi.emplace(gkeys[i], i);
+            }
+            if (!gi.empty()) {
+                auto ins = gi.emplace(k, groups.size());
+                g = ins.first->second;
+            }
+            if (g == groups.size()) {
+                groups.emplace_back();
+                gkeys.push_back(k);
+            }
+            groups[g].push_back(s);
         }
         for (auto &g : groups) {
-            int32_t j1 = j + 1;
-            if (g.size() == 1) {
-                j1 = nblk[g[0]];
-            } else {
-                for (;; ++j1) {
-                    bool same = true;
-                    for (int32_t s : g) {
-                        if (nblk[s] <= j1 || key(s, j1) != key(g[0], j1)) { same = false; break; }
-                    }
-                    if (!same) break;
-                }
+            if (g.size() == 1) {   // a single member: its whole remaining row is one segment
+                const int32_t s = g[0];
+                segs.push_back(Seg{j * bs, lens[s], s, (int32_t)order.size(), (int32_t)order.size() + 1});
+                order.push_back(s);
+                continue;
             }
+            // the group shares blocks [j, j1): j1 is the first block where
+            // some member's key differs from the first member's (or a row
+            // ends), found row by row
+            int32_t j1 = nblk[g[0]];
+            for (size_t i = 1; i < g.size() && j1 > j + 1; ++i) j1 = std::min(j1, agree(g[0], g[i], j + 1));
             size_t si = segs.size();
             segs.push_back(Seg{j * bs, std::min(j1 * bs, lens[g[0]]), g[0], 0, 0});
             int32_t lo = (int32_t)order.size();
