@@ -156,7 +156,7 @@ def _stream(stream):
 
 def _host_i32(a):
     a = np.ascontiguousarray(a, dtype=np.int32)
-    return a, a.ctypes.data_as(ctypes.c_void_p)
+    return a, a.ctypes.data
 
 
 # ------------------------------------------------------------------ pool
@@ -203,7 +203,7 @@ def seq_reserve(pool, seq: int, ntok: int):
     """Bookkeeping-only append: returns (slots int32 [ntok], cow int32 [3])."""
     slots = np.zeros(max(ntok, 1), np.int32)
     cow = np.zeros(3, np.int32)
-    _check(load().seq_reserve(pool, seq, ntok, slots.ctypes.data_as(_P), cow.ctypes.data_as(_P)),
+    _check(load().seq_reserve(pool, seq, ntok, slots.ctypes.data, cow.ctypes.data),
            "seq_reserve")
     return slots[:ntok], cow
 
@@ -214,7 +214,7 @@ def seq_accept_draft(pool, seq: int, ctx_len: int, parent, accepted: int, stream
     par, pp = _host_i32(parent)
     out = np.zeros(max(len(par), 1), np.int32)
     n = _I32()
-    _check(load().seq_accept_draft(pool, seq, ctx_len, pp, len(par), accepted, out.ctypes.data_as(_P),
+    _check(load().seq_accept_draft(pool, seq, ctx_len, pp, len(par), accepted, out.ctypes.data,
                                    ctypes.byref(n), _stream(stream)), "seq_accept_draft")
     return out[:n.value]
 
@@ -232,7 +232,7 @@ def seq_block_table(pool, seq: int) -> np.ndarray:
     n = _I32()
     _check(load().seq_block_table(pool, seq, None, 0, ctypes.byref(n)), "seq_block_table")
     out = np.zeros(max(n.value, 1), np.int32)
-    _check(load().seq_block_table(pool, seq, out.ctypes.data_as(_P), len(out), ctypes.byref(n)),
+    _check(load().seq_block_table(pool, seq, out.ctypes.data, len(out), ctypes.byref(n)),
            "seq_block_table")
     return out[:n.value]
 
@@ -263,10 +263,10 @@ def kvp_cow_count(pool) -> int:
 
 def kvp_gather_tables(pool, seqs, width: int):
     s, sp = _host_i32(seqs)
-    t = np.full((len(s), width), -1, np.int32)
-    lens = np.zeros(len(s), np.int32)
-    _check(load().kvp_gather_tables(pool, sp, len(s), width, t.ctypes.data_as(_P),
-                                    lens.ctypes.data_as(_P)), "kvp_gather_tables")
+    t = np.empty((len(s), width), np.int32)   # rows are padded with -1 by the library
+    lens = np.empty(len(s), np.int32)
+    _check(load().kvp_gather_tables(pool, sp, len(s), width, t.ctypes.data,
+                                    lens.ctypes.data), "kvp_gather_tables")
     return t, lens
 
 
@@ -390,7 +390,7 @@ def kvp_radix_match(cache, tokens):
     t, tp = _host_i32(tokens)
     out = np.zeros(max(len(t), 1), np.int32)   # at least n_tokens / block_size
     n, lock = _I32(), _I32()
-    _check(load().kvp_radix_match(cache, tp, len(t), out.ctypes.data_as(_P), len(out), ctypes.byref(n),
+    _check(load().kvp_radix_match(cache, tp, len(t), out.ctypes.data, len(out), ctypes.byref(n),
                                   ctypes.byref(lock)), "kvp_radix_match")
     return out[:n.value], lock.value
 
@@ -420,7 +420,7 @@ def kvp_radix_dump(cache):
     n = ctypes.c_int64()
     load().kvp_radix_dump(cache, None, 0, ctypes.byref(n))   # sizes the buffer
     w = np.zeros(max(n.value, 1), np.int32)
-    _check(load().kvp_radix_dump(cache, w.ctypes.data_as(_P), len(w), ctypes.byref(n)), "kvp_radix_dump")
+    _check(load().kvp_radix_dump(cache, w.ctypes.data, len(w), ctypes.byref(n)), "kvp_radix_dump")
     out, i = [], 0
     w = w[:n.value].tolist()
     while i < len(w):
