@@ -1,10 +1,12 @@
 /*
- * kvp.h -- C ABI of the paged, prefix-shared KV pool and its attention kernels
- * (GB300 / sm_103a).
+ * kvp.h -- C ABI of the paged, prefix-shared KV pool, its prefix cache and its
+ * attention kernels (GB300 / sm_103a).
  *
  * Conventions for every entry point:
  *   - returns KVP_OK (0) or a negative KVP_ERR_* code; out-parameters are
- *     written only on success and state is left unchanged on failure;
+ *     written only on success and state is left unchanged on failure, except
+ *     where a function says otherwise (kvp_radix_evict reports how far it
+ *     got; seq_accept_draft's bookkeeping stands when its launch fails);
  *   - "device" pointers are CUDA global memory on the current device, owned by
  *     the caller; "host" pointers are ordinary host memory owned by the caller;
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream);
