@@ -13,6 +13,13 @@ between timed steps, outside the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload dendrite|trellis0.5|mcts|verify8|...] [--sweep]
+                    [--sweep-set a,b,...] [--cost-table]
+
+--sweep adds short device-timed runs of the phi sweep, MCTS and verify, and
+host-timed runs of the radix prefix cache on the Trellis session pattern
+(radix0.0 / 0.5 / 0.9, with the oracle beside them).  --cost-table prints
+the tree-verify cost f(B, c, n) (B 1-32, contexts 512-8192, drafts of 16-64
+nodes) and exits.
 
 N > 1 runs independent replicas, one per GPU (torchrun; no data-path
 collective).  `--impl reference` times the fp64 CPU oracle on the host cores
