@@ -653,38 +653,48 @@ struct Occupancy {
     bool ok = false;
 };
 
+// Per device: the kernel's shared-memory attribute is set and its
+// occupancy queried once for each device that runs it.
 template <int D>
 Occupancy &occupancy() {
-    static Occupancy occ;
-    static std::once_flag once;
-    std::call_once(once, [] {
+    static Occupancy occ[kMaxDevices];
+    static std::once_flag once[kMaxDevices];
+    // no usable device (host-only planning): the configured occupancy
+    static Occupancy none{152, KCfg<D>::MIN_BLOCKS, false};
+    const int dev = current_device();
+    if (dev < 0) return none;
+    std::call_once(once[dev], [dev] {
         using C = KCfg<D>;
-        occ.per_sm = C::MIN_BLOCKS;
-        occ.sms = 152;
-        int dev = 0, n = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return;
+        Occupancy &o = occ[dev];
+        o.per_sm = C::MIN_BLOCKS;
+        o.sms = device_sm_count();
         if (cudaFuncSetAttribute(attn_item_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM) != cudaSuccess)
             return;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) occ.sms = sms;
+        int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_item_kernel<D>, kThreads, C::SMEM) ==
                 cudaSuccess && n > 0)
-            occ.per_sm = n;
-        occ.ok = true;
+            o.per_sm = n;
+        o.ok = true;
     });
-    return occ;
+    return occ[dev];
 }
 
-// A second stream (per thread) so that the tcgen05 and mma.sync kernels of one
-// call can share the GPU: the caller's stream forks to it and joins back.
+// A second stream per (thread, device) so that the tcgen05 and mma.sync
+// kernels of one call can share the GPU: the caller's stream forks to it and
+// joins back.  Created on first use, with that device current.
 struct SideStream {
     cudaStream_t s = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
-    bool ok = false;
-    SideStream() {
-        ok = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess &&
-             cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess &&
-             cudaEventCreateWithFlags(&join, cudaEventDisableTiming) == cudaSuccess;
+    int state = 0;   // 0: not tried, 1: ready, -1: creation failed
+    bool ensure() {
+        if (state == 0)
+            state = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess &&
+                            cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess &&
+                            cudaEventCreateWithFlags(&join, cudaEventDisableTiming) == cudaSuccess
+                        ? 1
+                        : -1;
+        return state == 1;
     }
 };
 
@@ -702,9 +712,11 @@ cudaError_t launch_d(const AttnLaunch &a, cudaStream_t stream, cudaEvent_t befor
         if (e0 != cudaSuccess) return e0;
     }
     const bool both = a.n_tc_units > 0 && a.n_units > 0;
-    thread_local SideStream side;
+    thread_local SideStream sides[kMaxDevices];
+    SideStream &side = sides[current_device()];   // occ.ok implies a valid device id
+    const bool fork = both && side.ensure();
     cudaStream_t mma_stream = stream;
-    if (both && side.ok) {
+    if (fork) {
         // fork: the mma.sync kernel runs beside the tcgen05 kernel, which then
         // takes one CTA per SM to leave room for it
         if (cudaEventRecord(side.fork, stream) != cudaSuccess ||
@@ -712,7 +724,7 @@ cudaError_t launch_d(const AttnLaunch &a, cudaStream_t stream, cudaEvent_t befor
             return cudaErrorUnknown;
         mma_stream = side.s;
     }
-    cudaError_t e = launch_attention_tc(a, stream, both && side.ok ? 1 : 0);
+    cudaError_t e = launch_attention_tc(a, stream, fork ? 1 : 0);
     if (e != cudaSuccess) return e;
     if (a.n_units > 0) {
         const int grid = a.n_units < occ.sms * occ.per_sm ? a.n_units : occ.sms * occ.per_sm;

@@ -909,21 +909,22 @@ struct TcOcc {
     bool ok = false;
 };
 
+// Per device: the shared-memory attribute is set once for each device.
 template <int D>
 TcOcc &tc_occ() {
-    static TcOcc occ;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return;
+    static TcOcc occ[kMaxDevices];
+    static std::once_flag once[kMaxDevices];
+    static TcOcc none;
+    const int dev = current_device();
+    if (dev < 0) return none;
+    std::call_once(once[dev], [dev] {
         if (cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  TcCfg<D>::SMEM) != cudaSuccess)
             return;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return;
-        occ.sms = sms;
-        occ.ok = true;
+        occ[dev].sms = device_sm_count();
+        occ[dev].ok = true;
     });
-    return occ;
+    return occ[dev];
 }
 
 template <int D>

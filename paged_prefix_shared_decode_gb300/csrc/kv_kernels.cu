@@ -126,23 +126,13 @@ __global__ void __launch_bounds__(256) kv_move_kernel(const __grid_constant__ Kv
     }
 }
 
-int sm_count() {
-    static int sms = [] {
-        int dev = 0, n = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 152;
-        return n;
-    }();
-    return sms;
-}
-
 // One launch over tokens [tok_done, tok_done + ntok) and triples
 // [cow_done, cow_done + ncow) with a parameter block of NS slots / NC triples.
 template <int NS, int NC>
 cudaError_t launch_part(const KvWrite &w, int cow_done, int ncow, int tok_done, int ntok, cudaStream_t stream) {
-    static KvWriteArgs<NS, NC> args;   // filled per launch (host code is not reentrant per pool)
-    KvWriteArgs<NS, NC> &a = args;
+    // on the stack: kernel parameters are copied at launch, so calls on
+    // different pools (or threads) never share this block
+    KvWriteArgs<NS, NC> a;
     a.k_pool = static_cast<uint4 *>(w.k_pool);
     a.v_pool = static_cast<uint4 *>(w.v_pool);
     a.k = static_cast<const uint4 *>(w.k);
@@ -162,7 +152,7 @@ cudaError_t launch_part(const KvWrite &w, int cow_done, int ncow, int tok_done, 
     for (int i = 0; i < ntok; ++i) a.slots[i] = w.slots[tok_done + i];
     const int64_t total = 2 * (a.cow_chunks + (int64_t)w.L * ntok * w.Hkv * a.CH);
     const int64_t want = (total + 255) / 256;
-    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 16));
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)device_sm_count() * 16));
     kv_write_kernel<NS, NC><<<blocks, 256, 0, stream>>>(a);
     count_launch();
     return cudaGetLastError();
@@ -185,7 +175,7 @@ cudaError_t launch_kv_move(const KvMove &m, cudaStream_t stream) {
         a.dst[i] = m.dst[i];
     }
     const int64_t n = 2LL * m.L * m.Hkv * a.CH;
-    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 16));
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, (int64_t)device_sm_count() * 16));
     kv_move_kernel<<<blocks, 256, 0, stream>>>(a);
     count_launch();
     return cudaGetLastError();

@@ -108,6 +108,15 @@ bool pool_block_in_use(const kvp_pool *p, int32_t b);
 void pool_hold_block(kvp_pool *p, int32_t b);
 bool pool_drop_block(kvp_pool *p, int32_t b);
 
+// Devices the library keeps per-device state for (SM counts, kernel
+// attributes, side streams); ids at or above this fail their launches.
+constexpr int kMaxDevices = 64;
+// Current device id, or -1 when there is none or it is >= kMaxDevices.
+int current_device();
+// SM count of the current device, looked up once per device (152 if the
+// query fails).
+int device_sm_count();
+
 // Counts every kernel launch the library makes.
 void count_launch();
 long long launch_count();

@@ -68,8 +68,8 @@ extern "C" int paged_decode_attention_noalloc(const void *q, const void *k_pool,
                                               int32_t num_seqs, int32_t max_blocks,
                                               const kvp_attn_desc *desc, void *out, float *lse,
                                               void *stream) {
-    const size_t need = kvp_decode_workspace_size(desc, block_tables, seq_lens, num_seqs, max_blocks);
-    if (need == 0 || need > kScratchBytes) return KVP_ERR_INVALID;
+    // paged_decode_attention plans once and rejects a plan larger than the
+    // workspace it is given (KVP_ERR_INVALID) before it enqueues anything
     void *ws = nullptr;
     int rc = scratch_address(&ws);
     if (rc != KVP_OK) return rc;

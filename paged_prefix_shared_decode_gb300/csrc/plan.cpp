@@ -130,20 +130,6 @@ struct Builder {
     }
 };
 
-int sm_count_cached() {
-    static int sms = 0;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        int dev = 0, v = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-            sms = v;
-        else
-            sms = 152;
-    });
-    return sms;
-}
-
 struct HostPlan {
     std::vector<WorkItem> items;      // mma.sync kernel
     std::vector<WorkItem> tc_items;   // tcgen05 kernel
@@ -541,6 +527,23 @@ int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k
 
 }  // namespace
 
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+int device_sm_count() {
+    static std::atomic<int> cache[kMaxDevices] = {};
+    const int dev = current_device();
+    if (dev < 0) return 152;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
+    cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
@@ -554,7 +557,7 @@ size_t kvp_decode_workspace_size(const kvp_attn_desc *desc, const int32_t *block
                                  const int32_t *seq_lens, int32_t num_seqs, int32_t max_blocks) {
     if (!desc_ok(desc) || num_seqs <= 0 || max_blocks <= 0 || !block_tables || !seq_lens) return 0;
     HostPlan hp;
-    if (build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, sm_count_cached(), hp))
+    if (build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, device_sm_count(), hp))
         return 0;
     return layout(hp, *desc).total;
 }
@@ -566,7 +569,7 @@ int paged_decode_attention(const void *q, const void *k_pool, const void *v_pool
     if (!desc_ok(desc) || num_seqs <= 0 || max_blocks <= 0 || !block_tables || !seq_lens)
         return KVP_ERR_INVALID;
     HostPlan hp;
-    int rc = build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, sm_count_cached(), hp);
+    int rc = build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, device_sm_count(), hp);
     if (rc) return rc;
     return run(hp, *desc, q, k_pool, v_pool, num_seqs, nullptr, 0, out, lse, workspace, ws_bytes,
                (cudaStream_t)stream);
@@ -577,7 +580,7 @@ size_t kvp_verify_workspace_size(const kvp_attn_desc *desc, const int32_t *block
                                  int32_t max_blocks) {
     if (!desc_ok(desc) || batch <= 0 || !ctx_lens || !block_tables || max_blocks <= 0) return 0;
     HostPlan hp;
-    if (build_verify(*desc, block_tables, ctx_lens, batch, n_draft, max_blocks, sm_count_cached(), hp))
+    if (build_verify(*desc, block_tables, ctx_lens, batch, n_draft, max_blocks, device_sm_count(), hp))
         return 0;
     return layout(hp, *desc).total;
 }
@@ -591,7 +594,7 @@ int tree_verify_attention(const void *q, const int32_t *tree_parent, int32_t n_d
         !tree_parent)
         return KVP_ERR_INVALID;
     HostPlan hp;
-    int rc = build_verify(*desc, block_tables, ctx_lens, batch, n_draft, max_blocks, sm_count_cached(), hp);
+    int rc = build_verify(*desc, block_tables, ctx_lens, batch, n_draft, max_blocks, device_sm_count(), hp);
     if (rc) return rc;
     return run(hp, *desc, q, k_pool, v_pool, batch * n_draft, tree_parent, n_draft, out, lse,
                workspace, ws_bytes, (cudaStream_t)stream);
