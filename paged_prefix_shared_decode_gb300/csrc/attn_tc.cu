@@ -875,35 +875,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ------------------------------------------------------------------ host
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// 2-D view of a pool: rows = L*NB*Hkv*bs token rows of d bf16; box = 64
-// columns x box_rows rows, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *pool, int D, long long rows, int box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides, box,
-                    es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 struct TcOcc {
     int sms = 0;
     bool ok = false;
@@ -935,7 +906,7 @@ cudaError_t launch_tc_d(const AttnLaunch &a, cudaStream_t stream) {
     const int box_rows = bs < kTileTokens ? bs : kTileTokens;
     const long long rows = (long long)a.L * a.NB * a.Hkv * bs;
     alignas(64) CUtensorMap km, vm;
-    if (!make_map(&km, a.k_pool, D, rows, box_rows) || !make_map(&vm, a.v_pool, D, rows, box_rows))
+    if (!make_pool_map(&km, a.k_pool, D, rows, box_rows) || !make_pool_map(&vm, a.v_pool, D, rows, box_rows))
         return cudaErrorInvalidValue;
     // one CTA per SM (its shared memory and TMEM allow no more)
     const int grid = a.n_tc_units < occ.sms ? a.n_tc_units : occ.sms;
@@ -945,6 +916,59 @@ cudaError_t launch_tc_d(const AttnLaunch &a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+struct MapKey {
+    const void *pool;
+    long long rows;
+    int D, box_rows;
+};
+
+}  // namespace
+
+// 2-D view of a pool: rows = L*NB*Hkv*bs token rows of d bf16; box = 64
+// columns x box_rows rows, 128-byte swizzle.  The last few maps built on
+// this thread are kept, since every call on the same pool needs the same two.
+bool make_pool_map(CUtensorMap *m, const void *pool, int D, long long rows, int box_rows) {
+    constexpr int kCache = 4;
+    thread_local MapKey keys[kCache] = {};
+    thread_local CUtensorMap maps[kCache];
+    thread_local int next = 0;
+    for (int i = 0; i < kCache; ++i)
+        if (keys[i].pool == pool && keys[i].rows == rows && keys[i].D == D && keys[i].box_rows == box_rows) {
+            *m = maps[i];
+            return true;
+        }
+    auto fn = encode_fn();
+    if (!fn || !pool) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides, box,
+                    es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    keys[next] = MapKey{pool, rows, D, box_rows};
+    maps[next] = *m;
+    next = (next + 1) % kCache;
+    return true;
+}
 
 bool tc_path_supported(int L, int NB, int Hkv, int bs) {
     // TMA row coordinates are 32-bit

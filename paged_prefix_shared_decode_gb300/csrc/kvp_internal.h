@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 struct kvp_pool;
@@ -92,6 +93,11 @@ cudaError_t launch_attention(const AttnLaunch &a, cudaStream_t stream, cudaEvent
 cudaError_t launch_attention_tc(const AttnLaunch &a, cudaStream_t stream, int ctas_per_sm);
 // Whether the tcgen05 kernel can address this pool (32-bit TMA row index).
 bool tc_path_supported(int L, int NB, int Hkv, int bs);
+// TMA view of a K or V pool as rows = L*NB*Hkv*bs token rows of D bf16
+// (box: 64 columns x box_rows rows, 128-byte swizzle), from a small
+// per-thread cache.  False when the driver's encoder is unavailable or
+// rejects the view.
+bool make_pool_map(CUtensorMap *m, const void *pool, int D, long long rows, int box_rows);
 // CTAs of the mma.sync work-item kernel that fit on one SM for head dim D.
 int attention_ctas_per_sm(int D);
 // Rows above which items of head dim D run on the tcgen05 kernel
