@@ -23,8 +23,9 @@ def test_workloads_and_descriptions(name):
 def test_peaks_and_traffic_lookup():
     peak, kind = bench.peaks()
     assert peak > 1000 and kind in ("measured", "fallback")
-    t = bench.traffic_for_current_kernel()
-    assert t is None or t["dram_bytes_per_launch"] > 0
+    for name in ("dendrite", "trellis_phi0.9", "mcts", "no-such-workload"):
+        t = bench.traffic_for(name)
+        assert t is None or t["dram_bytes_per_launch"] > 0
 
 
 def _free_port():
