@@ -79,6 +79,29 @@ typedef struct {
  * which case seq_append / seq_append_batch return KVP_ERR_STATE (use
  * seq_reserve).  The pool never allocates or frees KV storage. */
 int kv_pool_create(const kvp_pool_desc *desc, void *k_storage, void *v_storage, kvp_pool **out);
+
+/*
+ * A pool of 4-bit pages ("Dendrite", section on FlashInfer kernels and
+ * TurboQuant integration: 4-bit KV compression that cuts KV memory 3.88x and
+ * is computed on directly; the quantiser is not given there).  Each (token,
+ * kv head) row of d values is kept as d signed 4-bit codes in [-7, 7] and one
+ * power-of-two scale 2^e, e an int8 in [-127, 127]:
+ *   e = the smallest integer with max|x| <= 7 * 2^e (-127 for a zero row),
+ *   code = x / 2^e rounded half to even, value = code * 2^e,
+ * 4 + 8/d bits per value (16 / 4.125 = 3.88x less than bf16 at d = 64).
+ * Storage, all device memory owned by the caller, 16-byte aligned:
+ *   k_codes, v_codes  [L][NB][Hkv][bs][d/2] bytes: element 2i of a row in
+ *                     the low nibble of byte i, 2i+1 in the high nibble
+ *                     (two's complement);
+ *   k_exps, v_exps    [L][NB][Hkv][bs] int8.
+ * Needs d = 64 or 128 and bs a multiple of 16, else KVP_ERR_INVALID.
+ * seq_append / seq_append_batch take bf16 K/V as for any pool and quantise
+ * them on the device (copy-on-write copies codes and exponents);
+ * seq_accept_draft moves codes and exponents.  Attention over such a pool:
+ * paged_decode_attention_kv4 with desc->kv_format = KVP_KV_4BIT.
+ */
+int kv_pool_create_kv4(const kvp_pool_desc *desc, void *k_codes, void *k_exps, void *v_codes,
+                       void *v_exps, kvp_pool **out);
 int kv_pool_destroy(kvp_pool *pool);
 
 /* New empty sequence ("allocate_sequence" in Dendrite's API example). */
@@ -242,10 +265,15 @@ typedef struct {
     int32_t use_sharing;   /* 1: blocks that several sequences share are read once per
                               tile of up to 64 query rows (cascade); 0: every sequence
                               reads its own blocks (the unshared baseline) */
+    int32_t kv_format;     /* KVP_KV_BF16 (0) or KVP_KV_4BIT (1): the pool's page format */
 } kvp_attn_desc;
 
-/* Device workspace bytes that paged_decode_attention needs for this batch
- * (same host tables and lengths as the call).  Returns 0 on invalid input. */
+enum { KVP_KV_BF16 = 0, KVP_KV_4BIT = 1 };
+
+/* Device workspace bytes that paged_decode_attention (or, with
+ * desc->kv_format = KVP_KV_4BIT, paged_decode_attention_kv4) needs for this
+ * batch (same host tables and lengths as the call).  Returns 0 on invalid
+ * input. */
 size_t kvp_decode_workspace_size(const kvp_attn_desc *desc, const int32_t *block_tables,
                                  const int32_t *seq_lens, int32_t num_seqs, int32_t max_blocks);
 
@@ -281,6 +309,20 @@ int paged_decode_attention(const void *q, const void *k_pool, const void *v_pool
                            int32_t max_blocks, const kvp_attn_desc *desc, void *out, float *lse,
                            void *workspace, size_t ws_bytes, void *stream);
 
+/*
+ * Decode attention over a pool of 4-bit pages (kv_pool_create_kv4): the same
+ * call and results as paged_decode_attention, with the keys and values being
+ * the pages' values code * 2^e.  k_codes / k_exps / v_codes / v_exps are the
+ * pool's storage; desc->kv_format must be KVP_KV_4BIT (paged_decode_attention
+ * rejects such a descriptor).  HBM traffic per token is (d/2 + 1) bytes per
+ * kv head for K and for V instead of 2d.
+ */
+int paged_decode_attention_kv4(const void *q, const void *k_codes, const void *k_exps,
+                               const void *v_codes, const void *v_exps, const int32_t *block_tables,
+                               const int32_t *seq_lens, int32_t num_seqs, int32_t max_blocks,
+                               const kvp_attn_desc *desc, void *out, float *lse, void *workspace,
+                               size_t ws_bytes, void *stream);
+
 size_t kvp_verify_workspace_size(const kvp_attn_desc *desc, const int32_t *block_tables,
                                  const int32_t *ctx_lens, int32_t batch, int32_t n_draft,
                                  int32_t max_blocks);
@@ -299,7 +341,7 @@ size_t kvp_verify_workspace_size(const kvp_attn_desc *desc, const int32_t *block
  * [batch].  Other arguments as for paged_decode_attention with
  * num_seqs = batch * n_draft query rows.  A bad parent pointer sets
  * KVP_DEVERR_TREE_PARENT in the workspace error word and that node is
- * treated as a root.
+ * treated as a root.  Pages must be bf16 (desc->kv_format = KVP_KV_BF16).
  */
 int tree_verify_attention(const void *q, const int32_t *tree_parent, int32_t n_draft,
                           const void *k_pool, const void *v_pool, const int32_t *block_tables,

@@ -17,17 +17,19 @@ import numpy as np
 
 __all__ = [
     "KvpError", "PoolDesc", "AttnDesc", "load", "lib_path",
-    "kv_pool_create", "kv_pool_destroy", "seq_alloc", "seq_fork", "seq_free", "seq_append",
+    "kv_pool_create", "kv_pool_create_kv4", "kv_pool_destroy", "seq_alloc", "seq_fork", "seq_free", "seq_append",
     "seq_append_batch", "seq_reserve", "seq_block_table", "seq_len", "block_refcount",
     "kvp_free_block_count", "kvp_cow_count", "kvp_gather_tables", "kvp_export_tables",
     "kvp_decode_workspace_size", "paged_decode_attention", "kvp_verify_workspace_size",
     "tree_verify_attention", "kvp_device_error", "kvp_decode_plan_stats", "kvp_strerror",
     "kvp_set_kernel_events", "kvp_kernel_launches", "paged_decode_attention_noalloc",
+    "paged_decode_attention_kv4", "KVP_KV_BF16", "KVP_KV_4BIT",
     "KVP_STATIC_WORKSPACE_BYTES",
     "KVP_OK", "KVP_ERR_INVALID", "KVP_ERR_OOM", "KVP_ERR_STATE", "KVP_ERR_CUDA", "KVP_ERR_DEVICE",
 ]
 
 KVP_OK, KVP_ERR_INVALID, KVP_ERR_OOM, KVP_ERR_STATE, KVP_ERR_CUDA, KVP_ERR_DEVICE = 0, -1, -2, -3, -4, -5
+KVP_KV_BF16, KVP_KV_4BIT = 0, 1   # page formats (kvp_attn_desc.kv_format)
 KVP_STATIC_WORKSPACE_BYTES = 32 << 20   # size of the library's own workspace (include/kvp.h)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -63,7 +65,8 @@ class AttnDesc(ctypes.Structure):
     _fields_ = [("num_layers", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
-                ("scale", ctypes.c_float), ("use_sharing", ctypes.c_int32)]
+                ("scale", ctypes.c_float), ("use_sharing", ctypes.c_int32),
+                ("kv_format", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -71,6 +74,7 @@ _I32 = ctypes.c_int32
 _I32P = ctypes.POINTER(ctypes.c_int32)
 _SIGS = {
     "kv_pool_create": ([ctypes.POINTER(PoolDesc), _P, _P, ctypes.POINTER(_P)], ctypes.c_int),
+    "kv_pool_create_kv4": ([ctypes.POINTER(PoolDesc), _P, _P, _P, _P, ctypes.POINTER(_P)], ctypes.c_int),
     "kv_pool_destroy": ([_P], ctypes.c_int),
     "seq_alloc": ([_P, _I32P], ctypes.c_int),
     "seq_fork": ([_P, _I32, _I32P], ctypes.c_int),
@@ -88,6 +92,8 @@ _SIGS = {
     "kvp_decode_workspace_size": ([ctypes.POINTER(AttnDesc), _P, _P, _I32, _I32], ctypes.c_size_t),
     "paged_decode_attention": ([_P, _P, _P, _P, _P, _I32, _I32, ctypes.POINTER(AttnDesc),
                                 _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "paged_decode_attention_kv4": ([_P, _P, _P, _P, _P, _P, _P, _I32, _I32, ctypes.POINTER(AttnDesc),
+                                    _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "kvp_verify_workspace_size": ([ctypes.POINTER(AttnDesc), _P, _P, _I32, _I32, _I32], ctypes.c_size_t),
     "tree_verify_attention": ([_P, _P, _I32, _P, _P, _P, _P, _I32, _I32, ctypes.POINTER(AttnDesc),
                                _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
@@ -165,6 +171,15 @@ def kv_pool_create(desc: PoolDesc, k_storage=None, v_storage=None):
     h = _P()
     _check(load().kv_pool_create(ctypes.byref(desc), _dev(k_storage), _dev(v_storage), ctypes.byref(h)),
            "kv_pool_create")
+    return h.value
+
+
+def kv_pool_create_kv4(desc: PoolDesc, k_codes, k_exps, v_codes, v_exps):
+    """A pool of 4-bit pages over caller storage: codes [L][NB][Hkv][bs][d/2]
+    uint8 and exponents [L][NB][Hkv][bs] int8, for K and for V."""
+    h = _P()
+    _check(load().kv_pool_create_kv4(ctypes.byref(desc), _dev(k_codes), _dev(k_exps), _dev(v_codes),
+                                     _dev(v_exps), ctypes.byref(h)), "kv_pool_create_kv4")
     return h.value
 
 
@@ -302,6 +317,17 @@ def paged_decode_attention(q, k_pool, v_pool, block_tables, seq_lens, desc: Attn
                                          t.shape[1], ctypes.byref(desc), _dev(out), _dev(lse),
                                          _dev(workspace), _ws_bytes(workspace, ws_bytes),
                                          _stream(stream)), "paged_decode_attention")
+
+
+def paged_decode_attention_kv4(q, k_codes, k_exps, v_codes, v_exps, block_tables, seq_lens,
+                               desc: AttnDesc, out, lse, workspace, ws_bytes=None, stream=None):
+    """Decode attention over a pool of 4-bit pages (desc.kv_format = KVP_KV_4BIT)."""
+    t, tp = _host_i32(block_tables)
+    ln, lp = _host_i32(seq_lens)
+    _check(load().paged_decode_attention_kv4(_dev(q), _dev(k_codes), _dev(k_exps), _dev(v_codes), _dev(v_exps),
+                                             tp, lp, t.shape[0], t.shape[1], ctypes.byref(desc), _dev(out),
+                                             _dev(lse), _dev(workspace), _ws_bytes(workspace, ws_bytes),
+                                             _stream(stream)), "paged_decode_attention_kv4")
 
 
 def paged_decode_attention_noalloc(q, k_pool, v_pool, block_tables, seq_lens, desc: AttnDesc, out,

@@ -17,7 +17,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-SOURCES = ["pool.cpp", "radix.cpp", "plan.cpp", "attn_kernels.cu", "attn_tc.cu", "kv_kernels.cu", "no_alloc.cu"]
+SOURCES = ["pool.cpp", "radix.cpp", "plan.cpp", "attn_kernels.cu", "attn_tc.cu", "kv_kernels.cu", "kv4_kernels.cu", "no_alloc.cu"]
 
 
 def _nvcc() -> str:

@@ -129,11 +129,30 @@ struct KCfg {
     static constexpr int KS = D / 16;   // k-steps of Q K^T
 };
 
-// One work unit with TS warps splitting each tile's tokens.
-template <int D, int TS>
+// 4-bit pages: a ring of staged codes and exponents, expanded into one bf16
+// K/V tile before each tile's math.
+template <int D>
+struct KCfg4 {
+    static constexpr int CH4 = D / 32;                     // 16-byte code chunks per row
+    static constexpr int CODE_BYTES = kTileTokens * D / 2; // one K (or V) tile of codes
+    static constexpr int NSTAGE = 3;
+    static constexpr int STAGE_BYTES = 2 * CODE_BYTES + 2 * kTileTokens;   // codes K, V; exponents K, V
+    static constexpr int BF_OFF = NSTAGE * STAGE_BYTES;    // bf16 K then V tile (the mma layout)
+    static constexpr int LUT_OFF = BF_OFF + 2 * KCfg<D>::TILE_BYTES;   // byte -> bf16x2 of its two codes
+    static constexpr int DESC_OFF = LUT_OFF + 256 * 4;
+    static constexpr int SMEM = DESC_OFF + kMaxItemTiles * (int)sizeof(KvTile);
+    // the token-split combine overlays the staging ring and bf16 tile
+    static_assert(4 * (KCfg<D>::NO * 4 + 4) * 32 * 4 <= LUT_OFF, "combine area");
+};
+
+// One work unit with TS warps splitting each tile's tokens.  KV4: the pool
+// holds 4-bit codes and row exponents (a.k_pool / a.v_pool are the codes).
+template <int D, int TS, bool KV4>
 __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it, int l, int kvh,
                                          int ntile, unsigned char *smem, const KvTile *s_tiles) {
     using C = KCfg<D>;
+    using C4 = KCfg4<D>;
+    constexpr int NSTAGE = KV4 ? C4::NSTAGE : C::NSTAGE;
     constexpr int TOKW = kTileTokens / TS;   // tokens per warp per tile
     constexpr int NT = TOKW / 8;             // score n-tiles per warp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -166,7 +185,87 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
     const size_t layer_base = (size_t)l * a.NB * a.Hkv * head_stride + (size_t)kvh * head_stride;
     const size_t block_stride = (size_t)a.Hkv * head_stride;
 
+    // 4-bit: codes of row r at row * D/2, exponent at row, row =
+    // ((l * NB + block) * Hkv + kvh) * bs + slot
+    auto issue4 = [&](int t) {
+        const KvTile &kt = s_tiles[t];
+        const int ntok = kt.ntok_flags & 0xFFFF;
+        const int jb = kt.tok0 >> bs_log2;
+        const uint32_t st = smem_addr(smem + (t % NSTAGE) * C4::STAGE_BYTES);
+        const uint8_t *kc = static_cast<const uint8_t *>(a.k_pool), *vc = static_cast<const uint8_t *>(a.v_pool);
+        const int8_t *ke = static_cast<const int8_t *>(a.k_exp), *ve = static_cast<const int8_t *>(a.v_exp);
+        const size_t lrow = (size_t)l * a.NB * a.Hkv;   // + block * Hkv + kvh, times bs
+        for (int x = threadIdx.x; x < kTileTokens * C4::CH4; x += kThreads) {
+            const int tok = x / C4::CH4, c = x % C4::CH4;
+            const uint8_t *sk = kc, *sv = vc;
+            int bytes = 0;
+            if (tok < ntok) {
+                const int pos = kt.tok0 + tok;
+                const int blk = kt.blk[(pos >> bs_log2) - jb];
+                if ((unsigned)blk < (unsigned)a.NB) {
+                    const size_t row = ((lrow + (size_t)blk * a.Hkv + kvh) << bs_log2) + (pos & bs_mask);
+                    sk = kc + row * (D / 2) + c * 16;
+                    sv = vc + row * (D / 2) + c * 16;
+                    bytes = 16;
+                } else if (c == 0) {
+                    atomicOr(a.err, 1);
+                }
+            }
+            cp_async16(st + tok * (D / 2) + c * 16, sk, bytes);
+            cp_async16(st + C4::CODE_BYTES + tok * (D / 2) + c * 16, sv, bytes);
+        }
+        // exponents: four groups of 16 tokens, each inside one block (tiles
+        // start on a block boundary and blocks are a multiple of 16 tokens)
+        if (threadIdx.x < 8) {
+            const int j = threadIdx.x & 3;
+            const bool is_v = threadIdx.x >= 4;
+            const int8_t *e = is_v ? ve : ke;
+            const int8_t *src = e;
+            int bytes = 0;
+            if (16 * j < ntok) {
+                const int pos = kt.tok0 + 16 * j;
+                const int blk = kt.blk[(pos >> bs_log2) - jb];
+                if ((unsigned)blk < (unsigned)a.NB) {
+                    src = e + ((lrow + (size_t)blk * a.Hkv + kvh) << bs_log2) + (pos & bs_mask);
+                    bytes = 16;
+                }
+            }
+            cp_async16(st + 2 * C4::CODE_BYTES + (is_v ? kTileTokens : 0) + 16 * j, src, bytes);
+        }
+    };
+    // expands the staged tile t into the bf16 tile: value = code * 2^e, by a
+    // table of each byte's two codes as bf16 pairs and an exact multiply by
+    // the power of two
+    auto expand4 = [&](int t) {
+        const unsigned char *stg = smem + (t % NSTAGE) * C4::STAGE_BYTES;
+        const uint32_t *lut = reinterpret_cast<const uint32_t *>(smem + C4::LUT_OFF);
+        for (int x = threadIdx.x; x < 2 * kTileTokens * C::CH; x += kThreads) {
+            const int kv = x / (kTileTokens * C::CH);
+            const int y = x % (kTileTokens * C::CH);
+            const int tok = y / C::CH, ch = y % C::CH;     // 8 values: codes bytes 4 ch .. 4 ch + 3
+            const uint32_t cw = *reinterpret_cast<const uint32_t *>(stg + kv * C4::CODE_BYTES + tok * (D / 2) + ch * 4);
+            const int e = (int)reinterpret_cast<const int8_t *>(stg + 2 * C4::CODE_BYTES + kv * kTileTokens)[tok];
+            // 2^e as bf16 (e >= -126: a normal number; -127: the subnormal 2^-127)
+            const uint32_t sb = e >= -126 ? (uint32_t)(e + 127) << 7 : 0x40u;
+            const uint32_t sb2 = sb | (sb << 16);
+            const __nv_bfloat162 sc2 = *reinterpret_cast<const __nv_bfloat162 *>(&sb2);
+            uint4 v;
+            uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const uint32_t pair = lut[(cw >> (8 * b)) & 0xFFu];
+                const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&pair), sc2);
+                vv[b] = *reinterpret_cast<const uint32_t *>(&r);
+            }
+            *reinterpret_cast<uint4 *>(smem + C4::BF_OFF + kv * C::TILE_BYTES + tok * D * 2 + ((ch ^ (tok & 7)) << 4)) = v;
+        }
+    };
+
     auto issue = [&](int t) {
+        if constexpr (KV4) {
+            issue4(t);
+            return;
+        }
         const KvTile &kt = s_tiles[t];
         const int ntok = kt.ntok_flags & 0xFFFF;
         const int jb = kt.tok0 >> bs_log2;
@@ -198,7 +297,7 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
     };
 
 #pragma unroll
-    for (int t = 0; t < C::NSTAGE - 1; ++t) {
+    for (int t = 0; t < NSTAGE - 1; ++t) {
         if (t < ntile) issue(t);
         cp_async_commit();
     }
@@ -224,10 +323,14 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
     for (int t = 0; t < ntile; ++t) {
-        cp_async_wait<C::NSTAGE - 2>();
+        cp_async_wait<NSTAGE - 2>();
         __syncthreads();
-        if (t + C::NSTAGE - 1 < ntile) issue(t + C::NSTAGE - 1);
+        if (t + NSTAGE - 1 < ntile) issue(t + NSTAGE - 1);
         cp_async_commit();
+        if constexpr (KV4) {
+            expand4(t);
+            __syncthreads();
+        }
 
         const KvTile &kt = s_tiles[t];
         const int ntok = kt.ntok_flags & 0xFFFF;
@@ -238,7 +341,7 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
         const int tb = sp * TOKW;
         if (!__any_sync(0xffffffffu, in0 || in1) || tb >= ntok) continue;
 
-        const uint32_t aK = smem_addr(smem + (t % C::NSTAGE) * C::STAGE_BYTES);
+        const uint32_t aK = KV4 ? smem_addr(smem + C4::BF_OFF) : smem_addr(smem + (t % C::NSTAGE) * C::STAGE_BYTES);
         const uint32_t aV = aK + C::TILE_BYTES;
 
         float s[NT][4];
@@ -427,12 +530,20 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
     }
 }
 
-template <int D>
+template <int D, bool KV4>
 __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kernel(const AttnLaunch a) {
     using C = KCfg<D>;
     extern __shared__ __align__(128) unsigned char smem[];
-    KvTile *s_tiles = reinterpret_cast<KvTile *>(smem + C::DESC_OFF);
+    KvTile *s_tiles = reinterpret_cast<KvTile *>(smem + (KV4 ? KCfg4<D>::DESC_OFF : C::DESC_OFF));
     __shared__ int s_unit;
+    if constexpr (KV4) {
+        // byte -> its two signed 4-bit codes (low nibble first) as bf16
+        uint32_t *lut = reinterpret_cast<uint32_t *>(smem + KCfg4<D>::LUT_OFF);
+        for (int b = threadIdx.x; b < 256; b += kThreads) {
+            const int lo = (b & 7) - (b & 8), hi = ((b >> 4) & 7) - ((b >> 4) & 8);
+            lut[b] = pack_bf16x2((float)lo, (float)hi);
+        }
+    }
     for (;;) {
         if (threadIdx.x == 0) s_unit = atomicAdd(a.counter, 1);
         __syncthreads();
@@ -456,9 +567,9 @@ __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kerne
         // The two-way split pays at head dim 128 (two CTAs per SM leave few
         // warps to hide latency); at head dim 64 the extra copy of the tile
         // loop costs more in instruction fetch than the split gains.
-        if (rows <= 16) run_unit<D, 4>(a, it, l, kvh, ntile, smem, s_tiles);
-        else if (D == 128 && rows <= 32) run_unit<D, 2>(a, it, l, kvh, ntile, smem, s_tiles);
-        else run_unit<D, 1>(a, it, l, kvh, ntile, smem, s_tiles);
+        if (rows <= 16) run_unit<D, 4, KV4>(a, it, l, kvh, ntile, smem, s_tiles);
+        else if (D == 128 && rows <= 32) run_unit<D, 2, KV4>(a, it, l, kvh, ntile, smem, s_tiles);
+        else run_unit<D, 1, KV4>(a, it, l, kvh, ntile, smem, s_tiles);
         __syncthreads();
     }
 }
@@ -655,7 +766,7 @@ struct Occupancy {
 
 // Per device: the kernel's shared-memory attribute is set and its
 // occupancy queried once for each device that runs it.
-template <int D>
+template <int D, bool KV4 = false>
 Occupancy &occupancy() {
     static Occupancy occ[kMaxDevices];
     static std::once_flag once[kMaxDevices];
@@ -668,11 +779,12 @@ Occupancy &occupancy() {
         Occupancy &o = occ[dev];
         o.per_sm = C::MIN_BLOCKS;
         o.sms = device_sm_count();
-        if (cudaFuncSetAttribute(attn_item_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM) != cudaSuccess)
+        const int smem_bytes = KV4 ? KCfg4<D>::SMEM : C::SMEM;
+        if (cudaFuncSetAttribute(attn_item_kernel<D, KV4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes) != cudaSuccess)
             return;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_item_kernel<D>, kThreads, C::SMEM) ==
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_item_kernel<D, KV4>, kThreads, smem_bytes) ==
                 cudaSuccess && n > 0)
             o.per_sm = n;
         o.ok = true;
@@ -726,9 +838,17 @@ cudaError_t launch_d(const AttnLaunch &a, cudaStream_t stream, cudaEvent_t befor
     }
     cudaError_t e = launch_attention_tc(a, stream, fork ? 1 : 0);
     if (e != cudaSuccess) return e;
-    if (a.n_units > 0) {
+    if (a.n_units > 0 && a.kv4) {
+        Occupancy &o4 = occupancy<D, true>();
+        if (!o4.ok) return cudaErrorInvalidDevice;
+        const int grid = a.n_units < o4.sms * o4.per_sm ? a.n_units : o4.sms * o4.per_sm;
+        attn_item_kernel<D, true><<<grid, kThreads, KCfg4<D>::SMEM, mma_stream>>>(a);
+        count_launch();
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    } else if (a.n_units > 0) {
         const int grid = a.n_units < occ.sms * occ.per_sm ? a.n_units : occ.sms * occ.per_sm;
-        attn_item_kernel<D><<<grid, kThreads, C::SMEM, mma_stream>>>(a);
+        attn_item_kernel<D, false><<<grid, kThreads, C::SMEM, mma_stream>>>(a);
         count_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -61,8 +61,11 @@ static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 struct AttnLaunch {
     const void *q;
-    const void *k_pool;
+    const void *k_pool;           // bf16 K, or the 4-bit codes (kv4)
     const void *v_pool;
+    const void *k_exp;            // kv4: row exponents
+    const void *v_exp;
+    int32_t kv4;
     int32_t NB, bs_log2, Hq, Hkv, G, nq, L, D;
     float scale_log2;
     const int32_t *tree_parent;   // null for decode
@@ -156,5 +159,31 @@ struct KvMove {
 };
 
 cudaError_t launch_kv_move(const KvMove &m, cudaStream_t stream);
+
+// The same two for a pool of 4-bit pages: codes [L][NB][Hkv][bs][d/2] bytes
+// (two signed 4-bit codes per byte, element 2i in the low nibble) and one
+// int8 power-of-two exponent per (token, kv head) row [L][NB][Hkv][bs].
+// Appended rows (bf16) are quantised on the device.
+struct Kv4Write {
+    void *k_codes, *v_codes, *k_exp, *v_exp;
+    const void *k, *v;     // appended bf16 [L][ntok][Hkv][d]
+    int32_t L, NB, Hkv, bs, d;
+    int32_t ntok;
+    const int32_t *slots;  // host: block*bs + slot per token
+    int32_t ncow;
+    const int32_t *cow;    // host: (src, dst, used) triples
+};
+cudaError_t launch_kv4_write(const Kv4Write &w, cudaStream_t stream);
+
+struct Kv4Move {
+    void *k_codes, *v_codes, *k_exp, *v_exp;
+    int32_t L, NB, Hkv, bs, d;
+    int32_t ncow;
+    const int32_t *cow;    // host: (source block, copy block) pairs
+    int32_t nmove;
+    const int32_t *src;    // host: block*bs + slot per kept token
+    const int32_t *dst;
+};
+cudaError_t launch_kv4_move(const Kv4Move &m, cudaStream_t stream);
 
 }  // namespace kvp

@@ -170,7 +170,8 @@ int tc_row_threshold(int head_dim) {
 namespace {
 
 bool tc_usable(const kvp_attn_desc &d) {
-    return tc_row_threshold(d.head_dim) != INT32_MAX &&
+    // 4-bit pages run on the mma.sync kernel only
+    return d.kv_format == KVP_KV_BF16 && tc_row_threshold(d.head_dim) != INT32_MAX &&
            tc_path_supported(d.num_layers, d.num_blocks, d.num_kv_heads, d.block_size);
 }
 
@@ -428,7 +429,8 @@ bool desc_ok(const kvp_attn_desc *d) {
         return false;
     // power-of-two block sizes >= 16: a 64-token tile touches at most 5 blocks
     const int32_t bs = d->block_size;
-    return bs >= 16 && bs <= (1 << 20) && (bs & (bs - 1)) == 0;
+    return bs >= 16 && bs <= (1 << 20) && (bs & (bs - 1)) == 0 &&
+           (d->kv_format == KVP_KV_BF16 || d->kv_format == KVP_KV_4BIT);
 }
 
 int log2_int(int32_t x) {
@@ -468,8 +470,11 @@ std::atomic<long long> g_launches{0};
 
 int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k_pool,
         const void *v_pool, int32_t nq, const int32_t *parent, int32_t n_draft, void *out,
-        float *lse, void *ws, size_t ws_bytes, cudaStream_t stream) {
+        float *lse, void *ws, size_t ws_bytes, cudaStream_t stream, const void *k_exp = nullptr,
+        const void *v_exp = nullptr) {
     if (!q || !k_pool || !v_pool || !out || !ws) return KVP_ERR_INVALID;
+    const bool kv4 = d.kv_format == KVP_KV_4BIT;
+    if (kv4 && (!k_exp || !v_exp || (((uintptr_t)k_exp | (uintptr_t)v_exp) & 15))) return KVP_ERR_INVALID;
     if (((uintptr_t)ws & 255) != 0) return KVP_ERR_INVALID;
     if (((uintptr_t)q | (uintptr_t)k_pool | (uintptr_t)v_pool | (uintptr_t)out) & 15)
         return KVP_ERR_INVALID;
@@ -499,6 +504,7 @@ int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k
     unsigned char *base = (unsigned char *)ws;
     AttnLaunch a{};
     a.q = q; a.k_pool = k_pool; a.v_pool = v_pool;
+    a.k_exp = k_exp; a.v_exp = v_exp; a.kv4 = kv4 ? 1 : 0;
     a.NB = d.num_blocks; a.bs_log2 = log2_int(d.block_size);
     a.Hq = d.num_q_heads; a.Hkv = d.num_kv_heads; a.G = d.num_q_heads / d.num_kv_heads;
     a.nq = nq; a.L = d.num_layers; a.D = d.head_dim;
@@ -566,13 +572,29 @@ int paged_decode_attention(const void *q, const void *k_pool, const void *v_pool
                            const int32_t *block_tables, const int32_t *seq_lens, int32_t num_seqs,
                            int32_t max_blocks, const kvp_attn_desc *desc, void *out, float *lse,
                            void *workspace, size_t ws_bytes, void *stream) {
-    if (!desc_ok(desc) || num_seqs <= 0 || max_blocks <= 0 || !block_tables || !seq_lens)
+    if (!desc_ok(desc) || desc->kv_format != KVP_KV_BF16 || num_seqs <= 0 || max_blocks <= 0 ||
+        !block_tables || !seq_lens)
         return KVP_ERR_INVALID;
     HostPlan hp;
     int rc = build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, device_sm_count(), hp);
     if (rc) return rc;
     return run(hp, *desc, q, k_pool, v_pool, num_seqs, nullptr, 0, out, lse, workspace, ws_bytes,
                (cudaStream_t)stream);
+}
+
+int paged_decode_attention_kv4(const void *q, const void *k_codes, const void *k_exps,
+                               const void *v_codes, const void *v_exps, const int32_t *block_tables,
+                               const int32_t *seq_lens, int32_t num_seqs, int32_t max_blocks,
+                               const kvp_attn_desc *desc, void *out, float *lse, void *workspace,
+                               size_t ws_bytes, void *stream) {
+    if (!desc_ok(desc) || desc->kv_format != KVP_KV_4BIT || num_seqs <= 0 || max_blocks <= 0 ||
+        !block_tables || !seq_lens)
+        return KVP_ERR_INVALID;
+    HostPlan hp;
+    int rc = build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, device_sm_count(), hp);
+    if (rc) return rc;
+    return run(hp, *desc, q, k_codes, v_codes, num_seqs, nullptr, 0, out, lse, workspace, ws_bytes,
+               (cudaStream_t)stream, k_exps, v_exps);
 }
 
 size_t kvp_verify_workspace_size(const kvp_attn_desc *desc, const int32_t *block_tables,
@@ -590,8 +612,8 @@ int tree_verify_attention(const void *q, const int32_t *tree_parent, int32_t n_d
                           const int32_t *ctx_lens, int32_t batch, int32_t max_blocks,
                           const kvp_attn_desc *desc, void *out, float *lse, void *workspace,
                           size_t ws_bytes, void *stream) {
-    if (!desc_ok(desc) || batch <= 0 || max_blocks <= 0 || !ctx_lens || !block_tables ||
-        !tree_parent)
+    if (!desc_ok(desc) || desc->kv_format != KVP_KV_BF16 || batch <= 0 || max_blocks <= 0 || !ctx_lens ||
+        !block_tables || !tree_parent)
         return KVP_ERR_INVALID;
     HostPlan hp;
     int rc = build_verify(*desc, block_tables, ctx_lens, batch, n_draft, max_blocks, device_sm_count(), hp);

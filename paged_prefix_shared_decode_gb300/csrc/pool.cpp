@@ -28,8 +28,11 @@
 
 struct kvp_pool {
     kvp_pool_desc desc{};
-    void *k = nullptr;
+    void *k = nullptr;       // bf16 K/V, or the 4-bit codes of a 4-bit pool
     void *v = nullptr;
+    void *k_exp = nullptr;   // 4-bit pool: row exponents
+    void *v_exp = nullptr;
+    bool kv4 = false;
     std::vector<int32_t> free_;            // back() is the front of the free list
     std::vector<int32_t> ref;
     std::vector<std::vector<int32_t>> tables;
@@ -126,6 +129,25 @@ int check_append(const kvp_pool *p, int32_t s, int32_t ntok,
 
 int issue_write(kvp_pool *p, const void *k, const void *v, int32_t ntok, void *stream) {
     if (ntok == 0 && p->cow.empty()) return KVP_OK;
+    if (p->kv4) {
+        kvp::Kv4Write w{};
+        w.k_codes = p->k;
+        w.v_codes = p->v;
+        w.k_exp = p->k_exp;
+        w.v_exp = p->v_exp;
+        w.k = k;
+        w.v = v;
+        w.L = p->desc.num_layers;
+        w.NB = p->desc.num_blocks;
+        w.Hkv = p->desc.num_kv_heads;
+        w.bs = p->desc.block_size;
+        w.d = p->desc.head_dim;
+        w.ntok = ntok;
+        w.slots = p->slots.data();
+        w.ncow = (int32_t)(p->cow.size() / 3);
+        w.cow = p->cow.data();
+        return kvp::launch_kv4_write(w, (cudaStream_t)stream) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+    }
     kvp::KvWrite w{};
     w.k_pool = p->k;
     w.v_pool = p->v;
@@ -146,24 +168,17 @@ int issue_write(kvp_pool *p, const void *k, const void *v, int32_t ntok, void *s
 
 bool aligned16(const void *ptr) { return ((uintptr_t)ptr & 15) == 0; }
 
-}  // namespace
 
-extern "C" {
+bool desc_valid(const kvp_pool_desc &d) {
+    return d.num_layers > 0 && d.num_blocks > 0 && d.block_size > 0 && d.num_kv_heads > 0 && d.head_dim > 0 &&
+           d.head_dim % 8 == 0 && d.max_seqs > 0 && d.max_blocks_per_seq > 0 &&
+           (int64_t)d.block_size * d.max_blocks_per_seq <= (int64_t)INT32_MAX / 2;
+}
 
-int kv_pool_create(const kvp_pool_desc *desc, void *k_storage, void *v_storage, kvp_pool **out) {
-    if (!desc || !out) return KVP_ERR_INVALID;
-    const kvp_pool_desc &d = *desc;
-    if (d.num_layers <= 0 || d.num_blocks <= 0 || d.block_size <= 0 || d.num_kv_heads <= 0 ||
-        d.head_dim <= 0 || d.head_dim % 8 != 0 || d.max_seqs <= 0 || d.max_blocks_per_seq <= 0)
-        return KVP_ERR_INVALID;
-    if ((k_storage == nullptr) != (v_storage == nullptr)) return KVP_ERR_INVALID;
-    if (k_storage && (!aligned16(k_storage) || !aligned16(v_storage))) return KVP_ERR_INVALID;
-    if ((int64_t)d.block_size * d.max_blocks_per_seq > (int64_t)INT32_MAX / 2) return KVP_ERR_INVALID;
+kvp_pool *new_pool(const kvp_pool_desc &d) {
     kvp_pool *p = new (std::nothrow) kvp_pool();
-    if (!p) return KVP_ERR_OOM;
+    if (!p) return nullptr;
     p->desc = d;
-    p->k = k_storage;
-    p->v = v_storage;
     std::vector<int32_t> a(d.num_blocks);
     for (int32_t i = 0; i < d.num_blocks; ++i) a[i] = i;
     if (d.alloc_seed != 0) {
@@ -179,6 +194,41 @@ int kv_pool_create(const kvp_pool_desc *desc, void *k_storage, void *v_storage, 
     p->lens.assign(d.max_seqs, 0);
     p->live.assign(d.max_seqs, 0);
     for (int32_t i = 0; i < d.max_seqs; ++i) p->free_ids.insert(i);
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_pool_create(const kvp_pool_desc *desc, void *k_storage, void *v_storage, kvp_pool **out) {
+    if (!desc || !out || !desc_valid(*desc)) return KVP_ERR_INVALID;
+    if ((k_storage == nullptr) != (v_storage == nullptr)) return KVP_ERR_INVALID;
+    if (k_storage && (!aligned16(k_storage) || !aligned16(v_storage))) return KVP_ERR_INVALID;
+    kvp_pool *p = new_pool(*desc);
+    if (!p) return KVP_ERR_OOM;
+    p->k = k_storage;
+    p->v = v_storage;
+    *out = p;
+    return KVP_OK;
+}
+
+int kv_pool_create_kv4(const kvp_pool_desc *desc, void *k_codes, void *k_exps, void *v_codes, void *v_exps,
+                       kvp_pool **out) {
+    if (!desc || !out || !desc_valid(*desc)) return KVP_ERR_INVALID;
+    const kvp_pool_desc &d = *desc;
+    // 16-byte code rows (d/2 bytes) and whole 16-byte groups of exponents per block
+    if ((d.head_dim != 64 && d.head_dim != 128) || d.block_size % 16 != 0) return KVP_ERR_INVALID;
+    if (!k_codes || !k_exps || !v_codes || !v_exps) return KVP_ERR_INVALID;
+    if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_exps) || !aligned16(v_exps))
+        return KVP_ERR_INVALID;
+    kvp_pool *p = new_pool(d);
+    if (!p) return KVP_ERR_OOM;
+    p->k = k_codes;
+    p->v = v_codes;
+    p->k_exp = k_exps;
+    p->v_exp = v_exps;
+    p->kv4 = true;
     *out = p;
     return KVP_OK;
 }
@@ -254,7 +304,24 @@ int seq_accept_draft(kvp_pool *p, int32_t seq, int32_t ctx_len, const int32_t *p
         p->stage.push_back(t[dp / bs] * bs + dp % bs);
     }
     int rc = KVP_OK;
-    if (p->k && (!p->cow.empty() || !p->slots.empty())) {
+    if (p->k && p->kv4 && (!p->cow.empty() || !p->slots.empty())) {
+        kvp::Kv4Move m{};
+        m.k_codes = p->k;
+        m.v_codes = p->v;
+        m.k_exp = p->k_exp;
+        m.v_exp = p->v_exp;
+        m.L = p->desc.num_layers;
+        m.NB = p->desc.num_blocks;
+        m.Hkv = p->desc.num_kv_heads;
+        m.bs = bs;
+        m.d = p->desc.head_dim;
+        m.ncow = (int32_t)shared.size();
+        m.cow = p->cow.data();
+        m.nmove = (int32_t)p->slots.size();
+        m.src = p->slots.data();
+        m.dst = p->stage.data();
+        if (kvp::launch_kv4_move(m, (cudaStream_t)stream) != cudaSuccess) rc = KVP_ERR_CUDA;
+    } else if (p->k && (!p->cow.empty() || !p->slots.empty())) {
         kvp::KvMove m{};
         m.k_pool = p->k;
         m.v_pool = p->v;

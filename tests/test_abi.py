@@ -1,6 +1,8 @@
 """The C ABI library loads without a GPU and exports every symbol that
 include/kvp.h declares; error codes map to messages."""
 import ctypes
+
+import numpy as np
 import os
 import re
 
@@ -60,3 +62,32 @@ def test_bookkeeping_pool_refuses_device_appends():
         kvp.seq_append(p, s, 0, 0, 1, stream=0)
     assert e.value.code == kvp.KVP_ERR_STATE
     kvp.kv_pool_destroy(p)
+
+
+def test_kv4_pool_and_descriptor_checks():
+    # a 4-bit pool needs d 64 or 128, blocks of a multiple of 16 tokens and
+    # four 16-byte aligned arrays; nothing is touched on the device here
+    a = 1 << 20   # any 16-byte aligned address: pool creation only records it
+    for d, bs in ((64, 16), (128, 32)):
+        p = kvp.kv_pool_create_kv4(kvp.PoolDesc(1, 8, bs, 2, d, 2, 4, 0), a, a, a, a)
+        kvp.kv_pool_destroy(p)
+    for d, bs in ((96, 16), (64, 8), (32, 16)):
+        with pytest.raises(kvp.KvpError):
+            kvp.kv_pool_create_kv4(kvp.PoolDesc(1, 8, bs, 2, d, 2, 4, 0), a, a, a, a)
+    with pytest.raises(kvp.KvpError):
+        kvp.kv_pool_create_kv4(kvp.PoolDesc(1, 8, 16, 2, 64, 2, 4, 0), a, a + 8, a, a)
+    with pytest.raises(kvp.KvpError):
+        kvp.kv_pool_create_kv4(kvp.PoolDesc(1, 8, 16, 2, 64, 2, 4, 0), a, 0, a, a)
+    # the 4-bit descriptor is refused by the bf16 entry points and vice versa
+    t = np.zeros((1, 1), np.int32)
+    ln = np.ones(1, np.int32)
+    d4 = kvp.AttnDesc(1, 4, 2, 64, 16, 8, 0.0, 1, kvp.KVP_KV_4BIT)
+    d16 = kvp.AttnDesc(1, 4, 2, 64, 16, 8, 0.0, 1, kvp.KVP_KV_BF16)
+    assert kvp.kvp_decode_workspace_size(d4, t, ln) > 0
+    with pytest.raises(kvp.KvpError):
+        kvp.paged_decode_attention(a, a, a, t, ln, d4, a, a, a, 1 << 20, stream=0)
+    with pytest.raises(kvp.KvpError):
+        kvp.paged_decode_attention_kv4(a, a, a, a, a, t, ln, d16, a, a, a, 1 << 20, stream=0)
+    bad = kvp.AttnDesc(1, 4, 2, 64, 16, 8, 0.0, 1, 7)   # no such page format
+    with pytest.raises(kvp.KvpError):
+        kvp.kvp_decode_workspace_size(bad, t, ln)
