@@ -272,15 +272,16 @@ def run_ours(a, rank, world, local):
             e.record(stream)
     torch.cuda.synchronize(dev)
 
+    # one step = kvp_decode_step on device buffers: append, plan from the
+    # pool's tables, attention
+    ios = [kvp.step_io(qd[i], out, lse, kd[i], vd[i]) for i in range(nsteps)]
+
     def step(i, timed_events=None):
-        kvp.seq_append_batch(r.pool, seqs, ntoks, kd[i], vd[i], stream=stream)
-        ht, hl = kvp.kvp_gather_tables(r.pool, seqs, MB)
         if timed_events is not None:
             kvp.kvp_set_kernel_events(timed_events[2], timed_events[3])
-        kvp.paged_decode_attention(qd[i], r.k_pool, r.v_pool, ht, hl, desc, out, lse, ws, ws_bytes,
-                                   stream=stream)
-        kvp.kvp_set_kernel_events(None, None)
-        return ht, hl
+        kvp.kvp_decode_step(r.pool, seqs, w.step_tokens, ios[i], desc, ws, ws_bytes, stream=stream)
+        if timed_events is not None:
+            kvp.kvp_set_kernel_events(None, None)
 
     for i in range(Wm):
         flush.fill_(i & 0xFF)
@@ -295,9 +296,9 @@ def run_ours(a, rank, world, local):
     for j in range(K):
         flush.fill_(j & 0xFF)
         ev[j][0].record(stream)
-        ht, hl = step(Wm + j, ev[j])
+        step(Wm + j, ev[j])
         ev[j][1].record(stream)
-        step_tables.append((ht, hl))
+        step_tables.append(kvp.kvp_gather_tables(r.pool, seqs, MB))   # host only, between steps
     torch.cuda.synchronize(dev)
     launches = kvp.kvp_kernel_launches() - launches0
     if world > 1:
@@ -347,9 +348,10 @@ def run_ours(a, rank, world, local):
 
 def run_e2e(kvp, r, w, seqs, ntoks, desc, ws, ws_bytes, flush, stream, dev, host_kv,
             host_q, MB):
-    """Same step through the public API from pinned host buffers: H2D of the
-    step's K, V and Q, append, plan (whose upload carries the block ids),
-    attention, D2H of out and lse, synchronise.  Wall clock per step."""
+    """Same step through the public API from page-locked host buffers: one
+    kvp_decode_step call does the H2D of the step's K, V and Q, the append,
+    the plan (whose upload carries the block ids), attention and the D2H of
+    out and lse; then the stream is synchronised.  Wall clock per step."""
     import torch
     s = w.shapes
     S = len(seqs)
@@ -365,21 +367,15 @@ def run_e2e(kvp, r, w, seqs, ntoks, desc, ws, ws_bytes, flush, stream, dev, host
     lse = torch.empty((s.L, S, s.Hq), dtype=torch.float32, device=dev)
     ho = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
     hl_ = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    ios = [kvp.step_io(qd, out, lse, kd, vd, h_k_new=hk[i], h_v_new=hv[i], h_q=hq[i], h_out=ho, h_lse=hl_)
+           for i in range(n)]
     times = []
     for i in range(n):
         flush.fill_(i & 0xFF)
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        kd.copy_(hk[i], non_blocking=True)
-        vd.copy_(hv[i], non_blocking=True)
-        qd.copy_(hq[i], non_blocking=True)
-        kvp.seq_append_batch(r.pool, seqs, ntoks, kd, vd, stream=stream)
-        ht, hl = kvp.kvp_gather_tables(r.pool, seqs, MB)
-        kvp.paged_decode_attention(qd, r.k_pool, r.v_pool, ht, hl, desc, out, lse, ws, ws_bytes,
-                                   stream=stream)
-        ho.copy_(out, non_blocking=True)
-        hl_.copy_(lse, non_blocking=True)
-        torch.cuda.synchronize(dev)
+        kvp.kvp_decode_step(r.pool, seqs, w.step_tokens, ios[i], desc, ws, ws_bytes, stream=stream)
+        stream.synchronize()
         times.append(time.perf_counter() - t0)
     sec = float(np.sum(times[1:])) if n > 1 else float(times[0])
     cnt = n - 1 if n > 1 else 1
@@ -387,8 +383,9 @@ def run_e2e(kvp, r, w, seqs, ntoks, desc, ws, ws_bytes, flush, stream, dev, host
     d2h = out.numel() * 2 + lse.numel() * 4
     return {"value": S * w.step_tokens * cnt / sec, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": sec / cnt * 1e3,
-            "how": "wall clock per step incl. pinned H2D of k/v/q, append, host plan and its upload, "
-                   "attention, D2H of out+lse and a synchronise; first step dropped"}
+            "how": "wall clock per step: one kvp_decode_step call (H2D of k/v/q from page-locked host "
+                   "memory, append, host plan and its upload, attention, D2H of out+lse) and a stream "
+                   "synchronise; first step dropped"}
 
 
 def run_verify_bench(a, w, rank, world, dev, single_layer=False):
@@ -575,6 +572,57 @@ def sweep_decode(name, dev):
     return entry
 
 
+def sweep_kv4(name, dev):
+    """A decode workload on a pool of 4-bit pages: unique bytes in that format
+    (d/2 code bytes + 1 exponent byte per row, K and V), kernel time, the HBM
+    fraction of those bytes, tokens/s; the bf16 pool's figures are the
+    matching entry without the suffix."""
+    import torch
+    import paged_prefix_shared_decode_gb300 as kvp
+    from paged_prefix_shared_decode_gb300.runner import PoolRunner
+    peak, _ = peaks()
+    base = name[:-len("_kv4")]
+    w = workload(base, 16)
+    s = w.shapes
+    g = torch.Generator(device=dev).manual_seed(1)
+
+    def kv_dev(w_, i):
+        n = w_.ops[i][2]
+        shape = (s.L, n, s.Hkv, s.d)
+        return (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16),
+                torch.randn(shape, generator=g, device=dev).to(torch.bfloat16))
+
+    r = PoolRunner(w, alloc_seed=1, kv4=True)
+    r.run_ops(kv_dev_fn=kv_dev)
+    S = len(w.batch)
+    seqs = np.array([r.ids[n] for n in w.batch], np.int32)
+    kv = torch.randn((s.L, S, s.Hkv, s.d), generator=g, device=dev).to(torch.bfloat16)
+    r.append_step(kv, kv)
+    ht, hl = kvp.kvp_gather_tables(r.pool, seqs, w.max_blocks_per_seq)
+    desc = r.attn_desc(True)
+    st = kvp.kvp_decode_plan_stats(desc, ht, hl)
+    # the planner counts bf16 bytes: rescale to the 4-bit rows
+    ub4 = st["unique_kv_bytes"] * (s.d // 2 + 1) // (2 * s.d)
+    q = torch.randn((s.L, S, s.Hq, s.d), generator=g, device=dev).to(torch.bfloat16)
+    o = torch.empty((s.L, S, s.Hq, s.d), dtype=torch.bfloat16, device=dev)
+    ls = torch.empty((s.L, S, s.Hq), dtype=torch.float32, device=dev)
+    flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    wsb = kvp.kvp_decode_workspace_size(desc, ht, hl)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    ms, kms = _timed_calls(lambda: kvp.paged_decode_attention_kv4(q, r.k_pool, r.k_exp, r.v_pool, r.v_exp, ht, hl,
+                                                                  desc, o, ls, ws, wsb, stream=stream), flush, stream)
+    entry = {"workload": name, "config": describe(w) + "; 4-bit pages (codes + one exponent per row)",
+             "sequences": S, "unique_kv_bytes": ub4, "bits_per_value": 4 + 8 / s.d,
+             "kernel_ms": kms, "ms_per_call": ms, "tokens_per_s": S / (ms / 1e3),
+             "unique_gb_per_s": ub4 / (kms / 1e3) / 1e9, "frac": ub4 / (kms / 1e3) / 1e9 / peak,
+             "kernel": "attn_item_kernel<d, 4-bit>", "traffic": None}
+    r.close()
+    del flush, ws
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_sweep(a, dev):
     """The rest of the metric beside the headline: the phi sweep, MCTS and
     verify on the device, the radix prefix cache on the host."""
@@ -582,12 +630,16 @@ def run_sweep(a, dev):
     import paged_prefix_shared_decode_gb300 as kvp
     out = []
     names = ["trellis0.0", "trellis0.25", "trellis0.5", "trellis0.75", "trellis0.9", "mcts",
-             "verify1", "verify8", "verify32", "radix0.5", "radix0.9"]
+             "verify1", "verify8", "verify32", "dendrite_kv4", "trellis0.0_kv4", "mcts_kv4",
+             "radix0.5", "radix0.9"]
     if a.sweep_set:
         names = [n for n in a.sweep_set.split(",") if n]
     for name in names:
         if name.startswith("radix"):
             out.append(prefix_cache_bench(kvp, float(name[len("radix"):]), with_oracle=not a.no_cpu_baseline))
+            continue
+        if name.endswith("_kv4"):
+            out.append(sweep_kv4(name, dev))
             continue
         if name.startswith("verify"):
             sub = argparse.Namespace(**vars(a))

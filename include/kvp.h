@@ -40,7 +40,8 @@ enum {
     KVP_ERR_OOM = -2,     /* no free block or sequence slot                   */
     KVP_ERR_STATE = -3,   /* operation not possible in the object's state     */
     KVP_ERR_CUDA = -4,    /* a CUDA runtime call failed                        */
-    KVP_ERR_DEVICE = -5   /* a kernel's own bounds check tripped (see below)  */
+    KVP_ERR_DEVICE = -5,  /* a kernel's own bounds check tripped (see below)  */
+    KVP_ERR_WORKSPACE = -6 /* kvp_decode_step: workspace too small (see there) */
 };
 
 /* Device error word bits (kvp_device_error). */
@@ -374,6 +375,62 @@ int paged_decode_attention_noalloc(const void *q, const void *k_pool, const void
                                    const int32_t *block_tables, const int32_t *seq_lens,
                                    int32_t num_seqs, int32_t max_blocks, const kvp_attn_desc *desc,
                                    void *out, float *lse, void *stream);
+
+/*
+ * Decode attention over pool sequences: paged_decode_attention with the block
+ * tables and lengths read from the pool itself, so the caller keeps no host
+ * tables.  Row s of q / out / lse is sequence seq_ids[s] (host array) at its
+ * current length.  desc must describe the pool (layers, kv heads, head dim,
+ * block size, block count and page format); 4-bit pools read their codes and
+ * exponents.  kvp_pool_decode_workspace_size returns the workspace bytes for
+ * the sequences as they are now (0 on invalid input).
+ */
+size_t kvp_pool_decode_workspace_size(const kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs,
+                                      const kvp_attn_desc *desc);
+int paged_decode_attention_pool(const kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs,
+                                const void *q, void *out, float *lse, const kvp_attn_desc *desc,
+                                void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * One decode step, host buffers in and out ("Dendrite", API example: every
+ * branch appends its new token and attends over its own blocks, the shared
+ * prefix included).  In stream order on `stream`:
+ *   1. host-to-device copies h_k_new -> d_k_new, h_v_new -> d_v_new and
+ *      h_q -> d_q (each skipped when its host pointer is NULL: the data is
+ *      already on the device);
+ *   2. seq_append_batch of ntok tokens to every sequence (skipped for ntok 0);
+ *   3. paged_decode_attention_pool over the sequences at their new lengths,
+ *      d_q -> d_out, d_lse;
+ *   4. device-to-host copies d_out -> h_out and d_lse -> h_lse (each skipped
+ *      when its host pointer is NULL).
+ * The call returns once all of it is enqueued; host outputs are valid after
+ * the stream synchronises, and host inputs must stay untouched until then.
+ * Page-locked host buffers make the copies asynchronous; pageable ones work,
+ * but the driver then stages each copy before returning.
+ *
+ * Shapes: k_new, v_new [L][num_seqs * ntok][Hkv][d] bf16, sequence-major;
+ * q, out [L][num_seqs][Hq][d] bf16; lse [L][num_seqs][Hq] fp32 (d_lse may be
+ * NULL, then h_lse must be NULL too).  seq_ids: host, distinct live
+ * sequences.  *ws_needed (may be NULL) receives the workspace bytes the
+ * attention needed.
+ * Errors: KVP_ERR_INVALID (bad arguments, descriptor not matching the pool)
+ * and KVP_ERR_OOM (the appends do not fit) before anything is enqueued;
+ * KVP_ERR_WORKSPACE when ws_bytes < *ws_needed: the copies and the append of
+ * step 1-2 are enqueued and the pool holds the new tokens, nothing else ran;
+ * grow the workspace and finish the step with paged_decode_attention_pool.
+ */
+typedef struct {
+    const void *h_k_new, *h_v_new, *h_q; /* host inputs, or NULL */
+    void *h_out;                         /* host outputs, or NULL */
+    float *h_lse;
+    void *d_k_new, *d_v_new, *d_q;       /* device inputs / staging */
+    void *d_out;                         /* device outputs */
+    float *d_lse;
+} kvp_step_io;
+
+int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, int32_t ntok,
+                    const kvp_step_io *io, const kvp_attn_desc *desc, void *workspace,
+                    size_t ws_bytes, size_t *ws_needed, void *stream);
 
 /* Reads (and clears) the device error word that the last attention call on
  * this workspace left; synchronises `stream`.  *err_out = 0 when clean. */

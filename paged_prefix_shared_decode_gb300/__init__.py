@@ -24,11 +24,14 @@ __all__ = [
     "tree_verify_attention", "kvp_device_error", "kvp_decode_plan_stats", "kvp_strerror",
     "kvp_set_kernel_events", "kvp_kernel_launches", "paged_decode_attention_noalloc",
     "paged_decode_attention_kv4", "KVP_KV_BF16", "KVP_KV_4BIT",
+    "kvp_pool_decode_workspace_size", "paged_decode_attention_pool", "StepIO", "step_io", "kvp_decode_step",
     "KVP_STATIC_WORKSPACE_BYTES",
     "KVP_OK", "KVP_ERR_INVALID", "KVP_ERR_OOM", "KVP_ERR_STATE", "KVP_ERR_CUDA", "KVP_ERR_DEVICE",
+    "KVP_ERR_WORKSPACE",
 ]
 
 KVP_OK, KVP_ERR_INVALID, KVP_ERR_OOM, KVP_ERR_STATE, KVP_ERR_CUDA, KVP_ERR_DEVICE = 0, -1, -2, -3, -4, -5
+KVP_ERR_WORKSPACE = -6
 KVP_KV_BF16, KVP_KV_4BIT = 0, 1   # page formats (kvp_attn_desc.kv_format)
 KVP_STATIC_WORKSPACE_BYTES = 32 << 20   # size of the library's own workspace (include/kvp.h)
 
@@ -51,7 +54,7 @@ def _strerror(code):
     except Exception:  # library missing: still describe the code
         return {0: "ok", -1: "invalid argument", -2: "out of blocks or sequence slots",
                 -3: "operation not possible in this state", -4: "CUDA runtime error",
-                -5: "device-side check failed"}.get(code, "unknown error")
+                -5: "device-side check failed", -6: "workspace too small"}.get(code, "unknown error")
 
 
 class PoolDesc(ctypes.Structure):
@@ -67,6 +70,12 @@ class AttnDesc(ctypes.Structure):
                 ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("use_sharing", ctypes.c_int32),
                 ("kv_format", ctypes.c_int32)]
+
+
+class StepIO(ctypes.Structure):
+    """kvp_step_io: host (h_*) and device (d_*) buffers of one decode step."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("h_k_new", "h_v_new", "h_q", "h_out", "h_lse",
+                                               "d_k_new", "d_v_new", "d_q", "d_out", "d_lse")]
 
 
 _P = ctypes.c_void_p
@@ -105,6 +114,11 @@ _SIGS = {
     "paged_decode_attention_noalloc": ([_P, _P, _P, _P, _P, _I32, _I32, ctypes.POINTER(AttnDesc), _P, _P,
                                         _P], ctypes.c_int),
     "kvp_kernel_launches": ([ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+    "kvp_pool_decode_workspace_size": ([_P, _P, _I32, ctypes.POINTER(AttnDesc)], ctypes.c_size_t),
+    "paged_decode_attention_pool": ([_P, _P, _I32, _P, _P, _P, ctypes.POINTER(AttnDesc), _P, ctypes.c_size_t,
+                                     _P], ctypes.c_int),
+    "kvp_decode_step": ([_P, _P, _I32, _I32, ctypes.POINTER(StepIO), ctypes.POINTER(AttnDesc), _P,
+                         ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t), _P], ctypes.c_int),
     "seq_alloc_prefix": ([_P, _P, _I32, _I32P], ctypes.c_int),
     "seq_accept_draft": ([_P, _I32, _I32, _P, _I32, _I32, _P, _I32P, _P], ctypes.c_int),
     "kvp_radix_create": ([_P, ctypes.POINTER(_P)], ctypes.c_int),
@@ -340,6 +354,64 @@ def paged_decode_attention_noalloc(q, k_pool, v_pool, block_tables, seq_lens, de
     _check(load().paged_decode_attention_noalloc(_dev(q), _dev(k_pool), _dev(v_pool), tp, lp, t.shape[0],
                                                  t.shape[1], ctypes.byref(desc), _dev(out), _dev(lse),
                                                  _stream(stream)), "paged_decode_attention_noalloc")
+
+
+def kvp_pool_decode_workspace_size(pool, seq_ids, desc: AttnDesc) -> int:
+    s, sp = _host_i32(seq_ids)
+    n = load().kvp_pool_decode_workspace_size(pool, sp, len(s), ctypes.byref(desc))
+    if n == 0:
+        raise KvpError(KVP_ERR_INVALID, "kvp_pool_decode_workspace_size")
+    return n
+
+
+def paged_decode_attention_pool(pool, seq_ids, q, out, lse, desc: AttnDesc, workspace, ws_bytes=None,
+                                stream=None):
+    """Decode attention over pool sequences (tables read from the pool)."""
+    s, sp = _host_i32(seq_ids)
+    _check(load().paged_decode_attention_pool(pool, sp, len(s), _dev(q), _dev(out), _dev(lse),
+                                              ctypes.byref(desc), _dev(workspace),
+                                              _ws_bytes(workspace, ws_bytes), _stream(stream)),
+           "paged_decode_attention_pool")
+
+
+def _host(x):
+    """Address of a host buffer: a CPU torch tensor (page-locked for
+    asynchronous copies), a numpy array, an int address or None."""
+    if x is None or isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        if not x.flags["C_CONTIGUOUS"]:
+            raise ValueError("expected a contiguous array")
+        return x.ctypes.data
+    if x.is_cuda:
+        raise ValueError("expected a host tensor")
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return x.data_ptr()
+
+
+def step_io(d_q, d_out, d_lse=None, d_k_new=None, d_v_new=None, h_k_new=None, h_v_new=None, h_q=None,
+            h_out=None, h_lse=None) -> StepIO:
+    """A kvp_step_io.  It holds raw addresses: keep the tensors alive while it
+    is in use."""
+    return StepIO(_host(h_k_new), _host(h_v_new), _host(h_q), _host(h_out), _host(h_lse),
+                  _dev(d_k_new), _dev(d_v_new), _dev(d_q), _dev(d_out), _dev(d_lse))
+
+
+def kvp_decode_step(pool, seq_ids, ntok: int, io: StepIO, desc: AttnDesc, workspace, ws_bytes=None,
+                    stream=None) -> int:
+    """One decode step (copies in, append, attention, copies out) on
+    `stream`; returns the workspace bytes the attention needed.  A
+    KVP_ERR_WORKSPACE error carries them as .ws_needed."""
+    s, sp = _host_i32(seq_ids)
+    need = ctypes.c_size_t(0)
+    rc = load().kvp_decode_step(pool, sp, len(s), ntok, ctypes.byref(io), ctypes.byref(desc), _dev(workspace),
+                                _ws_bytes(workspace, ws_bytes), ctypes.byref(need), _stream(stream))
+    if rc != KVP_OK:
+        e = KvpError(rc, "kvp_decode_step")
+        e.ws_needed = need.value
+        raise e
+    return need.value
 
 
 def kvp_verify_workspace_size(desc: AttnDesc, block_tables, ctx_lens, n_draft: int) -> int:

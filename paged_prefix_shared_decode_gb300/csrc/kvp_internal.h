@@ -117,6 +117,25 @@ bool pool_block_in_use(const kvp_pool *p, int32_t b);
 void pool_hold_block(kvp_pool *p, int32_t b);
 bool pool_drop_block(kvp_pool *p, int32_t b);
 
+// The checks of seq_append_batch with no change to the pool: KVP_OK when
+// every append fits; *total_out (may be null) = the tokens appended.
+int append_batch_check(kvp_pool *p, int32_t nseq, const int32_t *seqs, const int32_t *ntoks,
+                       int64_t *total_out = nullptr);
+
+// A pool's shape and device storage (codes and exponents for 4-bit pages).
+struct PoolView {
+    int32_t L, NB, bs, Hkv, d;
+    const void *k, *v, *k_exp, *v_exp;
+    bool kv4;
+};
+PoolView pool_view(const kvp_pool *p);
+
+// Block tables of seqs[0..n) as rows of `width` (the longest table; padded
+// with -1) and their lengths, into caller vectors.  KVP_ERR_INVALID for a
+// sequence that is not live.
+int pool_tables(const kvp_pool *p, const int32_t *seqs, int32_t n, int32_t *width, int32_t **tables,
+                int32_t **lens);
+
 // Devices the library keeps per-device state for (SM counts, kernel
 // attributes, side streams); ids at or above this fail their launches.
 constexpr int kMaxDevices = 64;

@@ -464,6 +464,8 @@ WsLayout layout(const HostPlan &hp, const kvp_attn_desc &d) {
 }
 
 // Host image of the plan region, reused across calls on the same thread.
+// It is pageable on purpose: a small pageable copy travels with the copy
+// command itself, which measured faster than a copy from page-locked memory.
 thread_local std::vector<unsigned char> t_image;
 thread_local cudaEvent_t t_ev_before = nullptr, t_ev_after = nullptr;
 std::atomic<long long> g_launches{0};
@@ -531,6 +533,27 @@ int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k
     return launch_attention(a, stream, t_ev_before, t_ev_after) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
+bool desc_matches_pool(const kvp_attn_desc &d, const PoolView &pv) {
+    return d.num_layers == pv.L && d.num_kv_heads == pv.Hkv && d.head_dim == pv.d &&
+           d.block_size == pv.bs && d.num_blocks == pv.NB &&
+           d.kv_format == (pv.kv4 ? KVP_KV_4BIT : KVP_KV_BF16);
+}
+
+// The decode plan of pool sequences at their current lengths.
+int plan_pool(const kvp_pool *pool, const int32_t *seqs, int32_t n, const kvp_attn_desc &d,
+              HostPlan &hp) {
+    int32_t width = 0, *tables = nullptr, *lens = nullptr;
+    int rc = pool_tables(pool, seqs, n, &width, &tables, &lens);
+    if (rc) return rc;
+    return build_decode(d, tables, lens, n, width, device_sm_count(), hp);
+}
+
+int run_pool(const HostPlan &hp, const kvp_attn_desc &d, const PoolView &pv, const void *q, int32_t n,
+             void *out, float *lse, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return run(hp, d, q, pv.k, pv.v, n, nullptr, 0, out, lse, ws, ws_bytes, stream,
+               pv.kv4 ? pv.k_exp : nullptr, pv.kv4 ? pv.v_exp : nullptr);
+}
+
 }  // namespace
 
 int current_device() {
@@ -595,6 +618,78 @@ int paged_decode_attention_kv4(const void *q, const void *k_codes, const void *k
     if (rc) return rc;
     return run(hp, *desc, q, k_codes, v_codes, num_seqs, nullptr, 0, out, lse, workspace, ws_bytes,
                (cudaStream_t)stream, k_exps, v_exps);
+}
+
+size_t kvp_pool_decode_workspace_size(const kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs,
+                                      const kvp_attn_desc *desc) {
+    if (!pool || !desc_ok(desc) || !desc_matches_pool(*desc, pool_view(pool))) return 0;
+    HostPlan hp;
+    if (plan_pool(pool, seq_ids, num_seqs, *desc, hp)) return 0;
+    return layout(hp, *desc).total;
+}
+
+int paged_decode_attention_pool(const kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs,
+                                const void *q, void *out, float *lse, const kvp_attn_desc *desc,
+                                void *workspace, size_t ws_bytes, void *stream) {
+    if (!pool || !desc_ok(desc)) return KVP_ERR_INVALID;
+    const PoolView pv = pool_view(pool);
+    if (!desc_matches_pool(*desc, pv)) return KVP_ERR_INVALID;
+    HostPlan hp;
+    int rc = plan_pool(pool, seq_ids, num_seqs, *desc, hp);
+    if (rc) return rc;
+    return run_pool(hp, *desc, pv, q, num_seqs, out, lse, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, int32_t ntok,
+                    const kvp_step_io *io, const kvp_attn_desc *desc, void *workspace,
+                    size_t ws_bytes, size_t *ws_needed, void *stream) {
+    if (!pool || !io || !desc_ok(desc) || num_seqs <= 0 || !seq_ids || ntok < 0 || !workspace)
+        return KVP_ERR_INVALID;
+    const PoolView pv = pool_view(pool);
+    if (!desc_matches_pool(*desc, pv)) return KVP_ERR_INVALID;
+    // everything the attention launch would reject, checked before any work
+    auto a16 = [](const void *p) { return ((uintptr_t)p & 15) == 0; };
+    if (!io->d_q || !io->d_out || !a16(io->d_q) || !a16(io->d_out) || ((uintptr_t)io->d_lse & 3) ||
+        ((uintptr_t)workspace & 255) || (io->h_lse && !io->d_lse))
+        return KVP_ERR_INVALID;
+    if (ntok > 0 && (!io->d_k_new || !io->d_v_new)) return KVP_ERR_INVALID;
+    if ((int64_t)num_seqs * ntok > INT32_MAX / 2) return KVP_ERR_INVALID;
+    const size_t kv_bytes = (size_t)pv.L * num_seqs * ntok * pv.Hkv * pv.d * 2;
+    const size_t rows = (size_t)desc->num_layers * num_seqs * desc->num_q_heads;
+    const size_t q_bytes = rows * desc->head_dim * 2, lse_bytes = rows * sizeof(float);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (ntok > 0) {   // the appends must fit before anything is enqueued
+        if (!a16(io->d_k_new) || !a16(io->d_v_new)) return KVP_ERR_INVALID;
+        thread_local std::vector<int32_t> t_ntoks;
+        t_ntoks.assign(num_seqs, ntok);
+        int rc = append_batch_check(pool, num_seqs, seq_ids, t_ntoks.data());
+        if (rc) return rc;
+    }
+    if (io->h_k_new && ntok > 0 &&
+        (cudaMemcpyAsync(io->d_k_new, io->h_k_new, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+         cudaMemcpyAsync(io->d_v_new, io->h_v_new, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess))
+        return KVP_ERR_CUDA;
+    if (io->h_q && cudaMemcpyAsync(io->d_q, io->h_q, q_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return KVP_ERR_CUDA;
+    if (ntok > 0) {
+        thread_local std::vector<int32_t> t_ntoks;
+        t_ntoks.assign(num_seqs, ntok);
+        int rc = seq_append_batch(pool, num_seqs, seq_ids, t_ntoks.data(), io->d_k_new, io->d_v_new, stream);
+        if (rc) return rc;
+    }
+    HostPlan hp;
+    int rc = plan_pool(pool, seq_ids, num_seqs, *desc, hp);
+    if (rc) return rc;
+    const size_t need = layout(hp, *desc).total;
+    if (ws_needed) *ws_needed = need;
+    if (ws_bytes < need) return KVP_ERR_WORKSPACE;
+    rc = run_pool(hp, *desc, pv, io->d_q, num_seqs, io->d_out, io->d_lse, workspace, ws_bytes, st);
+    if (rc) return rc;
+    if (io->h_out && cudaMemcpyAsync(io->h_out, io->d_out, q_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return KVP_ERR_CUDA;
+    if (io->h_lse && cudaMemcpyAsync(io->h_lse, io->d_lse, lse_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return KVP_ERR_CUDA;
+    return KVP_OK;
 }
 
 size_t kvp_verify_workspace_size(const kvp_attn_desc *desc, const int32_t *block_tables,

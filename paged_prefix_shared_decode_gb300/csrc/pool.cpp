@@ -415,23 +415,11 @@ int seq_append(kvp_pool *p, int32_t seq, const void *k, const void *v, int32_t n
 
 int seq_append_batch(kvp_pool *p, int32_t nseq, const int32_t *seqs, const int32_t *ntoks,
                      const void *k, const void *v, void *stream) {
-    if (!p || nseq < 0 || (nseq > 0 && (!seqs || !ntoks))) return KVP_ERR_INVALID;
-    if (!p->k) return KVP_ERR_STATE;
-    std::unordered_map<int32_t, int32_t> dec;
-    std::set<int32_t> seen;
-    int64_t need = 0, total = 0;
-    for (int32_t i = 0; i < nseq; ++i) {
-        if (!seen.insert(seqs[i]).second) return KVP_ERR_INVALID;
-        Need nd{};
-        int rc = check_append(p, seqs[i], ntoks[i], &dec, &nd);
-        if (rc) return rc;
-        if (nd.cow) dec[p->tables[seqs[i]].back()] += 1;
-        need += nd.cow + nd.fresh;
-        total += ntoks[i];
-    }
-    if (total > INT32_MAX / 2) return KVP_ERR_INVALID;
+    int64_t total = 0;
+    int rc = kvp::append_batch_check(p, nseq, seqs, ntoks, &total);
+    if (rc != KVP_OK && rc != KVP_ERR_OOM) return rc;
     if (total > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return KVP_ERR_INVALID;
-    if (need > (int64_t)p->free_.size()) return KVP_ERR_OOM;
+    if (rc) return rc;
     p->slots.clear();
     p->cow.clear();
     for (int32_t i = 0; i < nseq; ++i) commit_append(p, seqs[i], ntoks[i], p->slots, p->cow);
@@ -518,6 +506,7 @@ const char *kvp_strerror(int code) {
         case KVP_ERR_STATE: return "operation not possible in this state";
         case KVP_ERR_CUDA: return "CUDA runtime error";
         case KVP_ERR_DEVICE: return "device-side check failed";
+        case KVP_ERR_WORKSPACE: return "workspace too small";
         default: return "unknown error";
     }
 }
@@ -537,6 +526,54 @@ bool pool_drop_block(kvp_pool *p, int32_t b) {
     if (--p->ref[b] != 0) return false;
     p->free_.push_back(b);   // the front of the free list
     return true;
+}
+
+int append_batch_check(kvp_pool *p, int32_t nseq, const int32_t *seqs, const int32_t *ntoks,
+                       int64_t *total_out) {
+    if (total_out) *total_out = 0;
+    if (!p || nseq < 0 || (nseq > 0 && (!seqs || !ntoks))) return KVP_ERR_INVALID;
+    if (!p->k) return KVP_ERR_STATE;
+    std::unordered_map<int32_t, int32_t> dec;
+    std::set<int32_t> seen;
+    int64_t need = 0, total = 0;
+    for (int32_t i = 0; i < nseq; ++i) {
+        if (!seen.insert(seqs[i]).second) return KVP_ERR_INVALID;
+        Need nd{};
+        int rc = check_append(p, seqs[i], ntoks[i], &dec, &nd);
+        if (rc) return rc;
+        if (nd.cow) dec[p->tables[seqs[i]].back()] += 1;
+        need += nd.cow + nd.fresh;
+        total += ntoks[i];
+    }
+    if (total > INT32_MAX / 2) return KVP_ERR_INVALID;
+    if (total_out) *total_out = total;
+    if (need > (int64_t)p->free_.size()) return KVP_ERR_OOM;
+    return KVP_OK;
+}
+
+PoolView pool_view(const kvp_pool *p) {
+    const kvp_pool_desc &d = p->desc;
+    return PoolView{d.num_layers, d.num_blocks, d.block_size, d.num_kv_heads, d.head_dim,
+                    p->k, p->v, p->k_exp, p->v_exp, p->kv4};
+}
+
+int pool_tables(const kvp_pool *p, const int32_t *seqs, int32_t n, int32_t *width, int32_t **tables,
+                int32_t **lens) {
+    if (!p || n <= 0 || !seqs) return KVP_ERR_INVALID;
+    int32_t w = 1;
+    for (int32_t i = 0; i < n; ++i) {
+        if (!is_live(p, seqs[i])) return KVP_ERR_INVALID;
+        w = std::max(w, (int32_t)p->tables[seqs[i]].size());
+    }
+    // the pool's scratch: valid until the next call on this pool
+    auto &st = const_cast<kvp_pool *>(p)->stage;
+    st.assign((size_t)n * w + n, -1);
+    int rc = kvp_gather_tables(p, seqs, n, w, st.data(), st.data() + (size_t)n * w);
+    if (rc) return rc;
+    *width = w;
+    *tables = st.data();
+    *lens = st.data() + (size_t)n * w;
+    return KVP_OK;
 }
 
 }  // namespace kvp

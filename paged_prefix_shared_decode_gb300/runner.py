@@ -7,7 +7,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (AttnDesc, PoolDesc, kv_pool_create, kv_pool_destroy, seq_alloc, seq_fork, seq_free,
+from . import (AttnDesc, PoolDesc, KVP_KV_BF16, KVP_KV_4BIT, kv_pool_create, kv_pool_create_kv4, kv_pool_destroy,
+               seq_alloc, seq_fork, seq_free,
                seq_append, seq_append_batch, seq_reserve, kvp_gather_tables, paged_decode_attention,
                kvp_decode_workspace_size, tree_verify_attention, kvp_verify_workspace_size)
 
@@ -25,16 +26,28 @@ def bf16_tensor(bits: np.ndarray, device="cuda"):
 
 
 class PoolRunner:
-    """A pool with device K/V storage and a name -> sequence id map."""
+    """A pool with device K/V storage and a name -> sequence id map.  With
+    kv4 the pool holds 4-bit pages (k_pool / v_pool are the codes, k_exp /
+    v_exp the row exponents); appends still take bf16 K/V."""
 
     def __init__(self, w, alloc_seed: int = 1, device: bool = True, poison: bool = False,
-                 num_blocks: int | None = None):
+                 num_blocks: int | None = None, kv4: bool = False):
         torch = _torch()
         s = w.shapes
         self.w = w
         self.shapes = s
         self.NB = num_blocks or w.num_blocks
-        self.k_pool = self.v_pool = None
+        self.k_pool = self.v_pool = self.k_exp = self.v_exp = None
+        self.kv4 = kv4
+        desc = PoolDesc(s.L, self.NB, s.bs, s.Hkv, s.d, w.max_seqs, w.max_blocks_per_seq, alloc_seed)
+        if kv4:
+            self.k_pool = torch.zeros((s.L, self.NB, s.Hkv, s.bs, s.d // 2), dtype=torch.uint8, device="cuda")
+            self.v_pool = torch.zeros_like(self.k_pool)
+            self.k_exp = torch.zeros((s.L, self.NB, s.Hkv, s.bs), dtype=torch.int8, device="cuda")
+            self.v_exp = torch.zeros_like(self.k_exp)
+            self.pool = kv_pool_create_kv4(desc, self.k_pool, self.k_exp, self.v_pool, self.v_exp)
+            self.ids = {}
+            return
         if device:
             shape = (s.L, self.NB, s.Hkv, s.bs, s.d)
             if poison:   # bf16 NaN in every slot: any read of an unwritten slot shows up
@@ -43,7 +56,6 @@ class PoolRunner:
             else:
                 self.k_pool = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
                 self.v_pool = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
-        desc = PoolDesc(s.L, self.NB, s.bs, s.Hkv, s.d, w.max_seqs, w.max_blocks_per_seq, alloc_seed)
         self.pool = kv_pool_create(desc, self.k_pool, self.v_pool)
         self.ids = {}
 
@@ -96,7 +108,8 @@ class PoolRunner:
 
     def attn_desc(self, use_sharing=True, scale=0.0) -> AttnDesc:
         s = self.shapes
-        return AttnDesc(s.L, s.Hq, s.Hkv, s.d, s.bs, self.NB, scale, 1 if use_sharing else 0)
+        return AttnDesc(s.L, s.Hq, s.Hkv, s.d, s.bs, self.NB, scale, 1 if use_sharing else 0,
+                        KVP_KV_4BIT if self.kv4 else KVP_KV_BF16)
 
 
 class DecodeCall:

@@ -91,3 +91,37 @@ def test_kv4_pool_and_descriptor_checks():
     bad = kvp.AttnDesc(1, 4, 2, 64, 16, 8, 0.0, 1, 7)   # no such page format
     with pytest.raises(kvp.KvpError):
         kvp.kvp_decode_workspace_size(bad, t, ln)
+
+
+def test_pool_decode_entry_points_on_the_host():
+    # tables read from the pool plan exactly like host tables of the same
+    # sequences; argument and state errors come back before any device work
+    p = kvp.kv_pool_create(kvp.PoolDesc(2, 64, 16, 2, 64, 8, 16, 3))
+    root = kvp.seq_alloc(p)
+    kvp.seq_reserve(p, root, 100)
+    kids = [kvp.seq_fork(p, root) for _ in range(3)]
+    for i, k in enumerate(kids):
+        kvp.seq_reserve(p, k, 5 + 17 * i)
+    seqs = [root] + kids
+    desc = kvp.AttnDesc(2, 8, 2, 64, 16, 64, 0.0, 1)
+    t, ln = kvp.kvp_gather_tables(p, seqs, 16)
+    assert kvp.kvp_pool_decode_workspace_size(p, seqs, desc) == kvp.kvp_decode_workspace_size(desc, t, ln)
+    for bad in (kvp.AttnDesc(2, 8, 2, 64, 16, 63, 0.0, 1),            # block count differs
+                kvp.AttnDesc(1, 8, 2, 64, 16, 64, 0.0, 1),            # layers differ
+                kvp.AttnDesc(2, 8, 2, 64, 16, 64, 0.0, 1, kvp.KVP_KV_4BIT)):
+        with pytest.raises(kvp.KvpError):
+            kvp.kvp_pool_decode_workspace_size(p, seqs, bad)
+    with pytest.raises(kvp.KvpError):
+        kvp.kvp_pool_decode_workspace_size(p, seqs + [7], desc)     # not a live sequence
+    a = 1 << 20
+    io = kvp.StepIO(None, None, None, None, None, a, a, a, a, a)
+    with pytest.raises(kvp.KvpError) as e:                           # no device storage
+        kvp.kvp_decode_step(p, seqs, 1, io, desc, a, 1 << 20, stream=0)
+    assert e.value.code == kvp.KVP_ERR_STATE
+    io_bad = kvp.StepIO(None, None, None, None, None, a, a, a + 8, a, a)   # misaligned q
+    with pytest.raises(kvp.KvpError) as e:
+        kvp.kvp_decode_step(p, seqs, 1, io_bad, desc, a, 1 << 20, stream=0)
+    assert e.value.code == kvp.KVP_ERR_INVALID
+    assert [kvp.seq_len(p, s) for s in seqs] == list(ln)              # nothing changed
+    assert kvp.kvp_strerror(kvp.KVP_ERR_WORKSPACE) == "workspace too small"
+    kvp.kv_pool_destroy(p)

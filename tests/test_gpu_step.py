@@ -1,0 +1,224 @@
+"""The pool-table entry points on the GPU:
+
+- kvp_decode_step from host buffers (page-locked torch tensors and pageable
+  numpy arrays): the pool's tables, lengths and copy-on-write count follow the
+  oracle's pool model, and out / lse match the fp64 oracle over the model's
+  host K/V store, step after step, on a forked batch whose first appends copy
+  a shared partial block;
+- paged_decode_attention_pool and kvp_decode_step give the same bits as
+  paged_decode_attention on host tables gathered from the same pool (the same
+  plan and kernels), for bf16 and 4-bit pages;
+- a too-small workspace returns KVP_ERR_WORKSPACE with the size needed after
+  the append, and paged_decode_attention_pool finishes the step; an append
+  that does not fit returns KVP_ERR_OOM with the pool unchanged."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from _util import check_close, check_lse, to_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import paged_prefix_shared_decode_gb300 as kvp  # noqa: E402
+from paged_prefix_shared_decode_gb300.runner import bf16_tensor  # noqa: E402
+
+L, HQ, HKV, D, BS = 2, 32, 4, 64, 16
+
+
+def host_bf16(bits, pinned=True):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.pin_memory() if pinned else t
+
+
+class Pool:
+    """A device pool (bf16 or 4-bit pages) and the oracle's pool model with a
+    host K/V store, driven in lockstep."""
+
+    def __init__(self, nb=96, kv4=False, seqs=16, mb=32, seed=4):
+        self.nb, self.mb, self.kv4 = nb, mb, kv4
+        shape = (L, nb, HKV, BS, D)
+        desc = kvp.PoolDesc(L, nb, BS, HKV, D, seqs, mb, seed)
+        if kv4:
+            self.kp = torch.zeros((L, nb, HKV, BS, D // 2), dtype=torch.uint8, device="cuda")
+            self.vp = torch.zeros_like(self.kp)
+            self.ke = torch.zeros((L, nb, HKV, BS), dtype=torch.int8, device="cuda")
+            self.ve = torch.zeros_like(self.ke)
+            self.pool = kvp.kv_pool_create_kv4(desc, self.kp, self.ke, self.vp, self.ve)
+        else:
+            self.kp = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+            self.vp = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+            self.pool = kvp.kv_pool_create(desc, self.kp, self.vp)
+        self.m = oracle.PoolModel(nb, BS, seqs, mb, alloc_seed=seed,
+                                  store=(np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)))
+        self.desc = kvp.AttnDesc(L, HQ, HKV, D, BS, nb, 0.0, 1, kvp.KVP_KV_4BIT if kv4 else kvp.KVP_KV_BF16)
+        self.draw = 0
+
+    def close(self):
+        kvp.kv_pool_destroy(self.pool)
+
+    def kv(self, total):
+        self.draw += 1
+        return (W.normal_bf16(61, self.draw, (L, total, HKV, D)),
+                W.normal_bf16(62, self.draw, (L, total, HKV, D)))
+
+    def append(self, seqs, ntoks):
+        k, v = self.kv(sum(ntoks))
+        kvp.seq_append_batch(self.pool, seqs, ntoks, bf16_tensor(k), bf16_tensor(v))
+        self.model_append(seqs, ntoks, k, v)
+
+    def model_append(self, seqs, ntoks, k, v):
+        off = 0
+        for s, n in zip(seqs, ntoks):
+            self.m.append(s, n, k[:, off:off + n], v[:, off:off + n])
+            off += n
+
+    def forked_batch(self):
+        root = self.m.alloc()
+        assert kvp.seq_alloc(self.pool) == root
+        self.append([root], [150])                 # ends in a partial block
+        kids = []
+        for _ in range(4):
+            c = self.m.fork(root)
+            assert kvp.seq_fork(self.pool, root) == c
+            kids.append(c)
+        return kids
+
+    def same(self, seqs):
+        assert kvp.kvp_cow_count(self.pool) == self.m.cow_copies
+        assert kvp.kvp_free_block_count(self.pool) == self.m.free_count()
+        for s in seqs:
+            assert list(kvp.seq_block_table(self.pool, s)) == self.m.table(s)
+            assert kvp.seq_len(self.pool, s) == self.m.length(s)
+
+    def oracle(self, q, seqs):
+        t = np.full((len(seqs), self.mb), -1, np.int32)
+        for i, s in enumerate(seqs):
+            tb = self.m.table(s)
+            t[i, :len(tb)] = tb
+        ln = np.array([self.m.length(s) for s in seqs], np.int32)
+        return oracle.decode_attention(q, self.m.store[0], self.m.store[1], t, ln)
+
+    def reference_call(self, q_dev, seqs):
+        """paged_decode_attention on host tables gathered from the pool."""
+        S = len(seqs)
+        t, ln = kvp.kvp_gather_tables(self.pool, seqs, self.mb)
+        ws = torch.empty(kvp.kvp_decode_workspace_size(self.desc, t, ln), dtype=torch.uint8, device="cuda")
+        out = torch.empty((L, S, HQ, D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((L, S, HQ), dtype=torch.float32, device="cuda")
+        if self.kv4:
+            kvp.paged_decode_attention_kv4(q_dev, self.kp, self.ke, self.vp, self.ve, t, ln, self.desc, out, lse, ws)
+        else:
+            kvp.paged_decode_attention(q_dev, self.kp, self.vp, t, ln, self.desc, out, lse, ws)
+        torch.cuda.synchronize()
+        return out, lse
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_decode_step_from_host_buffers(pinned):
+    p = Pool()
+    seqs = p.forked_batch()
+    S = len(seqs)
+    d_k = torch.empty((L, S, HKV, D), dtype=torch.bfloat16, device="cuda")
+    d_v = torch.empty_like(d_k)
+    d_q = torch.empty((L, S, HQ, D), dtype=torch.bfloat16, device="cuda")
+    d_out = torch.empty_like(d_q)
+    d_lse = torch.empty((L, S, HQ), dtype=torch.float32, device="cuda")
+    h_out = torch.empty(d_out.shape, dtype=torch.bfloat16)
+    h_lse = torch.empty(d_lse.shape, dtype=torch.float32)
+    if pinned:
+        h_out, h_lse = h_out.pin_memory(), h_lse.pin_memory()
+    ws = torch.empty(4 << 20, dtype=torch.uint8, device="cuda")
+    for step in range(4):
+        k, v = p.kv(S)
+        q = W.normal_bf16(63, step, (L, S, HQ, D))
+        if pinned:
+            hk, hv, hq = host_bf16(k), host_bf16(v), host_bf16(q)
+        else:   # pageable numpy buffers
+            hk, hv, hq = k, v, q
+        io = kvp.step_io(d_q, d_out, d_lse, d_k, d_v, h_k_new=hk, h_v_new=hv, h_q=hq,
+                         h_out=h_out if pinned else None, h_lse=h_lse if pinned else None)
+        need = kvp.kvp_decode_step(p.pool, seqs, 1, io, p.desc, ws)
+        torch.cuda.synchronize()
+        assert 0 < need <= ws.numel()
+        assert kvp.kvp_device_error(ws) == 0
+        p.model_append(seqs, [1] * S, k, v)
+        p.same(seqs)
+        got = (h_out, h_lse) if pinned else (d_out.cpu(), d_lse.cpu())
+        want, want_lse = p.oracle(q, seqs)
+        check_close(to_f64(got[0]), want)
+        check_lse(to_f64(got[1]), want_lse)
+        # the same bits as the host-table entry point on the same pool state
+        ro, rl = p.reference_call(bf16_tensor(q), seqs)
+        assert torch.equal(ro.cpu(), got[0].cpu()) and torch.equal(rl.cpu(), got[1].cpu())
+    assert p.m.cow_copies >= 4      # every child's first append copied the shared partial block
+    p.close()
+
+
+@pytest.mark.parametrize("kv4", [False, True])
+def test_pool_tables_entry_matches_host_tables(kv4):
+    p = Pool(kv4=kv4)
+    seqs = p.forked_batch()
+    p.append(seqs, [3, 17, 40, 1])
+    S = len(seqs)
+    q = bf16_tensor(W.normal_bf16(64, 0, (L, S, HQ, D)))
+    ws = torch.empty(kvp.kvp_pool_decode_workspace_size(p.pool, seqs, p.desc), dtype=torch.uint8, device="cuda")
+    out = torch.empty((L, S, HQ, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((L, S, HQ), dtype=torch.float32, device="cuda")
+    kvp.paged_decode_attention_pool(p.pool, seqs, q, out, lse, p.desc, ws)
+    torch.cuda.synchronize()
+    ro, rl = p.reference_call(q, seqs)
+    assert torch.equal(out, ro) and torch.equal(lse, rl)
+    # a device-only step (inputs already on the device, outputs left there)
+    k, v = p.kv(S)
+    io = kvp.step_io(q, out, lse, bf16_tensor(k), bf16_tensor(v))
+    kvp.kvp_decode_step(p.pool, seqs, 1, io, p.desc, torch.empty(4 << 20, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    p.model_append(seqs, [1] * S, k, v)
+    p.same(seqs)
+    ro, rl = p.reference_call(q, seqs)
+    assert torch.equal(out, ro) and torch.equal(lse, rl)
+    p.close()
+
+
+def test_small_workspace_and_full_pool():
+    p = Pool(nb=40)     # small enough that one sequence can take every free block
+    seqs = p.forked_batch()
+    S = len(seqs)
+    k, v = p.kv(S)
+    q = bf16_tensor(W.normal_bf16(65, 0, (L, S, HQ, D)))
+    out = torch.empty((L, S, HQ, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((L, S, HQ), dtype=torch.float32, device="cuda")
+    io = kvp.step_io(q, out, lse, bf16_tensor(k), bf16_tensor(v))
+    small = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvp.KvpError) as e:
+        kvp.kvp_decode_step(p.pool, seqs, 1, io, p.desc, small)
+    assert e.value.code == kvp.KVP_ERR_WORKSPACE and e.value.ws_needed > 1024
+    p.model_append(seqs, [1] * S, k, v)     # the append went through
+    p.same(seqs)
+    ws = torch.empty(e.value.ws_needed, dtype=torch.uint8, device="cuda")
+    kvp.paged_decode_attention_pool(p.pool, seqs, q, out, lse, p.desc, ws)
+    torch.cuda.synchronize()
+    want, want_lse = p.oracle(W.normal_bf16(65, 0, (L, S, HQ, D)), seqs)
+    check_close(to_f64(out), want)
+    check_lse(to_f64(lse), want_lse)
+    # fill the pool: a step whose appends need more blocks than are free
+    # changes nothing
+    free = kvp.kvp_free_block_count(p.pool)
+    filler = p.m.alloc()
+    assert kvp.seq_alloc(p.pool) == filler
+    p.append([filler], [free * BS])
+    assert kvp.kvp_free_block_count(p.pool) == 0
+    lens = [kvp.seq_len(p.pool, s) for s in seqs]
+    k, v = p.kv(S * BS)
+    io = kvp.step_io(q, out, lse, bf16_tensor(k), bf16_tensor(v))
+    with pytest.raises(kvp.KvpError) as e:
+        kvp.kvp_decode_step(p.pool, seqs, BS, io, p.desc, ws)
+    assert e.value.code == kvp.KVP_ERR_OOM
+    assert [kvp.seq_len(p.pool, s) for s in seqs] == lens
+    p.same(seqs + [filler])
+    p.close()
