@@ -17,6 +17,14 @@
 // four ways (with at most 32 rows at head dim 128, two ways) and combine
 // their (m, l, o) through shared memory.
 //
+// 4-bit pages (codes in [-7, 7] and one power-of-two exponent per token row,
+// value = code * 2^e) are staged as codes and exponents -- 4.125 bits per
+// value at head dim 64 instead of 16.  Units whose warps split the tiles'
+// tokens take the codes from shared memory straight into the mma operands
+// (exact bf16 code * 2^e, formed in registers); units of more than 16 rows,
+// whose warps all read every token, first expand each tile once into a bf16
+// tile in shared memory and then run the bf16 path.
+//
 // A unit writes out (bf16) and lse (fp32, natural log) directly, or -- when
 // its rows' keys are split over several units -- normalised partial o and a
 // base-2 lse per row, which the merge kernels combine (one warp per query
@@ -114,6 +122,53 @@ __global__ void tree_mask_kernel(const int32_t *parent, int32_t nq, int32_t n, u
     if (q < nq) mask[q] = ancestor_mask(parent, q / n, q % n, n, err);
 }
 
+// 4-bit codes to bf16 mma operands.  A code c in [-7, 7] stored as a
+// two's-complement nibble u becomes bf16(136 + c) by placing u ^ 8 in the
+// low mantissa bits of 128 (bits 0x4300); then fma(x, 2^e, -136 * 2^e) =
+// c * 2^e exactly (one rounding of an exact, representable result) when
+// 2^e and 136 * 2^e are normal bf16 numbers (-126 <= e <= 120); otherwise
+// x - 136 = c (exact) and a multiply by 2^e.
+__device__ __forceinline__ uint32_t bf16_exp2_bits(int e) {   // 2^e, e in [-127, 127]
+    return e >= -126 ? (uint32_t)(e + 127) << 7 : 0x40u;
+}
+__device__ __forceinline__ uint32_t bf16_neg136_bits(int e) {   // -136 * 2^e, e in [-126, 120]
+    return 0x8000u | ((uint32_t)(134 + e) << 7) | 0x08u;
+}
+// scale pair (2^ea, 2^eb) as bf16x2 with the -136 * 2^e pair packed above
+// it: .x = scales, .y = constants (callers check the fused range)
+__device__ __forceinline__ uint2 exp_pair2(int ea, int eb) {
+    const int ca = min(max(ea, -126), 120), cb = min(max(eb, -126), 120);
+    return make_uint2(bf16_exp2_bits(ea) | (bf16_exp2_bits(eb) << 16),
+                      bf16_neg136_bits(ca) | (bf16_neg136_bits(cb) << 16));
+}
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w, int i) {   // nibbles i and i + 4 as bf16(136 + c)
+    return ((w >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
+}
+__device__ __forceinline__ uint32_t conv_pair(uint32_t x, uint2 sc, bool fused) {
+    __nv_bfloat162 xv = *reinterpret_cast<__nv_bfloat162 *>(&x);
+    const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&sc.x);
+    __nv_bfloat162 r;
+    if (fused) {
+        const __nv_bfloat162 c2 = *reinterpret_cast<const __nv_bfloat162 *>(&sc.y);
+        r = __hfma2(xv, s2, c2);
+    } else {
+        const uint32_t k136 = 0x43084308u;
+        r = __hmul2(__hsub2(xv, *reinterpret_cast<const __nv_bfloat162 *>(&k136)), s2);
+    }
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+// K word (8 dims of one token with exponent e) -> b[0..3] = pairs 0..3
+__device__ __forceinline__ void code_pairs_k(uint32_t w, int e, bool fused, uint32_t (&b)[4]) {
+    const uint2 sc = exp_pair2(e, e);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b[i] = conv_pair(nib_pair(w, i), sc, fused);
+}
+// V word (4 dims of two tokens) with its exponent pair -> b[0..3]
+__device__ __forceinline__ void code_pairs_v(uint32_t w, uint2 sc, bool fused, uint32_t (&b)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b[i] = conv_pair(nib_pair(w, i), sc, fused);
+}
+
 template <int D>
 struct KCfg {
     static constexpr int CH = D / 8;                        // 16-byte chunks per token row
@@ -134,6 +189,10 @@ struct KCfg {
 template <int D>
 struct KCfg4 {
     static constexpr int CH4 = D / 32;                     // 16-byte code chunks per row
+    // code rows are 32 (d 64) or 64 (d 128) bytes: chunk c of row tok is
+    // stored at chunk c ^ ((tok >> SWS) & (CH4 - 1)), so that the 8 rows an
+    // ldmatrix reads fall in different banks
+    static constexpr int SWS = CH4 == 2 ? 2 : 1;
     static constexpr int CODE_BYTES = kTileTokens * D / 2; // one K (or V) tile of codes
     static constexpr int NSTAGE = 3;
     static constexpr int STAGE_BYTES = 2 * CODE_BYTES + 2 * kTileTokens;   // codes K, V; exponents K, V
@@ -147,7 +206,7 @@ struct KCfg4 {
 
 // One work unit with TS warps splitting each tile's tokens.  KV4: the pool
 // holds 4-bit codes and row exponents (a.k_pool / a.v_pool are the codes).
-template <int D, int TS, bool KV4>
+template <int D, int TS, bool KV4, bool TREE>
 __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it, int l, int kvh,
                                          int ntile, unsigned char *smem, const KvTile *s_tiles) {
     using C = KCfg<D>;
@@ -211,8 +270,9 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
                     atomicOr(a.err, 1);
                 }
             }
-            cp_async16(st + tok * (D / 2) + c * 16, sk, bytes);
-            cp_async16(st + C4::CODE_BYTES + tok * (D / 2) + c * 16, sv, bytes);
+            const int cs = (c ^ ((tok >> C4::SWS) & (C4::CH4 - 1))) * 16;
+            cp_async16(st + tok * (D / 2) + cs, sk, bytes);
+            cp_async16(st + C4::CODE_BYTES + tok * (D / 2) + cs, sv, bytes);
         }
         // exponents: four groups of 16 tokens, each inside one block (tiles
         // start on a block boundary and blocks are a multiple of 16 tokens)
@@ -243,7 +303,8 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
             const int kv = x / (kTileTokens * C::CH);
             const int y = x % (kTileTokens * C::CH);
             const int tok = y / C::CH, ch = y % C::CH;     // 8 values: codes bytes 4 ch .. 4 ch + 3
-            const uint32_t cw = *reinterpret_cast<const uint32_t *>(stg + kv * C4::CODE_BYTES + tok * (D / 2) + ch * 4);
+            const int cs = ((ch >> 2) ^ ((tok >> C4::SWS) & (C4::CH4 - 1))) * 16 + (ch & 3) * 4;
+            const uint32_t cw = *reinterpret_cast<const uint32_t *>(stg + kv * C4::CODE_BYTES + tok * (D / 2) + cs);
             const int e = (int)reinterpret_cast<const int8_t *>(stg + 2 * C4::CODE_BYTES + kv * kTileTokens)[tok];
             // 2^e as bf16 (e >= -126: a normal number; -127: the subnormal 2^-127)
             const uint32_t sb = e >= -126 ? (uint32_t)(e + 127) << 7 : 0x40u;
@@ -266,15 +327,19 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
             issue4(t);
             return;
         }
+        // a tile may start anywhere in a block (a verify tile's draft tokens
+        // start right after the context), so block and slot come from the
+        // absolute position
         const KvTile &kt = s_tiles[t];
         const int ntok = kt.ntok_flags & 0xFFFF;
         const int jb = kt.tok0 >> bs_log2;
         const uint32_t dK = smem_addr(smem + (t % C::NSTAGE) * C::STAGE_BYTES);
         const uint32_t dV = dK + C::TILE_BYTES;
+        const __nv_bfloat16 *kb = kpool + layer_base, *vb = vpool + layer_base;
+        const int tok_t = threadIdx.x / C::CH, c = threadIdx.x % C::CH;
 #pragma unroll
         for (int i = 0; i < kTileTokens * C::CH / kThreads; ++i) {
-            const int x = threadIdx.x + i * kThreads;
-            const int tok = x / C::CH, c = x % C::CH;
+            const int tok = tok_t + i * (kThreads / C::CH);
             const uint32_t off = tok * D * 2 + ((c ^ (tok & 7)) << 4);
             const __nv_bfloat16 *sk = kpool, *sv = vpool;
             int bytes = 0;
@@ -282,10 +347,9 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
                 const int pos = kt.tok0 + tok;
                 const int blk = kt.blk[(pos >> bs_log2) - jb];
                 if ((unsigned)blk < (unsigned)a.NB) {
-                    const size_t e = layer_base + (size_t)blk * block_stride +
-                                     (size_t)(pos & bs_mask) * D + c * 8;
-                    sk = kpool + e;
-                    sv = vpool + e;
+                    const size_t e = (size_t)blk * block_stride + (size_t)((pos & bs_mask) * D + c * 8);
+                    sk = kb + e;
+                    sv = vb + e;
                     bytes = 16;
                 } else if (c == 0) {
                     atomicOr(a.err, 1);
@@ -302,17 +366,42 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
         cp_async_commit();
     }
 
+    // REG4: 4-bit codes go from shared memory straight into mma operands.
+    // A thread's ldmatrix word of K codes holds 8 dims of one token, 32 c +
+    // 8 tq + k for nibble k; nibble pairs (i, i + 4) form its bf16 pairs, so
+    // the Q K^T contraction runs over dims in that order and Q's fragments
+    // are gathered to match (k-step 2c + h pairs dims 8 tq + 2h + {0, 4} and
+    // 8 tq + 2h + {1, 5} of chunk c).
+    constexpr bool REG4 = KV4 && TS > 1;
     uint32_t qf[C::KS][4];
+    if constexpr (REG4) {
 #pragma unroll
-    for (int kk = 0; kk < C::KS; ++kk) {
-        const int c = kk * 16 + 2 * tq;
-        qf[kk][0] = has0 ? ld_u32(q0 + c) : 0u;
-        qf[kk][1] = has1 ? ld_u32(q1 + c) : 0u;
-        qf[kk][2] = has0 ? ld_u32(q0 + c + 8) : 0u;
-        qf[kk][3] = has1 ? ld_u32(q1 + c + 8) : 0u;
+        for (int c = 0; c < C4::CH4; ++c) {
+            uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
+            if (has0) x0 = __ldg(reinterpret_cast<const uint4 *>(q0 + 32 * c + 8 * tq));
+            if (has1) x1 = __ldg(reinterpret_cast<const uint4 *>(q1 + 32 * c + 8 * tq));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t lo0 = h ? x0.y : x0.x, hi0 = h ? x0.w : x0.z;
+                const uint32_t lo1 = h ? x1.y : x1.x, hi1 = h ? x1.w : x1.z;
+                qf[2 * c + h][0] = __byte_perm(lo0, hi0, 0x5410);
+                qf[2 * c + h][1] = __byte_perm(lo1, hi1, 0x5410);
+                qf[2 * c + h][2] = __byte_perm(lo0, hi0, 0x7632);
+                qf[2 * c + h][3] = __byte_perm(lo1, hi1, 0x7632);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int kk = 0; kk < C::KS; ++kk) {
+            const int c = kk * 16 + 2 * tq;
+            qf[kk][0] = has0 ? ld_u32(q0 + c) : 0u;
+            qf[kk][1] = has1 ? ld_u32(q1 + c) : 0u;
+            qf[kk][2] = has0 ? ld_u32(q0 + c + 8) : 0u;
+            qf[kk][3] = has1 ? ld_u32(q1 + c + 8) : 0u;
+        }
     }
     uint64_t tm0 = ~0ull, tm1 = ~0ull;
-    if (a.tree_mask) {
+    if (TREE) {
         if (has0) tm0 = a.tree_mask[qt0];
         if (has1) tm1 = a.tree_mask[qt1];
     }
@@ -327,14 +416,14 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
         __syncthreads();
         if (t + NSTAGE - 1 < ntile) issue(t + NSTAGE - 1);
         cp_async_commit();
-        if constexpr (KV4) {
+        if constexpr (KV4 && !REG4) {
             expand4(t);
             __syncthreads();
         }
 
         const KvTile &kt = s_tiles[t];
         const int ntok = kt.ntok_flags & 0xFFFF;
-        const bool tree = (kt.ntok_flags >> 16) & kTileTree;
+        const bool tree = TREE && ((kt.ntok_flags >> 16) & kTileTree);
         const int mlo = kt.members & 0xFFFF, mhi = kt.members >> 16;
         const bool in0 = has0 && mem0 >= mlo && mem0 < mhi;
         const bool in1 = has1 && mem1 >= mlo && mem1 < mhi;
@@ -347,6 +436,51 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
         float s[NT][4];
 #pragma unroll
         for (int j = 0; j < NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+        // REG4: codes and exponents of this tile's stage
+        const unsigned char *stg4 = REG4 ? smem + (t % NSTAGE) * C4::STAGE_BYTES : smem;
+        const uint32_t aK4 = smem_addr(stg4), aV4 = aK4 + C4::CODE_BYTES;
+        const int8_t *ek4 = reinterpret_cast<const int8_t *>(stg4 + 2 * C4::CODE_BYTES);
+        const int8_t *ev4 = ek4 + kTileTokens;
+        // fused conversion code * 2^e = fma(bf16(136 + code), 2^e, -136 * 2^e)
+        // needs both factors normal: -126 <= e <= 120 for every token of the
+        // warp's share of the tile (else: subtract, then multiply)
+        bool fused4 = true;
+        if constexpr (REG4) {
+#pragma unroll
+            for (int j2 = 0; j2 < NT / 2; ++j2) {
+                const int t0k = tb + 16 * j2;
+                const int e0 = ek4[t0k + gq], e1 = ek4[t0k + 8 + gq];
+                const int e2 = ev4[t0k + 2 * tq], e3 = ev4[t0k + 2 * tq + 1];
+                const int e4 = ev4[t0k + 8 + 2 * tq], e5 = ev4[t0k + 9 + 2 * tq];
+                const int lo = min(min(min(e0, e1), min(e2, e3)), min(e4, e5));
+                const int hi = max(max(max(e0, e1), max(e2, e3)), max(e4, e5));
+                fused4 = fused4 && lo >= -126 && hi <= 120;
+            }
+            fused4 = __all_sync(0xffffffffu, fused4);
+        }
+        if constexpr (REG4) {
+#pragma unroll
+            for (int j2 = 0; j2 < NT / 2; ++j2) {
+                const int t0k = tb + 16 * j2;
+#pragma unroll
+                for (int cp = 0; cp < C4::CH4 / 2; ++cp) {
+                    const int tok = t0k + ((lane >> 4) << 3) + (lane & 7);
+                    const int ch = 2 * cp + ((lane >> 3) & 1);
+                    uint32_t w[4];
+                    ldsm_x4(aK4 + tok * (D / 2) + ((ch ^ ((tok >> C4::SWS) & (C4::CH4 - 1))) << 4), w[0], w[1], w[2],
+                            w[3]);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const int e = ek4[t0k + ((m >> 1) << 3) + gq];
+                        const int c = 2 * cp + (m & 1);
+                        uint32_t b[4];
+                        code_pairs_k(w[m], e, fused4, b);
+                        mma16816(s[2 * j2 + (m >> 1)], qf[2 * c], b[0], b[1]);
+                        mma16816(s[2 * j2 + (m >> 1)], qf[2 * c + 1], b[2], b[3]);
+                    }
+                }
+            }
+        } else
 #pragma unroll
         for (int kk = 0; kk < C::KS; ++kk) {
 #pragma unroll
@@ -426,6 +560,31 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
                                     pack_bf16x2(s[2 * k2][2], s[2 * k2][3]),
                                     pack_bf16x2(s[2 * k2 + 1][0], s[2 * k2 + 1][1]),
                                     pack_bf16x2(s[2 * k2 + 1][2], s[2 * k2 + 1][3])};
+            if constexpr (REG4) {
+                // V: .trans ldmatrix words hold 4 dims (32 c + 4 gq + i) of
+                // two tokens; n-tile 4 c + i takes nibble i of each
+                const int t0k = tb + k2 * 16;
+                const uint2 sv0 = exp_pair2(ev4[t0k + 2 * tq], ev4[t0k + 2 * tq + 1]);
+                const uint2 sv1 = exp_pair2(ev4[t0k + 8 + 2 * tq], ev4[t0k + 9 + 2 * tq]);
+#pragma unroll
+                for (int cp = 0; cp < C4::CH4 / 2; ++cp) {
+                    const int m = lane >> 3;
+                    const int tok = t0k + ((m & 1) << 3) + (lane & 7);
+                    const int ch = 2 * cp + (m >> 1);
+                    uint32_t w[4];
+                    ldsm_x4_t(aV4 + tok * (D / 2) + ((ch ^ ((tok >> C4::SWS) & (C4::CH4 - 1))) << 4), w[0], w[1],
+                              w[2], w[3]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t b0[4], b1[4];
+                        code_pairs_v(w[2 * h], sv0, fused4, b0);
+                        code_pairs_v(w[2 * h + 1], sv1, fused4, b1);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) mma16816(o[4 * (2 * cp + h) + i], pa, b0[i], b1[i]);
+                    }
+                }
+                continue;
+            }
             const int tok = tb + k2 * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
             for (int n2 = 0; n2 < C::NO / 2; ++n2) {
@@ -491,6 +650,54 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
     const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
     const float lse2_0 = l0 > 0.f ? m0 + __log2f(l0) : -INFINITY;
     const float lse2_1 = l1 > 0.f ? m1 + __log2f(l1) : -INFINITY;
+    if constexpr (REG4) {
+        // o[4 c + i][0 / 1] is dim 32 c + 8 tq + i / + 4 + i (rows 0; 2 / 3 for row 1)
+        float v0[C::NO * 2], v1[C::NO * 2];
+#pragma unroll
+        for (int c = 0; c < C4::CH4; ++c)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v0[8 * c + i] = o[4 * c + i][0] * inv0;
+                v0[8 * c + 4 + i] = o[4 * c + i][1] * inv0;
+                v1[8 * c + i] = o[4 * c + i][2] * inv1;
+                v1[8 * c + 4 + i] = o[4 * c + i][3] * inv1;
+            }
+        if (it.out_base < 0) {
+            __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(a.out);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                if (!(r ? has1 : has0)) continue;
+                const int qt = r ? qt1 : qt0, row = r ? row1 : row0;
+                const float *v = r ? v1 : v0;
+                __nv_bfloat16 *dst = ob + (((size_t)l * a.nq + qt) * a.Hq + kvh * G + row % G) * D;
+#pragma unroll
+                for (int c = 0; c < C4::CH4; ++c)
+                    *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * tq) =
+                        make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                   pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+                if (a.lse && tq == 0)
+                    a.lse[((size_t)l * a.nq + qt) * a.Hq + kvh * G + row % G] =
+                        (r ? lse2_1 : lse2_0) * 0.6931471805599453f;
+            }
+        } else {
+            const size_t rb = ((size_t)l * a.Hkv + kvh) * a.P + it.out_base;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                if (!(r ? has1 : has0)) continue;
+                const int row = r ? row1 : row0;
+                const float *v = r ? v1 : v0;
+                float *dst = a.part_o + (rb + row) * D;
+#pragma unroll
+                for (int c = 0; c < C4::CH4; ++c) {
+                    *reinterpret_cast<float4 *>(dst + 32 * c + 8 * tq) = make_float4(v[8 * c], v[8 * c + 1], v[8 * c + 2], v[8 * c + 3]);
+                    *reinterpret_cast<float4 *>(dst + 32 * c + 8 * tq + 4) =
+                        make_float4(v[8 * c + 4], v[8 * c + 5], v[8 * c + 6], v[8 * c + 7]);
+                }
+                if (tq == 0) a.part_lse[rb + row] = r ? lse2_1 : lse2_0;
+            }
+        }
+        return;
+    }
     if (it.out_base < 0) {
         __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(a.out);
         if (has0) {
@@ -530,7 +737,7 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
     }
 }
 
-template <int D, bool KV4>
+template <int D, bool KV4, bool TREE>
 __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kernel(const AttnLaunch a) {
     using C = KCfg<D>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -567,9 +774,9 @@ __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kerne
         // The two-way split pays at head dim 128 (two CTAs per SM leave few
         // warps to hide latency); at head dim 64 the extra copy of the tile
         // loop costs more in instruction fetch than the split gains.
-        if (rows <= 16) run_unit<D, 4, KV4>(a, it, l, kvh, ntile, smem, s_tiles);
-        else if (D == 128 && rows <= 32) run_unit<D, 2, KV4>(a, it, l, kvh, ntile, smem, s_tiles);
-        else run_unit<D, 1, KV4>(a, it, l, kvh, ntile, smem, s_tiles);
+        if (rows <= 16) run_unit<D, 4, KV4, TREE>(a, it, l, kvh, ntile, smem, s_tiles);
+        else if (D == 128 && rows <= 32) run_unit<D, 2, KV4, TREE>(a, it, l, kvh, ntile, smem, s_tiles);
+        else run_unit<D, 1, KV4, TREE>(a, it, l, kvh, ntile, smem, s_tiles);
         __syncthreads();
     }
 }
@@ -766,7 +973,7 @@ struct Occupancy {
 
 // Per device: the kernel's shared-memory attribute is set and its
 // occupancy queried once for each device that runs it.
-template <int D, bool KV4 = false>
+template <int D, bool KV4 = false, bool TREE = false>
 Occupancy &occupancy() {
     static Occupancy occ[kMaxDevices];
     static std::once_flag once[kMaxDevices];
@@ -780,11 +987,11 @@ Occupancy &occupancy() {
         o.per_sm = C::MIN_BLOCKS;
         o.sms = device_sm_count();
         const int smem_bytes = KV4 ? KCfg4<D>::SMEM : C::SMEM;
-        if (cudaFuncSetAttribute(attn_item_kernel<D, KV4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(attn_item_kernel<D, KV4, TREE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem_bytes) != cudaSuccess)
             return;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_item_kernel<D, KV4>, kThreads, smem_bytes) ==
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_item_kernel<D, KV4, TREE>, kThreads, smem_bytes) ==
                 cudaSuccess && n > 0)
             o.per_sm = n;
         o.ok = true;
@@ -842,13 +1049,21 @@ cudaError_t launch_d(const AttnLaunch &a, cudaStream_t stream, cudaEvent_t befor
         Occupancy &o4 = occupancy<D, true>();
         if (!o4.ok) return cudaErrorInvalidDevice;
         const int grid = a.n_units < o4.sms * o4.per_sm ? a.n_units : o4.sms * o4.per_sm;
-        attn_item_kernel<D, true><<<grid, kThreads, KCfg4<D>::SMEM, mma_stream>>>(a);
+        attn_item_kernel<D, true, false><<<grid, kThreads, KCfg4<D>::SMEM, mma_stream>>>(a);
+        count_launch();
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    } else if (a.n_units > 0 && a.tree_mask) {
+        Occupancy &ot = occupancy<D, false, true>();
+        if (!ot.ok) return cudaErrorInvalidDevice;
+        const int grid = a.n_units < ot.sms * ot.per_sm ? a.n_units : ot.sms * ot.per_sm;
+        attn_item_kernel<D, false, true><<<grid, kThreads, C::SMEM, mma_stream>>>(a);
         count_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     } else if (a.n_units > 0) {
         const int grid = a.n_units < occ.sms * occ.per_sm ? a.n_units : occ.sms * occ.per_sm;
-        attn_item_kernel<D, false><<<grid, kThreads, C::SMEM, mma_stream>>>(a);
+        attn_item_kernel<D, false, false><<<grid, kThreads, C::SMEM, mma_stream>>>(a);
         count_launch();
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
