@@ -29,7 +29,10 @@
 // through shared memory.  The running max is raised only when a step's max
 // exceeds it by more than 32, so p < 2^32; O_g is then rescaled in TMEM.
 // Every wait is bounded; on a timeout the CTA sets bit 4 of the workspace
-// error word, all roles leave their loops and TMEM is freed.
+// error word and all roles leave their loops; before the CTA frees its TMEM
+// and ends, the producers let the copies they issued land and the MMA thread
+// lets its MMAs complete (bounded waits too).  Softmax warps none of whose
+// rows is in the unit (a half-filled tile) keep only the barriers.
 //
 // TMEM columns: S_0 [0, 128), S_1 [128, 256), O_0 [256, 256 + d),
 // O_1 [256 + d, 256 + 2d).
@@ -212,7 +215,8 @@ struct TcCfg {
     static constexpr int B_UNIT_FULL = 0, B_UNIT_EMPTY = 2, B_K_FULL = 4, B_K_EMPTY = B_K_FULL + NK,
                          B_V_FULL = B_K_EMPTY + NK, B_V_EMPTY = B_V_FULL + NV, B_S_FULL = B_V_EMPTY + NV,
                          B_P_FULL = B_S_FULL + 2, B_Q_FULL = B_P_FULL + 2, B_Q_EMPTY = B_Q_FULL + 1,
-                         B_O_FULL = B_Q_EMPTY + 1, B_O_EMPTY = B_O_FULL + 1, N_BARS = B_O_EMPTY + 1;
+                         B_O_FULL = B_Q_EMPTY + 1, B_O_EMPTY = B_O_FULL + 1, B_DRAIN = B_O_EMPTY + 1,
+                         N_BARS = B_DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;   // tmem address, abort flag
     static constexpr int SMEM = MISC_OFF + 16 + 1024;       // + slack to align the base to 1024
     static constexpr int S_COL = 0, O_COL = 2 * kStepTokens;
@@ -384,6 +388,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(bar(C::B_Q_EMPTY), 1);
         mbar_init(bar(C::B_O_FULL), 1);
         mbar_init(bar(C::B_O_EMPTY), kSoftThreads);
+        mbar_init(bar(C::B_DRAIN), 1);
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -408,6 +413,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         *s_abort = 1;
         atomicOr(a.err, KVP_DEVERR_WAIT_TIMEOUT);
         return false;
+    };
+    // bounded wait that records nothing: lets copies and MMAs already in
+    // flight land before the CTA frees its shared memory and TMEM (after a
+    // normal run they have all landed and it returns at once)
+    auto settle = [&](uint32_t b, uint32_t parity) {
+        for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(b, parity); ++i) {
+        }
     };
 
     const int n_items = a.n_tc_units / (a.L * a.Hkv);
@@ -510,6 +522,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) mbar_arrive(bar(C::B_UNIT_EMPTY + slot));
             if (!alive || __shfl_sync(0xffffffffu, *s_abort, 0)) break;
         }
+        // this warp's copies land before the CTA ends: its own cp.async, and
+        // the transaction bytes of the last stages it armed
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+        if (lane == 0)
+            for (uint32_t k = g > (uint32_t)nring ? g - (uint32_t)nring : 0u; k < g; ++k)
+                settle(bar(b_full + k % nring), (k / nring) & 1);
+        __syncwarp();
     } else if (warp == kUnitWarp) {
         // ------------------------------------------------------------ units and Q
         auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
@@ -690,6 +709,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 umma_commit(bar(C::B_O_FULL));
                 mbar_arrive(bar(C::B_UNIT_EMPTY + slot));
             }
+            // every MMA this thread issued completes before TMEM is freed
+            umma_commit(bar(C::B_DRAIN));
+            settle(bar(C::B_DRAIN), 0);
         }
         __syncwarp();
     } else {
@@ -724,12 +746,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int qt = 0;
             if (has) qt = __ldg(a.members + it.member_off + mem);
             const uint64_t tmask = has && a.tree_mask ? a.tree_mask[qt] : ~0ull;
+            // a warp none of whose 32 rows is in the unit (a half-filled
+            // 128-row tile) only keeps the group's barriers: the rows of P it
+            // would write are never read back into an output row, since every
+            // row of O depends on its own row of P alone
+            const bool idle = !__any_sync(0xffffffffu, has);
 
             float m = -INFINITY, lsum = 0.f;
             for (int t = pair ? 0 : grp; t < nsteps; t += pair ? 1 : 2) {
                 ok = wait(bar(C::B_S_FULL + grp), ns & 1) && ok;
                 ns += 1;
                 tc_after();
+                if (idle) {
+                    tc_before();
+                    mbar_arrive(bar(C::B_P_FULL + grp));
+                    continue;
+                }
                 int nv0 = 0, nv1 = 0;
                 bool tr0 = false, tr1 = false;
                 {
@@ -817,7 +849,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 cb = D;
             }
             const bool write = has && nsteps > 0;
-            for (int c0 = ca; c0 < cb; c0 += 32) {
+            for (int c0 = ca; !idle && c0 < cb; c0 += 32) {
                 uint32_t x[32], y[32];
                 tmem_ld32(o_tm + c0, x);
                 tmem_ld32(o_tm + D + c0, y);
