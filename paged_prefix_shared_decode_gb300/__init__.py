@@ -25,6 +25,7 @@ __all__ = [
     "kvp_set_kernel_events", "kvp_kernel_launches", "paged_decode_attention_noalloc",
     "paged_decode_attention_kv4", "KVP_KV_BF16", "KVP_KV_4BIT",
     "kvp_pool_decode_workspace_size", "paged_decode_attention_pool", "StepIO", "step_io", "kvp_decode_step",
+    "DecodeStep",
     "KVP_STATIC_WORKSPACE_BYTES",
     "KVP_OK", "KVP_ERR_INVALID", "KVP_ERR_OOM", "KVP_ERR_STATE", "KVP_ERR_CUDA", "KVP_ERR_DEVICE",
     "KVP_ERR_WORKSPACE",
@@ -412,6 +413,31 @@ def kvp_decode_step(pool, seq_ids, ntok: int, io: StepIO, desc: AttnDesc, worksp
         e.ws_needed = need.value
         raise e
     return need.value
+
+
+class DecodeStep:
+    """kvp_decode_step with its arguments marshalled once, for a loop that
+    repeats the step on the same sequences and buffers: each call is then a
+    single foreign call.  Keep `io`'s tensors alive while it is in use."""
+
+    def __init__(self, pool, seq_ids, ntok: int, io: StepIO, desc: AttnDesc, workspace, ws_bytes=None,
+                 stream=None):
+        self._seqs = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        self._io, self._desc = io, desc
+        self.ws_needed = ctypes.c_size_t(0)
+        self._fn = load().kvp_decode_step
+        self._args = (ctypes.c_void_p(pool), ctypes.c_void_p(self._seqs.ctypes.data), _I32(len(self._seqs)),
+                      _I32(ntok), ctypes.byref(io), ctypes.byref(desc), ctypes.c_void_p(_dev(workspace)),
+                      ctypes.c_size_t(_ws_bytes(workspace, ws_bytes)), ctypes.byref(self.ws_needed),
+                      ctypes.c_void_p(_stream(stream)))
+
+    def __call__(self) -> int:
+        rc = self._fn(*self._args)
+        if rc != KVP_OK:
+            e = KvpError(rc, "kvp_decode_step")
+            e.ws_needed = self.ws_needed.value
+            raise e
+        return self.ws_needed.value
 
 
 def kvp_verify_workspace_size(desc: AttnDesc, block_tables, ctx_lens, n_draft: int) -> int:

@@ -1,7 +1,7 @@
 """The pool-table entry points on the GPU:
 
-- kvp_decode_step from host buffers (page-locked torch tensors and pageable
-  numpy arrays): the pool's tables, lengths and copy-on-write count follow the
+- kvp_decode_step from host buffers (page-locked torch tensors through the
+  prepared DecodeStep call, and pageable numpy arrays): the pool's tables, lengths and copy-on-write count follow the
   oracle's pool model, and out / lse match the fp64 oracle over the model's
   host K/V store, step after step, on a forked batch whose first appends copy
   a shared partial block;
@@ -142,7 +142,10 @@ def test_decode_step_from_host_buffers(pinned):
             hk, hv, hq = k, v, q
         io = kvp.step_io(d_q, d_out, d_lse, d_k, d_v, h_k_new=hk, h_v_new=hv, h_q=hq,
                          h_out=h_out if pinned else None, h_lse=h_lse if pinned else None)
-        need = kvp.kvp_decode_step(p.pool, seqs, 1, io, p.desc, ws)
+        if pinned:   # the prepared call (arguments marshalled once)
+            need = kvp.DecodeStep(p.pool, seqs, 1, io, p.desc, ws)()
+        else:
+            need = kvp.kvp_decode_step(p.pool, seqs, 1, io, p.desc, ws)
         torch.cuda.synchronize()
         assert 0 < need <= ws.numel()
         assert kvp.kvp_device_error(ws) == 0
