@@ -82,6 +82,16 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the kernel before it in the stream still
+// runs; griddep_wait() returns once that kernel has completed and its writes
+// are visible (at once when launched normally).  griddep_trigger() lets the
+// next kernel start launching before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // 2^x on the SFU (hardware instruction); 2^-inf = +0.
 __device__ __forceinline__ float exp2_sfu(float x) {
     float y;
@@ -751,11 +761,18 @@ __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kerne
             lut[b] = pack_bf16x2((float)lo, (float)hi);
         }
     }
+    // the plan (work items, tile descriptors, counters) was uploaded before
+    // the kernel that may still be running; K/V, q and the tree masks are
+    // read only after it has completed
+    bool waited = false;
     for (;;) {
         if (threadIdx.x == 0) s_unit = atomicAdd(a.counter, 1);
         __syncthreads();
         const int unit = s_unit;
-        if (unit >= a.n_units) break;
+        if (unit >= a.n_units) {
+            griddep_trigger();
+            break;
+        }
         // item-major order: items are sorted longest first, so the longest
         // units start first (over every layer and kv head) and the shortest
         // fill the tail; row tiles of one item, adjacent in the list, are
@@ -771,6 +788,10 @@ __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kerne
         for (int i = threadIdx.x; i < ntile * 2; i += kThreads) dst[i] = src[i];
         __syncthreads();
         const int rows = it.n_members * a.G;
+        if (!waited) {
+            griddep_wait();
+            waited = true;
+        }
         // The two-way split pays at head dim 128 (two CTAs per SM leave few
         // warps to hide latency); at head dim 64 the extra copy of the tile
         // loop costs more in instruction fetch than the split gains.
@@ -781,10 +802,13 @@ __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kerne
     }
 }
 
-// One warp per (layer, query token, query head); entries are independent
-// loads, unrolled four at a time.
+// One warp per (layer, query token, query head).  The first 32 entries are
+// read lanes-over-entries (entry id and lse, one load round), so their
+// weights sit in registers and the loads of their partial rows are all
+// independent; entries past 32 (rare) are taken one by one.
 template <int D>
-__global__ void __launch_bounds__(kThreads) merge_kernel(const AttnLaunch a) {
+__global__ void __launch_bounds__(kThreads, 8) merge_kernel(const AttnLaunch a) {
+    griddep_wait();   // the partial rows come from the attention kernel before
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gw = blockIdx.x * (kThreads / 32) + warp;
     const int qt = gw / a.Hq, h = gw % a.Hq, l = blockIdx.y;
@@ -795,20 +819,25 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const AttnLaunch a) {
     const int kvh = h / a.G, g = h % a.G;
     const size_t rb = ((size_t)l * a.Hkv + kvh) * a.P + g;
     const int32_t *ent = a.entries + md.off;
-    float M = -INFINITY;
-    for (int c = lane; c < md.cnt; c += 32) M = fmaxf(M, a.part_lse[rb + __ldg(ent + c)]);
+    int e0 = 0;
+    float l0 = -INFINITY;
+    if (lane < md.cnt) {
+        e0 = __ldg(ent + lane);
+        l0 = a.part_lse[rb + e0];
+    }
+    float M = l0;
+    for (int c = lane + 32; c < md.cnt; c += 32) M = fmaxf(M, a.part_lse[rb + __ldg(ent + c)]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float Mb = M == -INFINITY ? 0.f : M;
+    const float w0 = lane < md.cnt ? exp2_sfu(l0 - Mb) : 0.f;
+    float wsum = w0;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
     float acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = 0.f;
-    float wsum = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < md.cnt; ++c) {
-        const size_t pr = rb + __ldg(ent + c);
-        const float w = exp2_sfu(a.part_lse[pr] - Mb);
-        wsum += w;
+    auto add = [&](size_t pr, float w) {
         const float *src = a.part_o + pr * D + lane * V;
         if constexpr (V == 2) {
             const float2 x = *reinterpret_cast<const float2 *>(src);
@@ -821,6 +850,16 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const AttnLaunch a) {
             acc[2] += w * x.z;
             acc[3] += w * x.w;
         }
+    };
+    const int n0 = md.cnt < 32 ? md.cnt : 32;
+#pragma unroll 8
+    for (int j = 0; j < n0; ++j)
+        add(rb + __shfl_sync(0xffffffffu, e0, j), __shfl_sync(0xffffffffu, w0, j));
+    for (int c = 32; c < md.cnt; ++c) {
+        const size_t pr = rb + __ldg(ent + c);
+        const float w = exp2_sfu(a.part_lse[pr] - Mb);
+        wsum += w;
+        add(pr, w);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
@@ -844,6 +883,7 @@ constexpr long long kMergeGroupMin = 2048;   // group warps over all layers
 
 template <int D, int G>
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_group_kernel(const AttnLaunch a) {
+    griddep_wait();   // the partial rows come from the attention kernel before
     constexpr int NF4 = G * D / 4;        // float4s per entry
     constexpr int K = (NF4 + 31) / 32;    // float4s per lane
     constexpr int E = 32 / G;             // entries per chunk
@@ -946,6 +986,25 @@ int merge_mode() {
     return mode;
 }
 
+// Launches `kernel` with programmatic stream serialisation: it may begin
+// while the previous kernel in the stream finishes (it waits with
+// griddep_wait() before reading that kernel's results).
+template <typename Kernel>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       const AttnLaunch &a) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 template <int D>
 void launch_merge(const AttnLaunch &a, cudaStream_t stream) {
     const long long groups = (long long)a.nq * a.Hkv;
@@ -954,16 +1013,16 @@ void launch_merge(const AttnLaunch &a, cudaStream_t stream) {
     const int mode = merge_mode();
     const bool grouped = mode == 1 || (mode == 0 && groups * a.L >= kMergeGroupMin);
     switch (grouped ? a.G : 0) {
-        case 1: merge_group_kernel<D, 1><<<grid, 32 * kMergeWarps, 0, stream>>>(a); return;
-        case 2: merge_group_kernel<D, 2><<<grid, 32 * kMergeWarps, 0, stream>>>(a); return;
-        case 4: merge_group_kernel<D, 4><<<grid, 32 * kMergeWarps, 0, stream>>>(a); return;
-        case 8: merge_group_kernel<D, 8><<<grid, 32 * kMergeWarps, 0, stream>>>(a); return;
-        case 16: merge_group_kernel<D, 16><<<grid, 32 * kMergeWarps, 0, stream>>>(a); return;
+        case 1: launch_pdl(merge_group_kernel<D, 1>, grid, dim3(32 * kMergeWarps), 0, stream, a); return;
+        case 2: launch_pdl(merge_group_kernel<D, 2>, grid, dim3(32 * kMergeWarps), 0, stream, a); return;
+        case 4: launch_pdl(merge_group_kernel<D, 4>, grid, dim3(32 * kMergeWarps), 0, stream, a); return;
+        case 8: launch_pdl(merge_group_kernel<D, 8>, grid, dim3(32 * kMergeWarps), 0, stream, a); return;
+        case 16: launch_pdl(merge_group_kernel<D, 16>, grid, dim3(32 * kMergeWarps), 0, stream, a); return;
         default: break;
     }
     const long long warps = (long long)a.nq * a.Hq;
     dim3 g1((unsigned)((warps + kThreads / 32 - 1) / (kThreads / 32)), a.L);
-    merge_kernel<D><<<g1, kThreads, 0, stream>>>(a);
+    launch_pdl(merge_kernel<D>, g1, dim3(kThreads), 0, stream, a);
 }
 
 struct Occupancy {
@@ -1049,23 +1108,23 @@ cudaError_t launch_d(const AttnLaunch &a, cudaStream_t stream, cudaEvent_t befor
         Occupancy &o4 = occupancy<D, true>();
         if (!o4.ok) return cudaErrorInvalidDevice;
         const int grid = a.n_units < o4.sms * o4.per_sm ? a.n_units : o4.sms * o4.per_sm;
-        attn_item_kernel<D, true, false><<<grid, kThreads, KCfg4<D>::SMEM, mma_stream>>>(a);
+        e = launch_pdl(attn_item_kernel<D, true, false>, dim3(grid), dim3(kThreads), KCfg4<D>::SMEM, mma_stream, a);
         count_launch();
-        e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     } else if (a.n_units > 0 && a.tree_mask) {
         Occupancy &ot = occupancy<D, false, true>();
         if (!ot.ok) return cudaErrorInvalidDevice;
         const int grid = a.n_units < ot.sms * ot.per_sm ? a.n_units : ot.sms * ot.per_sm;
-        attn_item_kernel<D, false, true><<<grid, kThreads, C::SMEM, mma_stream>>>(a);
+        e = launch_pdl(attn_item_kernel<D, false, true>, dim3(grid), dim3(kThreads), C::SMEM, mma_stream, a);
         count_launch();
-        e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     } else if (a.n_units > 0) {
         const int grid = a.n_units < occ.sms * occ.per_sm ? a.n_units : occ.sms * occ.per_sm;
-        attn_item_kernel<D, false, false><<<grid, kThreads, C::SMEM, mma_stream>>>(a);
+        e = launch_pdl(attn_item_kernel<D, false, false>, dim3(grid), dim3(kThreads), C::SMEM, mma_stream, a);
         count_launch();
-        e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (mma_stream != stream) {

@@ -122,6 +122,13 @@ bool pool_drop_block(kvp_pool *p, int32_t b);
 int append_batch_check(kvp_pool *p, int32_t nseq, const int32_t *seqs, const int32_t *ntoks,
                        int64_t *total_out = nullptr);
 
+// seq_append_batch in two halves: the checks and the bookkeeping (the slots
+// and copy-on-write triples stay staged in the pool), then the device write
+// of the staged append.  Nothing else may touch the pool in between.
+int append_batch_commit(kvp_pool *p, int32_t nseq, const int32_t *seqs, const int32_t *ntoks, const void *k,
+                        const void *v, int32_t *total_out);
+int append_issue(kvp_pool *p, const void *k, const void *v, int32_t total, void *stream);
+
 // A pool's shape and device storage (codes and exponents for 4-bit pages).
 struct PoolView {
     int32_t L, NB, bs, Hkv, d;

@@ -470,10 +470,20 @@ thread_local std::vector<unsigned char> t_image;
 thread_local cudaEvent_t t_ev_before = nullptr, t_ev_after = nullptr;
 std::atomic<long long> g_launches{0};
 
+// An append whose bookkeeping is done and whose device write is issued
+// between the plan upload and the attention launch, so that the attention
+// kernel follows the write kernel directly in the stream (and may start
+// while it finishes).
+struct StagedAppend {
+    kvp_pool *pool;
+    const void *k, *v;
+    int32_t total;
+};
+
 int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k_pool,
         const void *v_pool, int32_t nq, const int32_t *parent, int32_t n_draft, void *out,
         float *lse, void *ws, size_t ws_bytes, cudaStream_t stream, const void *k_exp = nullptr,
-        const void *v_exp = nullptr) {
+        const void *v_exp = nullptr, const StagedAppend *append = nullptr) {
     if (!q || !k_pool || !v_pool || !out || !ws) return KVP_ERR_INVALID;
     const bool kv4 = d.kv_format == KVP_KV_4BIT;
     if (kv4 && (!k_exp || !v_exp || (((uintptr_t)k_exp | (uintptr_t)v_exp) & 15))) return KVP_ERR_INVALID;
@@ -503,6 +513,10 @@ int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k
     // pageable source: the copy is staged before the call returns
     if (cudaMemcpyAsync(ws, img, w.plan_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return KVP_ERR_CUDA;
+    if (append) {
+        const int rc = append_issue(append->pool, append->k, append->v, append->total, stream);
+        if (rc) return rc;
+    }
     unsigned char *base = (unsigned char *)ws;
     AttnLaunch a{};
     a.q = q; a.k_pool = k_pool; a.v_pool = v_pool;
@@ -549,9 +563,10 @@ int plan_pool(const kvp_pool *pool, const int32_t *seqs, int32_t n, const kvp_at
 }
 
 int run_pool(const HostPlan &hp, const kvp_attn_desc &d, const PoolView &pv, const void *q, int32_t n,
-             void *out, float *lse, void *ws, size_t ws_bytes, cudaStream_t stream) {
+             void *out, float *lse, void *ws, size_t ws_bytes, cudaStream_t stream,
+             const StagedAppend *append = nullptr) {
     return run(hp, d, q, pv.k, pv.v, n, nullptr, 0, out, lse, ws, ws_bytes, stream,
-               pv.kv4 ? pv.k_exp : nullptr, pv.kv4 ? pv.v_exp : nullptr);
+               pv.kv4 ? pv.k_exp : nullptr, pv.kv4 ? pv.v_exp : nullptr, append);
 }
 
 }  // namespace
@@ -658,9 +673,9 @@ int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, in
     const size_t rows = (size_t)desc->num_layers * num_seqs * desc->num_q_heads;
     const size_t q_bytes = rows * desc->head_dim * 2, lse_bytes = rows * sizeof(float);
     cudaStream_t st = (cudaStream_t)stream;
+    thread_local std::vector<int32_t> t_ntoks;
     if (ntok > 0) {   // the appends must fit before anything is enqueued
         if (!a16(io->d_k_new) || !a16(io->d_v_new)) return KVP_ERR_INVALID;
-        thread_local std::vector<int32_t> t_ntoks;
         t_ntoks.assign(num_seqs, ntok);
         int rc = append_batch_check(pool, num_seqs, seq_ids, t_ntoks.data());
         if (rc) return rc;
@@ -671,19 +686,26 @@ int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, in
         return KVP_ERR_CUDA;
     if (io->h_q && cudaMemcpyAsync(io->d_q, io->h_q, q_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return KVP_ERR_CUDA;
+    // the append's bookkeeping now, its device write right before attention
+    StagedAppend staged{pool, io->d_k_new, io->d_v_new, 0};
     if (ntok > 0) {
-        thread_local std::vector<int32_t> t_ntoks;
-        t_ntoks.assign(num_seqs, ntok);
-        int rc = seq_append_batch(pool, num_seqs, seq_ids, t_ntoks.data(), io->d_k_new, io->d_v_new, stream);
+        int rc = append_batch_commit(pool, num_seqs, seq_ids, t_ntoks.data(), io->d_k_new, io->d_v_new,
+                                     &staged.total);
         if (rc) return rc;
     }
     HostPlan hp;
     int rc = plan_pool(pool, seq_ids, num_seqs, *desc, hp);
-    if (rc) return rc;
-    const size_t need = layout(hp, *desc).total;
-    if (ws_needed) *ws_needed = need;
-    if (ws_bytes < need) return KVP_ERR_WORKSPACE;
-    rc = run_pool(hp, *desc, pv, io->d_q, num_seqs, io->d_out, io->d_lse, workspace, ws_bytes, st);
+    if (rc == KVP_OK) {
+        const size_t need = layout(hp, *desc).total;
+        if (ws_needed) *ws_needed = need;
+        if (ws_bytes < need) rc = KVP_ERR_WORKSPACE;
+    }
+    if (rc) {   // the pool already holds the new tokens: write them
+        if (ntok > 0 && append_issue(pool, staged.k, staged.v, staged.total, stream)) return KVP_ERR_CUDA;
+        return rc;
+    }
+    rc = run_pool(hp, *desc, pv, io->d_q, num_seqs, io->d_out, io->d_lse, workspace, ws_bytes, st,
+                  ntok > 0 ? &staged : nullptr);
     if (rc) return rc;
     if (io->h_out && cudaMemcpyAsync(io->h_out, io->d_out, q_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return KVP_ERR_CUDA;

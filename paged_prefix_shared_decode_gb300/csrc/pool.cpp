@@ -415,15 +415,10 @@ int seq_append(kvp_pool *p, int32_t seq, const void *k, const void *v, int32_t n
 
 int seq_append_batch(kvp_pool *p, int32_t nseq, const int32_t *seqs, const int32_t *ntoks,
                      const void *k, const void *v, void *stream) {
-    int64_t total = 0;
-    int rc = kvp::append_batch_check(p, nseq, seqs, ntoks, &total);
-    if (rc != KVP_OK && rc != KVP_ERR_OOM) return rc;
-    if (total > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return KVP_ERR_INVALID;
+    int32_t total = 0;
+    int rc = kvp::append_batch_commit(p, nseq, seqs, ntoks, k, v, &total);
     if (rc) return rc;
-    p->slots.clear();
-    p->cow.clear();
-    for (int32_t i = 0; i < nseq; ++i) commit_append(p, seqs[i], ntoks[i], p->slots, p->cow);
-    return issue_write(p, k, v, (int32_t)total, stream);
+    return issue_write(p, k, v, total, stream);
 }
 
 int seq_block_table(const kvp_pool *p, int32_t seq, int32_t *host_out, int32_t cap,
@@ -549,6 +544,24 @@ int append_batch_check(kvp_pool *p, int32_t nseq, const int32_t *seqs, const int
     if (total_out) *total_out = total;
     if (need > (int64_t)p->free_.size()) return KVP_ERR_OOM;
     return KVP_OK;
+}
+
+int append_batch_commit(kvp_pool *p, int32_t nseq, const int32_t *seqs, const int32_t *ntoks, const void *k,
+                        const void *v, int32_t *total_out) {
+    int64_t total = 0;
+    int rc = append_batch_check(p, nseq, seqs, ntoks, &total);
+    if (rc != KVP_OK && rc != KVP_ERR_OOM) return rc;
+    if (total > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return KVP_ERR_INVALID;
+    if (rc) return rc;
+    p->slots.clear();
+    p->cow.clear();
+    for (int32_t i = 0; i < nseq; ++i) commit_append(p, seqs[i], ntoks[i], p->slots, p->cow);
+    *total_out = (int32_t)total;
+    return KVP_OK;
+}
+
+int append_issue(kvp_pool *p, const void *k, const void *v, int32_t total, void *stream) {
+    return issue_write(p, k, v, total, stream);
 }
 
 PoolView pool_view(const kvp_pool *p) {
