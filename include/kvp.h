@@ -406,7 +406,14 @@ int paged_decode_attention_pool(const kvp_pool *pool, const int32_t *seq_ids, in
  * The call returns once all of it is enqueued; host outputs are valid after
  * the stream synchronises, and host inputs must stay untouched until then.
  * Page-locked host buffers make the copies asynchronous; pageable ones work,
- * but the driver then stages each copy before returning.
+ * but the driver then stages each copy before returning.  With
+ * KVP_STEP_HOST_MAPPED in io->flags the host buffers must be page-locked and
+ * addressable by the device (cudaHostAlloc, or registered with
+ * cudaHostRegisterMapped; under unified addressing any page-locked memory)
+ * and 16-byte aligned: the inputs then cross in one copy kernel into the d_*
+ * buffers, and the attention kernels write out and lse straight into h_out /
+ * h_lse (d_out and d_lse are then neither read nor written and may be NULL),
+ * instead of one copy-engine transfer per buffer.
  *
  * Shapes: k_new, v_new [L][num_seqs * ntok][Hkv][d] bf16, sequence-major;
  * q, out [L][num_seqs][Hq][d] bf16; lse [L][num_seqs][Hq] fp32 (d_lse may be
@@ -426,7 +433,10 @@ typedef struct {
     void *d_k_new, *d_v_new, *d_q;       /* device inputs / staging */
     void *d_out;                         /* device outputs */
     float *d_lse;
+    uint32_t flags;                      /* KVP_STEP_* */
 } kvp_step_io;
+
+enum { KVP_STEP_HOST_MAPPED = 1 };
 
 int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, int32_t ntok,
                     const kvp_step_io *io, const kvp_attn_desc *desc, void *workspace,

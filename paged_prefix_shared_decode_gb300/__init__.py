@@ -25,7 +25,7 @@ __all__ = [
     "kvp_set_kernel_events", "kvp_kernel_launches", "paged_decode_attention_noalloc",
     "paged_decode_attention_kv4", "KVP_KV_BF16", "KVP_KV_4BIT",
     "kvp_pool_decode_workspace_size", "paged_decode_attention_pool", "StepIO", "step_io", "kvp_decode_step",
-    "DecodeStep",
+    "DecodeStep", "KVP_STEP_HOST_MAPPED",
     "KVP_STATIC_WORKSPACE_BYTES",
     "KVP_OK", "KVP_ERR_INVALID", "KVP_ERR_OOM", "KVP_ERR_STATE", "KVP_ERR_CUDA", "KVP_ERR_DEVICE",
     "KVP_ERR_WORKSPACE",
@@ -76,7 +76,11 @@ class AttnDesc(ctypes.Structure):
 class StepIO(ctypes.Structure):
     """kvp_step_io: host (h_*) and device (d_*) buffers of one decode step."""
     _fields_ = [(n, ctypes.c_void_p) for n in ("h_k_new", "h_v_new", "h_q", "h_out", "h_lse",
-                                               "d_k_new", "d_v_new", "d_q", "d_out", "d_lse")]
+                                               "d_k_new", "d_v_new", "d_q", "d_out", "d_lse")] + \
+               [("flags", ctypes.c_uint32)]
+
+
+KVP_STEP_HOST_MAPPED = 1   # kvp_step_io.flags: host buffers page-locked and device-addressable
 
 
 _P = ctypes.c_void_p
@@ -392,11 +396,16 @@ def _host(x):
 
 
 def step_io(d_q, d_out, d_lse=None, d_k_new=None, d_v_new=None, h_k_new=None, h_v_new=None, h_q=None,
-            h_out=None, h_lse=None) -> StepIO:
+            h_out=None, h_lse=None, host_mapped=None) -> StepIO:
     """A kvp_step_io.  It holds raw addresses: keep the tensors alive while it
-    is in use."""
+    is in use.  host_mapped (default: every host buffer given is a pinned
+    torch tensor) sets KVP_STEP_HOST_MAPPED."""
+    hosts = [x for x in (h_k_new, h_v_new, h_q, h_out, h_lse) if x is not None]
+    if host_mapped is None:
+        host_mapped = bool(hosts) and all(not isinstance(x, (int, np.ndarray)) and x.is_pinned() for x in hosts)
     return StepIO(_host(h_k_new), _host(h_v_new), _host(h_q), _host(h_out), _host(h_lse),
-                  _dev(d_k_new), _dev(d_v_new), _dev(d_q), _dev(d_out), _dev(d_lse))
+                  _dev(d_k_new), _dev(d_v_new), _dev(d_q), _dev(d_out), _dev(d_lse),
+                  KVP_STEP_HOST_MAPPED if host_mapped else 0)
 
 
 def kvp_decode_step(pool, seq_ids, ntok: int, io: StepIO, desc: AttnDesc, workspace, ws_bytes=None,

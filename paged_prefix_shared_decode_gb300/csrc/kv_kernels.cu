@@ -27,6 +27,7 @@ constexpr int kMaxCow = 256;      // copy-on-write triples per launch
 constexpr int kSmallSlots = 64, kSmallCow = 16;
 constexpr int kMaxMoves = kMaxDraft;   // kept draft tokens per accept
 constexpr int kMaxMoveCow = kMaxDraft; // blocks copied before the moves (bs 1: one per token)
+constexpr int kMaxSegs = 4;            // buffers of one copy launch
 
 template <int NS, int NC>
 struct KvWriteArgs {
@@ -158,7 +159,54 @@ cudaError_t launch_part(const KvWrite &w, int cow_done, int ncow, int tok_done, 
     return cudaGetLastError();
 }
 
+// Copies up to kMaxSegs buffers in one launch, through the SMs: a decode
+// step's inputs from page-locked host memory.  Every segment is 16-byte
+// aligned; whole 16-byte chunks first, then the last bytes (a multiple of 4)
+// one word at a time.
+struct CopySegs {
+    const void *src[kMaxSegs];
+    void *dst[kMaxSegs];
+    int64_t bytes[kMaxSegs];
+    int32_t n;
+};
+
+__global__ void __launch_bounds__(256) copy_segs_kernel(const __grid_constant__ CopySegs c) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int s = 0; s < c.n; ++s) {
+        const int64_t n16 = c.bytes[s] >> 4;
+        const uint4 *src = static_cast<const uint4 *>(c.src[s]);
+        uint4 *dst = static_cast<uint4 *>(c.dst[s]);
+        for (int64_t i = t0; i < n16; i += stride) dst[i] = src[i];
+        const int64_t w0 = n16 * 4, nw = c.bytes[s] >> 2;
+        const uint32_t *sw = static_cast<const uint32_t *>(c.src[s]);
+        uint32_t *dw = static_cast<uint32_t *>(c.dst[s]);
+        for (int64_t i = w0 + t0; i < nw; i += stride) dw[i] = sw[i];
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_copy_segments(const void *const *src, void *const *dst, const int64_t *bytes, int n,
+                                 cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    if (n > kMaxSegs) return cudaErrorInvalidValue;
+    CopySegs c{};
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) {
+        c.src[i] = src[i];
+        c.dst[i] = dst[i];
+        c.bytes[i] = bytes[i];
+        total += bytes[i];
+    }
+    c.n = n;
+    // about one 16-byte chunk per thread, at most two CTAs per SM
+    const int64_t want = (total / 16 + 255) / 256;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, 2LL * device_sm_count()));
+    copy_segs_kernel<<<grid, 256, 0, stream>>>(c);
+    count_launch();
+    return cudaGetLastError();
+}
 
 cudaError_t launch_kv_move(const KvMove &m, cudaStream_t stream) {
     if (m.ncow == 0 && m.nmove == 0) return cudaSuccess;

@@ -186,6 +186,11 @@ struct KvMove {
 
 cudaError_t launch_kv_move(const KvMove &m, cudaStream_t stream);
 
+// One launch copying n <= 4 buffers (16-byte aligned, sizes multiples of 4)
+// through the SMs.
+cudaError_t launch_copy_segments(const void *const *src, void *const *dst, const int64_t *bytes, int n,
+                                 cudaStream_t stream);
+
 // The same two for a pool of 4-bit pages: codes [L][NB][Hkv][bs][d/2] bytes
 // (two signed 4-bit codes per byte, element 2i in the low nibble) and one
 // int8 power-of-two exponent per (token, kv head) row [L][NB][Hkv][bs].

@@ -662,35 +662,55 @@ int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, in
         return KVP_ERR_INVALID;
     const PoolView pv = pool_view(pool);
     if (!desc_matches_pool(*desc, pv)) return KVP_ERR_INVALID;
+    if (io->flags & ~(uint32_t)KVP_STEP_HOST_MAPPED) return KVP_ERR_INVALID;
+    if ((int64_t)num_seqs * ntok > INT32_MAX / 2) return KVP_ERR_INVALID;
+    // Inputs go to the device buffers (copy-engine transfers, or one copy
+    // kernel over all of them from mapped host memory); mapped host outputs
+    // are written straight by the attention kernels.
+    const bool mapped = (io->flags & KVP_STEP_HOST_MAPPED) != 0;
+    const void *k_new = io->d_k_new, *v_new = io->d_v_new, *q = io->d_q;
+    void *out = mapped && io->h_out ? io->h_out : io->d_out;
+    float *lse = mapped && io->h_lse ? io->h_lse : io->d_lse;
     // everything the attention launch would reject, checked before any work
     auto a16 = [](const void *p) { return ((uintptr_t)p & 15) == 0; };
-    if (!io->d_q || !io->d_out || !a16(io->d_q) || !a16(io->d_out) || ((uintptr_t)io->d_lse & 3) ||
-        ((uintptr_t)workspace & 255) || (io->h_lse && !io->d_lse))
+    if (!q || !out || !a16(q) || !a16(out) || ((uintptr_t)lse & 3) || ((uintptr_t)workspace & 255))
         return KVP_ERR_INVALID;
-    if (ntok > 0 && (!io->d_k_new || !io->d_v_new)) return KVP_ERR_INVALID;
-    if ((int64_t)num_seqs * ntok > INT32_MAX / 2) return KVP_ERR_INVALID;
+    if (!mapped && ((io->h_out && !io->d_out) || (io->h_lse && !io->d_lse))) return KVP_ERR_INVALID;
+    if (mapped && !(a16(io->h_k_new) && a16(io->h_v_new) && a16(io->h_q))) return KVP_ERR_INVALID;
     const size_t kv_bytes = (size_t)pv.L * num_seqs * ntok * pv.Hkv * pv.d * 2;
     const size_t rows = (size_t)desc->num_layers * num_seqs * desc->num_q_heads;
     const size_t q_bytes = rows * desc->head_dim * 2, lse_bytes = rows * sizeof(float);
     cudaStream_t st = (cudaStream_t)stream;
     thread_local std::vector<int32_t> t_ntoks;
     if (ntok > 0) {   // the appends must fit before anything is enqueued
-        if (!a16(io->d_k_new) || !a16(io->d_v_new)) return KVP_ERR_INVALID;
+        if (!k_new || !v_new || !a16(k_new) || !a16(v_new)) return KVP_ERR_INVALID;
         t_ntoks.assign(num_seqs, ntok);
         int rc = append_batch_check(pool, num_seqs, seq_ids, t_ntoks.data());
         if (rc) return rc;
     }
-    if (io->h_k_new && ntok > 0 &&
-        (cudaMemcpyAsync(io->d_k_new, io->h_k_new, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-         cudaMemcpyAsync(io->d_v_new, io->h_v_new, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess))
-        return KVP_ERR_CUDA;
-    if (io->h_q && cudaMemcpyAsync(io->d_q, io->h_q, q_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return KVP_ERR_CUDA;
+    if (mapped) {   // all inputs in one copy kernel
+        const void *src[3];
+        void *dst[3];
+        int64_t len[3];
+        int n = 0;
+        if (io->h_k_new && ntok > 0) {
+            src[n] = io->h_k_new, dst[n] = io->d_k_new, len[n++] = (int64_t)kv_bytes;
+            src[n] = io->h_v_new, dst[n] = io->d_v_new, len[n++] = (int64_t)kv_bytes;
+        }
+        if (io->h_q) src[n] = io->h_q, dst[n] = io->d_q, len[n++] = (int64_t)q_bytes;
+        if (launch_copy_segments(src, dst, len, n, st) != cudaSuccess) return KVP_ERR_CUDA;
+    } else {
+        if (io->h_k_new && ntok > 0 &&
+            (cudaMemcpyAsync(io->d_k_new, io->h_k_new, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+             cudaMemcpyAsync(io->d_v_new, io->h_v_new, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess))
+            return KVP_ERR_CUDA;
+        if (io->h_q && cudaMemcpyAsync(io->d_q, io->h_q, q_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return KVP_ERR_CUDA;
+    }
     // the append's bookkeeping now, its device write right before attention
-    StagedAppend staged{pool, io->d_k_new, io->d_v_new, 0};
+    StagedAppend staged{pool, k_new, v_new, 0};
     if (ntok > 0) {
-        int rc = append_batch_commit(pool, num_seqs, seq_ids, t_ntoks.data(), io->d_k_new, io->d_v_new,
-                                     &staged.total);
+        int rc = append_batch_commit(pool, num_seqs, seq_ids, t_ntoks.data(), k_new, v_new, &staged.total);
         if (rc) return rc;
     }
     HostPlan hp;
@@ -704,9 +724,9 @@ int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, in
         if (ntok > 0 && append_issue(pool, staged.k, staged.v, staged.total, stream)) return KVP_ERR_CUDA;
         return rc;
     }
-    rc = run_pool(hp, *desc, pv, io->d_q, num_seqs, io->d_out, io->d_lse, workspace, ws_bytes, st,
-                  ntok > 0 ? &staged : nullptr);
+    rc = run_pool(hp, *desc, pv, q, num_seqs, out, lse, workspace, ws_bytes, st, ntok > 0 ? &staged : nullptr);
     if (rc) return rc;
+    if (mapped) return KVP_OK;
     if (io->h_out && cudaMemcpyAsync(io->h_out, io->d_out, q_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return KVP_ERR_CUDA;
     if (io->h_lse && cudaMemcpyAsync(io->h_lse, io->d_lse, lse_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)

@@ -1,7 +1,8 @@
 """The pool-table entry points on the GPU:
 
 - kvp_decode_step from host buffers (page-locked torch tensors through the
-  prepared DecodeStep call, and pageable numpy arrays): the pool's tables, lengths and copy-on-write count follow the
+  prepared DecodeStep call, crossing in copy kernels or copy-engine
+  transfers, and pageable numpy arrays): the pool's tables, lengths and copy-on-write count follow the
   oracle's pool model, and out / lse match the fp64 oracle over the model's
   host K/V store, step after step, on a forked batch whose first appends copy
   a shared partial block;
@@ -118,8 +119,11 @@ class Pool:
         return out, lse
 
 
-@pytest.mark.parametrize("pinned", [True, False])
-def test_decode_step_from_host_buffers(pinned):
+@pytest.mark.parametrize("mode", ["mapped", "pinned", "pageable"])
+def test_decode_step_from_host_buffers(mode):
+    # mapped: page-locked buffers crossing in one copy kernel each way;
+    # pinned: the same buffers through copy-engine transfers; pageable: numpy
+    pinned = mode != "pageable"
     p = Pool()
     seqs = p.forked_batch()
     S = len(seqs)
@@ -141,7 +145,9 @@ def test_decode_step_from_host_buffers(pinned):
         else:   # pageable numpy buffers
             hk, hv, hq = k, v, q
         io = kvp.step_io(d_q, d_out, d_lse, d_k, d_v, h_k_new=hk, h_v_new=hv, h_q=hq,
-                         h_out=h_out if pinned else None, h_lse=h_lse if pinned else None)
+                         h_out=h_out if pinned else None, h_lse=h_lse if pinned else None,
+                         host_mapped=mode == "mapped")
+        assert io.flags == (kvp.KVP_STEP_HOST_MAPPED if mode == "mapped" else 0)
         if pinned:   # the prepared call (arguments marshalled once)
             need = kvp.DecodeStep(p.pool, seqs, 1, io, p.desc, ws)()
         else:
