@@ -51,13 +51,72 @@ struct Seg {
     int32_t lo, hi;       // members (positions in pre-order) [lo, hi)
 };
 
+struct HostPlan {
+    std::vector<WorkItem> items;      // mma.sync kernel
+    std::vector<WorkItem> tc_items;   // tcgen05 kernel
+    std::vector<KvTile> tiles;
+    std::vector<int32_t> members;
+    std::vector<MergeDesc> merge;
+    std::vector<int32_t> entries;
+    int32_t n_row_tiles = 0, n_partial_rows = 0, n_units = 0, n_tc_units = 0;
+    int32_t n_tree_q = 0;   // query tokens with a draft-tree mask (verify)
+    int64_t unique_kv_bytes = 0;
+
+    void clear() {
+        items.clear();
+        tc_items.clear();
+        tiles.clear();
+        members.clear();
+        merge.clear();
+        entries.clear();
+        n_row_tiles = n_partial_rows = n_units = n_tc_units = n_tree_q = 0;
+        unique_kv_bytes = 0;
+    }
+};
+
+// Items before chunking, stored flat: item i has members [m0, m1) of `mem`
+// (query tokens) and KV tiles [t0, t1) of `kv`.
+struct Protos {
+    struct Item {
+        int32_t m0, m1, t0, t1;
+    };
+    std::vector<int32_t> mem;
+    std::vector<KvTile> kv;
+    std::vector<Item> items;
+    void clear() {
+        mem.clear();
+        kv.clear();
+        items.clear();
+    }
+    int32_t n_mem(const Item &it) const { return it.m1 - it.m0; }
+    int32_t n_kv(const Item &it) const { return it.t1 - it.t0; }
+};
+
+// Working storage of the planner, kept per thread so that planning a batch
+// allocates nothing once the buffers have grown to its size.
+struct Scratch {
+    std::vector<int32_t> nblk, order, members, gid, tmp, gcount, bounds, priv_seg, priv_cnt;
+    std::vector<int64_t> gkeys;
+    std::unordered_map<int64_t, int32_t> gmap;
+    std::vector<Seg> segs;
+    Protos protos, packed;
+    std::vector<int32_t> cur_mem;
+    std::vector<KvTile> cur_kv;
+    std::vector<int32_t> cover, ent_cnt, ent_pos;
+    struct Chunked {
+        WorkItem it;
+        int64_t cost;
+        int32_t idx;
+        bool tc;
+    };
+    std::vector<Chunked> cs;
+};
+
 struct Builder {
     const int32_t *tables;
     const int32_t *lens;
     int32_t S, MB, bs;
-    std::vector<int32_t> nblk;
-    std::vector<int32_t> order;   // pre-order of sequences
-    std::vector<Seg> segs;
+    Scratch &sc;
 
     int32_t valid(int32_t s, int32_t j) const { return std::min(bs, lens[s] - j * bs); }
     int64_t key(int32_t s, int32_t j) const {
@@ -69,7 +128,7 @@ struct Builder {
     // block both hold full blocks, so only that block's valid count needs
     // comparing.
     int32_t agree(int32_t s0, int32_t s1, int32_t from) const {
-        const int32_t lim = std::min(nblk[s0], nblk[s1]);
+        const int32_t lim = std::min(sc.nblk[s0], sc.nblk[s1]);
         const int32_t *r0 = tables + (size_t)s0 * MB, *r1 = tables + (size_t)s1 * MB;
         int32_t x = from;
         while (x < lim && r0[x] == r1[x]) ++x;
@@ -77,76 +136,72 @@ struct Builder {
         return x;
     }
 
-    // `members` share blocks [0, j); emit their subtree
-    void build(const std::vector<int32_t> &members, int32_t j) {
-        std::vector<int32_t> rest;
-        for (int32_t s : members) {
-            if (nblk[s] <= j) order.push_back(s);   // path ends here: first in order
-            else rest.push_back(s);
+    // The n members at m (rows of the tables) share blocks [0, j); emit their
+    // subtree.  Members whose rows end at j come first in pre-order; the rest
+    // are regrouped in place by the key of block j, groups in order of first
+    // appearance (a linear scan while there are few distinct keys, a hash map
+    // after), and each group is handled in turn.
+    void build(int32_t *m, int32_t n, int32_t j) {
+        int32_t nr = 0;
+        for (int32_t i = 0; i < n; ++i) {
+            if (sc.nblk[m[i]] <= j) sc.order.push_back(m[i]);
+            else m[nr++] = m[i];
         }
-        // group by the key of block j, groups in order of first appearance
-        // (a linear scan while there are few distinct keys, a hash map after)
-        std::vector<std::vector<int32_t>> groups;
-        std::vector<int64_t> gkeys;
-        std::unordered_map<int64_t, size_t> gi;
-        for (int32_t s : rest) {
-            const int64_t k = key(s, j);
-            size_t g = groups.size();
-            if (gi.empty()) {
-                for (size_t i = 0; i < gkeys.size(); ++i)
-                    if (gkeys[i] == k) { g = i; break; }
-                if (g == groups.size() && gkeys.size() == 16)
-                    for (size_t i = 0; i < gkeys.size(); ++i) gi.emplace(gkeys[i], i);
+        if (nr == 0) return;
+        sc.gkeys.clear();
+        sc.gmap.clear();
+        sc.gid.resize(nr);
+        for (int32_t i = 0; i < nr; ++i) {
+            const int64_t k = key(m[i], j);
+            int32_t g = (int32_t)sc.gkeys.size();
+            if (sc.gmap.empty()) {
+                for (int32_t x = 0; x < (int32_t)sc.gkeys.size(); ++x)
+                    if (sc.gkeys[x] == k) { g = x; break; }
+                if (g == (int32_t)sc.gkeys.size() && sc.gkeys.size() == 16)
+                    for (int32_t x = 0; x < 16; ++x) sc.gmap.emplace(sc.gkeys[x], x);
             }
-            if (!gi.empty()) {
-                auto ins = gi.emplace(k, groups.size());
-                g = ins.first->second;
-            }
-            if (g == groups.size()) {
-                groups.emplace_back();
-                gkeys.push_back(k);
-            }
-            groups[g].push_back(s);
+            if (!sc.gmap.empty()) g = sc.gmap.emplace(k, (int32_t)sc.gkeys.size()).first->second;
+            if (g == (int32_t)sc.gkeys.size()) sc.gkeys.push_back(k);
+            sc.gid[i] = g;
         }
-        for (auto &g : groups) {
-            if (g.size() == 1) {   // a single member: its whole remaining row is one segment
-                const int32_t s = g[0];
-                segs.push_back(Seg{j * bs, lens[s], s, (int32_t)order.size(), (int32_t)order.size() + 1});
-                order.push_back(s);
+        const int32_t ng = (int32_t)sc.gkeys.size();
+        // group boundaries of this call sit on a shared stack: the recursion
+        // below reuses every other scratch buffer
+        const size_t base = sc.bounds.size();
+        sc.bounds.resize(base + ng + 1, 0);
+        for (int32_t i = 0; i < nr; ++i) sc.bounds[base + sc.gid[i] + 1] += 1;
+        for (int32_t g = 0; g < ng; ++g) sc.bounds[base + g + 1] += sc.bounds[base + g];
+        sc.gcount.assign(sc.bounds.begin() + base, sc.bounds.begin() + base + ng);
+        sc.tmp.resize(nr);
+        for (int32_t i = 0; i < nr; ++i) sc.tmp[sc.gcount[sc.gid[i]]++] = m[i];
+        std::copy(sc.tmp.begin(), sc.tmp.begin() + nr, m);
+        for (int32_t g = 0; g < ng; ++g) {
+            int32_t *gm = m + sc.bounds[base + g];
+            const int32_t gn = sc.bounds[base + g + 1] - sc.bounds[base + g];
+            if (gn == 1) {   // a single member: its whole remaining row is one segment
+                const int32_t s0 = gm[0];
+                sc.segs.push_back(Seg{j * bs, lens[s0], s0, (int32_t)sc.order.size(), (int32_t)sc.order.size() + 1});
+                sc.order.push_back(s0);
                 continue;
             }
             // the group shares blocks [j, j1): j1 is the first block where
             // some member's key differs from the first member's (or a row
             // ends), found row by row
-            int32_t j1 = nblk[g[0]];
-            for (size_t i = 1; i < g.size() && j1 > j + 1; ++i) j1 = std::min(j1, agree(g[0], g[i], j + 1));
-            size_t si = segs.size();
-            segs.push_back(Seg{j * bs, std::min(j1 * bs, lens[g[0]]), g[0], 0, 0});
-            int32_t lo = (int32_t)order.size();
-            build(g, j1);
-            segs[si].lo = lo;
-            segs[si].hi = (int32_t)order.size();
+            int32_t j1 = sc.nblk[gm[0]];
+            for (int32_t i = 1; i < gn && j1 > j + 1; ++i) j1 = std::min(j1, agree(gm[0], gm[i], j + 1));
+            const size_t si = sc.segs.size();
+            sc.segs.push_back(Seg{j * bs, std::min(j1 * bs, lens[gm[0]]), gm[0], 0, 0});
+            const int32_t lo = (int32_t)sc.order.size();
+            build(gm, gn, j1);
+            sc.segs[si].lo = lo;
+            sc.segs[si].hi = (int32_t)sc.order.size();
         }
+        sc.bounds.resize(base);
     }
 };
 
-struct HostPlan {
-    std::vector<WorkItem> items;      // mma.sync kernel
-    std::vector<WorkItem> tc_items;   // tcgen05 kernel
-    std::vector<KvTile> tiles;
-    std::vector<int32_t> members;
-    std::vector<MergeDesc> merge;
-    std::vector<int32_t> entries;
-    int32_t n_row_tiles = 0, n_partial_rows = 0, n_units = 0, n_tc_units = 0;
-    int32_t n_tree_q = 0;   // query tokens with a draft-tree mask (verify)
-    int64_t unique_kv_bytes = 0;
-};
-
-// An item before chunking: members (query tokens) and its KV tiles.
-struct ProtoItem {
-    std::vector<int32_t> members;
-    std::vector<KvTile> kv;
-};
+thread_local Scratch t_scratch;
+thread_local HostPlan t_plan;
 
 }  // namespace
 
@@ -214,60 +269,85 @@ void push_range(std::vector<KvTile> &kv, const TileSrc &src, int32_t row, int32_
     }
 }
 
+// Opens an item of `protos` whose members are given; tiles are then pushed
+// to protos.kv and close_item() ends it (an item without tiles is dropped).
+void open_item(Protos &pr, const int32_t *mem, int32_t n) {
+    pr.items.push_back(Protos::Item{(int32_t)pr.mem.size(), 0, (int32_t)pr.kv.size(), 0});
+    pr.mem.insert(pr.mem.end(), mem, mem + n);
+    pr.items.back().m1 = (int32_t)pr.mem.size();
+}
+void close_item(Protos &pr) {
+    Protos::Item &it = pr.items.back();
+    it.t1 = (int32_t)pr.kv.size();
+    if (it.t1 == it.t0) {
+        pr.mem.resize(it.m0);
+        pr.items.pop_back();
+    }
+}
+
 // Chunk items into work items, lay out partial rows and merge lists.  Items
 // with more than `thr` rows go to the tcgen05 kernel (one CTA per SM), the
 // rest to the mma.sync kernel (`mma_ctas` CTAs per SM).
 // Items of at most 16 rows and a few tiles cost more in per-unit start-up
-// than in work; pack them into items of up to 64 rows, each tile keeping the
-// member interval of the item it came from.
-void pack_small(std::vector<ProtoItem> &protos, int32_t G, int thr) {
-    // stay on the mma.sync kernel: at most 64 rows and at most the threshold
-    const int kPackRows = thr < 64 ? thr : 64;
+// than in work; pack them into items of up to 32 rows, each tile keeping the
+// member interval of the item it came from.  (A tile of one member leaves
+// the warps of the other members' rows idle, so packs stay small: 32 rows
+// measured 8% faster than 64 on Trellis phi = 0.9 and equal on MCTS; no
+// packing made MCTS 43% slower.)
+void pack_small(Scratch &sc, int32_t G, int thr) {
+    // stay on the mma.sync kernel: at most 32 rows and at most the threshold
+    const int kPackRows = thr < 32 ? thr : 32;
     constexpr int kPackTiles = 4, kPackMaxTiles = 64;
-    std::vector<ProtoItem> out;
-    ProtoItem cur;
+    const Protos &in = sc.protos;
+    Protos &out = sc.packed;
+    out.clear();
+    sc.cur_mem.clear();
+    sc.cur_kv.clear();
     auto flush = [&]() {
-        if (!cur.members.empty()) out.push_back(std::move(cur));
-        cur = ProtoItem{};
+        if (sc.cur_mem.empty()) return;
+        open_item(out, sc.cur_mem.data(), (int32_t)sc.cur_mem.size());
+        out.kv.insert(out.kv.end(), sc.cur_kv.begin(), sc.cur_kv.end());
+        close_item(out);
+        sc.cur_mem.clear();
+        sc.cur_kv.clear();
     };
-    for (auto &p : protos) {
-        const int rows = (int)p.members.size() * G;
-        const bool small = rows <= 16 && rows <= thr && (int)p.kv.size() <= kPackTiles;
+    for (const auto &p : in.items) {
+        const int rows = in.n_mem(p) * G;
+        const bool small = rows <= 16 && rows <= thr && in.n_kv(p) <= kPackTiles;
         if (!small) {
-            out.push_back(std::move(p));
+            open_item(out, in.mem.data() + p.m0, in.n_mem(p));
+            out.kv.insert(out.kv.end(), in.kv.begin() + p.t0, in.kv.begin() + p.t1);
+            close_item(out);
             continue;
         }
-        if ((int)(cur.members.size() + p.members.size()) * G > kPackRows ||
-            (int)(cur.kv.size() + p.kv.size()) > kPackMaxTiles)
+        if ((int)(sc.cur_mem.size() + in.n_mem(p)) * G > kPackRows ||
+            (int)(sc.cur_kv.size() + in.n_kv(p)) > kPackMaxTiles)
             flush();
-        const int32_t off = (int32_t)cur.members.size();
-        cur.members.insert(cur.members.end(), p.members.begin(), p.members.end());
-        for (KvTile t : p.kv) {
-            const int32_t lo = (t.members & 0xFFFF) + off, hi = (t.members >> 16) + off;
-            t.members = lo | (hi << 16);
-            cur.kv.push_back(t);
+        const int32_t off = (int32_t)sc.cur_mem.size();
+        sc.cur_mem.insert(sc.cur_mem.end(), in.mem.begin() + p.m0, in.mem.begin() + p.m1);
+        for (int32_t t = p.t0; t < p.t1; ++t) {
+            KvTile k = in.kv[t];
+            const int32_t lo = (k.members & 0xFFFF) + off, hi = (k.members >> 16) + off;
+            k.members = lo | (hi << 16);
+            sc.cur_kv.push_back(k);
         }
     }
     flush();
-    protos.swap(out);
 }
 
-void finish(HostPlan &hp, std::vector<ProtoItem> &protos, int32_t G, int32_t nq,
-            int32_t layers_heads, int32_t sms, int32_t mma_ctas, int thr) {
-    pack_small(protos, G, thr);
-    struct Chunked {
-        WorkItem it;
-        int64_t cost;
-        bool tc;
-    };
-    std::vector<Chunked> cs;
-    std::vector<int32_t> cover(nq, 0);
+void finish(HostPlan &hp, Scratch &sc, int32_t G, int32_t nq, int32_t layers_heads, int32_t sms,
+            int32_t mma_ctas, int thr) {
+    pack_small(sc, G, thr);
+    const Protos &pr = sc.packed;
+    auto &cs = sc.cs;
+    cs.clear();
+    sc.cover.assign(nq, 0);
     for (int pass = 0; pass < 2; ++pass) {
         const bool tc = pass == 1;
         int64_t total_tiles = 0, n_protos = 0;
-        for (auto &p : protos) {
-            if (((int)p.members.size() * G > thr) != tc) continue;
-            total_tiles += (int64_t)p.kv.size();
+        for (const auto &p : pr.items) {
+            if ((pr.n_mem(p) * G > thr) != tc) continue;
+            total_tiles += pr.n_kv(p);
             n_protos += 1;
         }
         if (n_protos == 0) continue;
@@ -278,53 +358,60 @@ void finish(HostPlan &hp, std::vector<ProtoItem> &protos, int32_t G, int32_t nq,
             int64_t want = (total_tiles * layers_heads + target_units - 1) / target_units;
             chunk = std::max<int64_t>(4, std::min<int64_t>(chunk, want));
         }
-        for (auto &p : protos) {
-            if (((int)p.members.size() * G > thr) != tc) continue;
+        for (const auto &p : pr.items) {
+            if ((pr.n_mem(p) * G > thr) != tc) continue;
             const int32_t moff = (int32_t)hp.members.size();
-            hp.members.insert(hp.members.end(), p.members.begin(), p.members.end());
-            const int64_t nt = (int64_t)p.kv.size();
+            hp.members.insert(hp.members.end(), pr.mem.begin() + p.m0, pr.mem.begin() + p.m1);
+            const int64_t nt = pr.n_kv(p);
             const int64_t nchunks = std::max<int64_t>(1, (nt + chunk - 1) / chunk);
             const int32_t tbase = (int32_t)hp.tiles.size();
-            hp.tiles.insert(hp.tiles.end(), p.kv.begin(), p.kv.end());
-            const int32_t rows = (int32_t)p.members.size() * G;
+            hp.tiles.insert(hp.tiles.end(), pr.kv.begin() + p.t0, pr.kv.begin() + p.t1);
+            const int32_t nm = pr.n_mem(p), rows = nm * G;
             for (int64_t c = 0; c < nchunks; ++c) {
                 const int64_t b = nt * c / nchunks, e = nt * (c + 1) / nchunks;
                 WorkItem it{};
                 it.tile_begin = tbase + (int32_t)b;
                 it.tile_end = tbase + (int32_t)e;
                 it.member_off = moff;
-                it.n_members = (int32_t)p.members.size();
+                it.n_members = nm;
                 it.out_base = 0;
                 // rows beyond 16 cost tensor and exp work per tile
-                cs.push_back(Chunked{it, (e - b) * (64 + std::max(16, rows)), tc});
-                for (int32_t m : p.members) cover[m] += 1;
+                cs.push_back(Scratch::Chunked{it, (e - b) * (64 + std::max(16, rows)), (int32_t)cs.size(), tc});
+                for (int32_t x = p.m0; x < p.m1; ++x) sc.cover[pr.mem[x]] += 1;
             }
         }
     }
-    // partial rows for every chunk whose members are not all covered once
+    // partial rows for every chunk whose members are not all covered once;
+    // each query's merge entries in chunk order
     int32_t P = 0;
-    std::vector<std::vector<int32_t>> ent(nq);
+    sc.ent_cnt.assign(nq + 1, 0);
     for (auto &c : cs) {
         bool direct = true;
         for (int32_t m = 0; m < c.it.n_members; ++m)
-            if (cover[hp.members[c.it.member_off + m]] != 1) direct = false;
+            if (sc.cover[hp.members[c.it.member_off + m]] != 1) direct = false;
         if (direct) {
             c.it.out_base = -1;
         } else {
             c.it.out_base = P;
-            for (int32_t m = 0; m < c.it.n_members; ++m)
-                ent[hp.members[c.it.member_off + m]].push_back(P + m * G);
+            for (int32_t m = 0; m < c.it.n_members; ++m) sc.ent_cnt[hp.members[c.it.member_off + m] + 1] += 1;
             P += c.it.n_members * G;
         }
     }
-    hp.merge.assign(nq, MergeDesc{0, 0});
-    for (int32_t q = 0; q < nq; ++q) {
-        hp.merge[q] = MergeDesc{(int32_t)hp.entries.size(), (int32_t)ent[q].size()};
-        hp.entries.insert(hp.entries.end(), ent[q].begin(), ent[q].end());
+    for (int32_t q = 0; q < nq; ++q) sc.ent_cnt[q + 1] += sc.ent_cnt[q];
+    hp.entries.resize(sc.ent_cnt[nq]);
+    sc.ent_pos.assign(sc.ent_cnt.begin(), sc.ent_cnt.end() - 1);
+    for (const auto &c : cs) {
+        if (c.it.out_base < 0) continue;
+        for (int32_t m = 0; m < c.it.n_members; ++m)
+            hp.entries[sc.ent_pos[hp.members[c.it.member_off + m]]++] = c.it.out_base + m * G;
     }
-    std::stable_sort(cs.begin(), cs.end(),
-                     [](const Chunked &a, const Chunked &b) { return a.cost > b.cost; });
-    for (auto &c : cs) (c.tc ? hp.tc_items : hp.items).push_back(c.it);
+    hp.merge.resize(nq);
+    for (int32_t q = 0; q < nq; ++q) hp.merge[q] = MergeDesc{sc.ent_cnt[q], sc.ent_cnt[q + 1] - sc.ent_cnt[q]};
+    // longest first; equal costs keep their order
+    std::sort(cs.begin(), cs.end(), [](const Scratch::Chunked &a, const Scratch::Chunked &b) {
+        return a.cost != b.cost ? a.cost > b.cost : a.idx < b.idx;
+    });
+    for (const auto &c : cs) (c.tc ? hp.tc_items : hp.items).push_back(c.it);
     hp.n_partial_rows = P;
     hp.n_units = (int32_t)hp.items.size() * layers_heads;
     hp.n_tc_units = (int32_t)hp.tc_items.size() * layers_heads;
@@ -334,56 +421,73 @@ void finish(HostPlan &hp, std::vector<ProtoItem> &protos, int32_t G, int32_t nq,
 int build_decode(const kvp_attn_desc &d, const int32_t *tables, const int32_t *lens, int32_t S,
                  int32_t MB, int sms, HostPlan &hp) {
     const int32_t bs = d.block_size, G = d.num_q_heads / d.num_kv_heads;
-    Builder b{tables, lens, S, MB, bs, std::vector<int32_t>(S), {}, {}};
+    Scratch &sc = t_scratch;
+    sc.nblk.resize(S);
     for (int32_t s = 0; s < S; ++s) {
         if (lens[s] <= 0) return KVP_ERR_INVALID;
         int64_t nb = ((int64_t)lens[s] + bs - 1) / bs;
         if (nb > MB) return KVP_ERR_INVALID;
-        b.nblk[s] = (int32_t)nb;
+        sc.nblk[s] = (int32_t)nb;
         for (int32_t j = 0; j < nb; ++j) {
             int32_t id = tables[(size_t)s * MB + j];
             if (id < 0 || id >= d.num_blocks) return KVP_ERR_INVALID;
         }
     }
     TileSrc src{tables, MB, bs};
-    std::vector<ProtoItem> protos;
+    Protos &pr = sc.protos;
+    pr.clear();
     const int64_t tok_bytes = 2LL * d.num_kv_heads * d.head_dim * 2 * d.num_layers;
     if (d.use_sharing) {
-        std::vector<int32_t> all(S);
-        std::iota(all.begin(), all.end(), 0);
-        b.build(all, 0);
-        for (auto &sg : b.segs) hp.unique_kv_bytes += (int64_t)(sg.tok1 - sg.tok0) * tok_bytes;
+        sc.order.clear();
+        sc.segs.clear();
+        sc.bounds.clear();
+        sc.members.resize(S);
+        std::iota(sc.members.begin(), sc.members.end(), 0);
+        Builder b{tables, lens, S, MB, bs, sc};
+        b.build(sc.members.data(), S, 0);
+        for (const auto &sg : sc.segs) hp.unique_kv_bytes += (int64_t)(sg.tok1 - sg.tok0) * tok_bytes;
         const int32_t per_tile = members_per_tile(G, tc_usable(d));
         for (int32_t lo = 0; lo < S; lo += per_tile) {
             const int32_t hi = std::min(S, lo + per_tile);
             hp.n_row_tiles += 1;
-            ProtoItem shared;
-            shared.members.assign(b.order.begin() + lo, b.order.begin() + hi);
-            std::vector<ProtoItem> priv(hi - lo);
-            for (int32_t m = lo; m < hi; ++m) priv[m - lo].members.push_back(b.order[m]);
-            for (auto &sg : b.segs) {   // pre-order: a segment precedes its subtree
-                int32_t a = std::max(lo, sg.lo), e = std::min(hi, sg.hi);
+            // the tile's shared item: segments that two or more of its members see
+            open_item(pr, sc.order.data() + lo, hi - lo);
+            sc.priv_seg.clear();
+            for (int32_t i = 0; i < (int32_t)sc.segs.size(); ++i) {   // pre-order: a segment precedes its subtree
+                const Seg &sg = sc.segs[i];
+                const int32_t a = std::max(lo, sg.lo), e = std::min(hi, sg.hi);
                 if (a >= e) continue;
-                if (e - a >= 2)
-                    push_range(shared.kv, src, sg.row, sg.tok0, sg.tok1, a - lo, e - lo, 0);
-                else
-                    push_range(priv[a - lo].kv, src, sg.row, sg.tok0, sg.tok1, 0, 1, 0);
+                if (e - a >= 2) push_range(pr.kv, src, sg.row, sg.tok0, sg.tok1, a - lo, e - lo, 0);
+                else sc.priv_seg.push_back(((a - lo) << 20) | i);   // a member's own segment
             }
-            if (!shared.kv.empty()) protos.push_back(std::move(shared));
-            for (auto &p : priv)
-                if (!p.kv.empty()) protos.push_back(std::move(p));
+            close_item(pr);
+            // one private item per member, its segments in pre-order
+            sc.priv_cnt.assign(hi - lo + 1, 0);
+            for (int32_t x : sc.priv_seg) sc.priv_cnt[(x >> 20) + 1] += 1;
+            for (int32_t m = 0; m < hi - lo; ++m) sc.priv_cnt[m + 1] += sc.priv_cnt[m];
+            sc.tmp.resize(sc.priv_seg.size());
+            sc.gcount.assign(sc.priv_cnt.begin(), sc.priv_cnt.end() - 1);
+            for (int32_t x : sc.priv_seg) sc.tmp[sc.gcount[x >> 20]++] = x & 0xFFFFF;
+            for (int32_t m = 0; m < hi - lo; ++m) {
+                if (sc.priv_cnt[m] == sc.priv_cnt[m + 1]) continue;
+                open_item(pr, sc.order.data() + lo + m, 1);
+                for (int32_t k = sc.priv_cnt[m]; k < sc.priv_cnt[m + 1]; ++k) {
+                    const Seg &sg = sc.segs[sc.tmp[k]];
+                    push_range(pr.kv, src, sg.row, sg.tok0, sg.tok1, 0, 1, 0);
+                }
+                close_item(pr);
+            }
         }
     } else {
         for (int32_t s = 0; s < S; ++s) {
             hp.unique_kv_bytes += (int64_t)lens[s] * tok_bytes;
             hp.n_row_tiles += 1;
-            ProtoItem p;
-            p.members.push_back(s);
-            push_range(p.kv, src, s, 0, lens[s], 0, 1, 0);
-            protos.push_back(std::move(p));
+            open_item(pr, &s, 1);
+            push_range(pr.kv, src, s, 0, lens[s], 0, 1, 0);
+            close_item(pr);
         }
     }
-    finish(hp, protos, G, S, d.num_layers * d.num_kv_heads, sms, attention_ctas_per_sm(d.head_dim),
+    finish(hp, sc, G, S, d.num_layers * d.num_kv_heads, sms, attention_ctas_per_sm(d.head_dim),
            tc_usable(d) ? tc_row_threshold(d.head_dim) : INT32_MAX);
     return KVP_OK;
 }
@@ -394,7 +498,9 @@ int build_verify(const kvp_attn_desc &d, const int32_t *tables, const int32_t *c
     if (n <= 0 || n > kMaxDraft) return KVP_ERR_INVALID;
     const int64_t tok_bytes = 2LL * d.num_kv_heads * d.head_dim * 2 * d.num_layers;
     TileSrc src{tables, MB, bs};
-    std::vector<ProtoItem> protos;
+    Scratch &sc = t_scratch;
+    Protos &pr = sc.protos;
+    pr.clear();
     const int32_t per_tile = members_per_tile(G, tc_usable(d));
     for (int32_t b = 0; b < B; ++b) {
         if (ctx[b] < 0) return KVP_ERR_INVALID;
@@ -408,15 +514,16 @@ int build_verify(const kvp_attn_desc &d, const int32_t *tables, const int32_t *c
         for (int32_t i0 = 0; i0 < n; i0 += per_tile) {
             int32_t i1 = std::min(n, i0 + per_tile);
             hp.n_row_tiles += 1;
-            ProtoItem p;
-            for (int32_t i = i0; i < i1; ++i) p.members.push_back(b * n + i);
-            push_range(p.kv, src, b, 0, ctx[b], 0, i1 - i0, 0);
+            sc.members.clear();
+            for (int32_t i = i0; i < i1; ++i) sc.members.push_back(b * n + i);
+            open_item(pr, sc.members.data(), i1 - i0);
+            push_range(pr.kv, src, b, 0, ctx[b], 0, i1 - i0, 0);
             // draft tokens 0 .. i1-1 (ancestors have smaller indices), tree-masked
-            push_range(p.kv, src, b, ctx[b], ctx[b] + i1, 0, i1 - i0, kTileTree);
-            protos.push_back(std::move(p));
+            push_range(pr.kv, src, b, ctx[b], ctx[b] + i1, 0, i1 - i0, kTileTree);
+            close_item(pr);
         }
     }
-    finish(hp, protos, G, B * n, d.num_layers * d.num_kv_heads, sms, attention_ctas_per_sm(d.head_dim),
+    finish(hp, sc, G, B * n, d.num_layers * d.num_kv_heads, sms, attention_ctas_per_sm(d.head_dim),
            tc_usable(d) ? tc_row_threshold(d.head_dim) : INT32_MAX);
     hp.n_tree_q = B * n;
     return KVP_OK;
@@ -600,7 +707,8 @@ extern "C" {
 size_t kvp_decode_workspace_size(const kvp_attn_desc *desc, const int32_t *block_tables,
                                  const int32_t *seq_lens, int32_t num_seqs, int32_t max_blocks) {
     if (!desc_ok(desc) || num_seqs <= 0 || max_blocks <= 0 || !block_tables || !seq_lens) return 0;
-    HostPlan hp;
+    HostPlan &hp = t_plan;
+    hp.clear();
     if (build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, device_sm_count(), hp))
         return 0;
     return layout(hp, *desc).total;
@@ -613,7 +721,8 @@ int paged_decode_attention(const void *q, const void *k_pool, const void *v_pool
     if (!desc_ok(desc) || desc->kv_format != KVP_KV_BF16 || num_seqs <= 0 || max_blocks <= 0 ||
         !block_tables || !seq_lens)
         return KVP_ERR_INVALID;
-    HostPlan hp;
+    HostPlan &hp = t_plan;
+    hp.clear();
     int rc = build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, device_sm_count(), hp);
     if (rc) return rc;
     return run(hp, *desc, q, k_pool, v_pool, num_seqs, nullptr, 0, out, lse, workspace, ws_bytes,
@@ -628,7 +737,8 @@ int paged_decode_attention_kv4(const void *q, const void *k_codes, const void *k
     if (!desc_ok(desc) || desc->kv_format != KVP_KV_4BIT || num_seqs <= 0 || max_blocks <= 0 ||
         !block_tables || !seq_lens)
         return KVP_ERR_INVALID;
-    HostPlan hp;
+    HostPlan &hp = t_plan;
+    hp.clear();
     int rc = build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, device_sm_count(), hp);
     if (rc) return rc;
     return run(hp, *desc, q, k_codes, v_codes, num_seqs, nullptr, 0, out, lse, workspace, ws_bytes,
@@ -638,7 +748,8 @@ int paged_decode_attention_kv4(const void *q, const void *k_codes, const void *k
 size_t kvp_pool_decode_workspace_size(const kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs,
                                       const kvp_attn_desc *desc) {
     if (!pool || !desc_ok(desc) || !desc_matches_pool(*desc, pool_view(pool))) return 0;
-    HostPlan hp;
+    HostPlan &hp = t_plan;
+    hp.clear();
     if (plan_pool(pool, seq_ids, num_seqs, *desc, hp)) return 0;
     return layout(hp, *desc).total;
 }
@@ -649,7 +760,8 @@ int paged_decode_attention_pool(const kvp_pool *pool, const int32_t *seq_ids, in
     if (!pool || !desc_ok(desc)) return KVP_ERR_INVALID;
     const PoolView pv = pool_view(pool);
     if (!desc_matches_pool(*desc, pv)) return KVP_ERR_INVALID;
-    HostPlan hp;
+    HostPlan &hp = t_plan;
+    hp.clear();
     int rc = plan_pool(pool, seq_ids, num_seqs, *desc, hp);
     if (rc) return rc;
     return run_pool(hp, *desc, pv, q, num_seqs, out, lse, workspace, ws_bytes, (cudaStream_t)stream);
@@ -713,7 +825,8 @@ int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, in
         int rc = append_batch_commit(pool, num_seqs, seq_ids, t_ntoks.data(), k_new, v_new, &staged.total);
         if (rc) return rc;
     }
-    HostPlan hp;
+    HostPlan &hp = t_plan;
+    hp.clear();
     int rc = plan_pool(pool, seq_ids, num_seqs, *desc, hp);
     if (rc == KVP_OK) {
         const size_t need = layout(hp, *desc).total;
@@ -738,7 +851,8 @@ size_t kvp_verify_workspace_size(const kvp_attn_desc *desc, const int32_t *block
                                  const int32_t *ctx_lens, int32_t batch, int32_t n_draft,
                                  int32_t max_blocks) {
     if (!desc_ok(desc) || batch <= 0 || !ctx_lens || !block_tables || max_blocks <= 0) return 0;
-    HostPlan hp;
+    HostPlan &hp = t_plan;
+    hp.clear();
     if (build_verify(*desc, block_tables, ctx_lens, batch, n_draft, max_blocks, device_sm_count(), hp))
         return 0;
     return layout(hp, *desc).total;
@@ -752,7 +866,8 @@ int tree_verify_attention(const void *q, const int32_t *tree_parent, int32_t n_d
     if (!desc_ok(desc) || desc->kv_format != KVP_KV_BF16 || batch <= 0 || max_blocks <= 0 || !ctx_lens ||
         !block_tables || !tree_parent)
         return KVP_ERR_INVALID;
-    HostPlan hp;
+    HostPlan &hp = t_plan;
+    hp.clear();
     int rc = build_verify(*desc, block_tables, ctx_lens, batch, n_draft, max_blocks, device_sm_count(), hp);
     if (rc) return rc;
     return run(hp, *desc, q, k_pool, v_pool, batch * n_draft, tree_parent, n_draft, out, lse,
@@ -778,7 +893,8 @@ int kvp_decode_plan_stats(const kvp_attn_desc *desc, const int32_t *block_tables
     if (!desc_ok(desc) || num_seqs <= 0 || max_blocks <= 0 || !block_tables || !seq_lens ||
         sm_count <= 0)
         return KVP_ERR_INVALID;
-    HostPlan hp;
+    HostPlan &hp = t_plan;
+    hp.clear();
     int rc = build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, sm_count, hp);
     if (rc) return rc;
     if (n_items) *n_items = (int32_t)(hp.items.size() + hp.tc_items.size());
