@@ -729,11 +729,13 @@ def memory_report(kvp, r, w, seqs, MB):
     unique = len(set(np.concatenate(rows).tolist()))
     private = sum(nblk)
     block_bytes = s.L * s.Hkv * s.bs * s.d * 2 * 2
-    return {"blocks_shared": unique, "blocks_unshared": private, "block_bytes": block_bytes,
-            "kv_bytes_shared": unique * block_bytes, "kv_bytes_unshared": private * block_bytes,
-            "saved_frac": 1.0 - unique / private,
-            "pages_context": "Dendrite: 1.1 GB vs 6 GB for a 4K prefix x 6 branches (>80% saved; model and "
-                             "precision unstated)"}
+    res = {"blocks_shared": unique, "blocks_unshared": private, "block_bytes": block_bytes,
+           "kv_bytes_shared": unique * block_bytes, "kv_bytes_unshared": private * block_bytes,
+           "saved_frac": 1.0 - unique / private}
+    if w.name == "dendrite":
+        res["pages_context"] = "Dendrite: 1.1 GB vs 6 GB for a 4K prefix x 6 branches (>80% saved; model and " \
+                               "precision unstated)"
+    return res
 
 
 # ------------------------------------------------- verify cost table (CAST)
