@@ -207,11 +207,10 @@ struct KCfg4 {
     static constexpr int NSTAGE = 3;
     static constexpr int STAGE_BYTES = 2 * CODE_BYTES + 2 * kTileTokens;   // codes K, V; exponents K, V
     static constexpr int BF_OFF = NSTAGE * STAGE_BYTES;    // bf16 K then V tile (the mma layout)
-    static constexpr int LUT_OFF = BF_OFF + 2 * KCfg<D>::TILE_BYTES;   // byte -> bf16x2 of its two codes
-    static constexpr int DESC_OFF = LUT_OFF + 256 * 4;
+    static constexpr int DESC_OFF = BF_OFF + 2 * KCfg<D>::TILE_BYTES;
     static constexpr int SMEM = DESC_OFF + kMaxItemTiles * (int)sizeof(KvTile);
     // the token-split combine overlays the staging ring and bf16 tile
-    static_assert(4 * (KCfg<D>::NO * 4 + 4) * 32 * 4 <= LUT_OFF, "combine area");
+    static_assert(4 * (KCfg<D>::NO * 4 + 4) * 32 * 4 <= DESC_OFF, "combine area");
 };
 
 // One work unit with TS warps splitting each tile's tokens.  KV4: the pool
@@ -306,29 +305,34 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
     // expands the staged tile t into the bf16 tile: value = code * 2^e, by a
     // table of each byte's two codes as bf16 pairs and an exact multiply by
     // the power of two
+    // expands the staged tile t into the bf16 tile: value = code * 2^e,
+    // formed exactly in registers (each thread: one 16-byte chunk of codes,
+    // 32 dims of one row, into four 16-byte chunks of the bf16 tile)
     auto expand4 = [&](int t) {
         const unsigned char *stg = smem + (t % NSTAGE) * C4::STAGE_BYTES;
-        const uint32_t *lut = reinterpret_cast<const uint32_t *>(smem + C4::LUT_OFF);
-        for (int x = threadIdx.x; x < 2 * kTileTokens * C::CH; x += kThreads) {
-            const int kv = x / (kTileTokens * C::CH);
-            const int y = x % (kTileTokens * C::CH);
-            const int tok = y / C::CH, ch = y % C::CH;     // 8 values: codes bytes 4 ch .. 4 ch + 3
-            const int cs = ((ch >> 2) ^ ((tok >> C4::SWS) & (C4::CH4 - 1))) * 16 + (ch & 3) * 4;
-            const uint32_t cw = *reinterpret_cast<const uint32_t *>(stg + kv * C4::CODE_BYTES + tok * (D / 2) + cs);
+        for (int x = threadIdx.x; x < 2 * kTileTokens * C4::CH4; x += kThreads) {
+            const int kv = x / (kTileTokens * C4::CH4);
+            const int y = x % (kTileTokens * C4::CH4);
+            const int tok = y / C4::CH4, q = y % C4::CH4;   // code chunk q: dims 32 q .. 32 q + 31
+            const uint4 cw = *reinterpret_cast<const uint4 *>(
+                stg + kv * C4::CODE_BYTES + tok * (D / 2) + ((q ^ ((tok >> C4::SWS) & (C4::CH4 - 1))) << 4));
             const int e = (int)reinterpret_cast<const int8_t *>(stg + 2 * C4::CODE_BYTES + kv * kTileTokens)[tok];
-            // 2^e as bf16 (e >= -126: a normal number; -127: the subnormal 2^-127)
-            const uint32_t sb = e >= -126 ? (uint32_t)(e + 127) << 7 : 0x40u;
-            const uint32_t sb2 = sb | (sb << 16);
-            const __nv_bfloat162 sc2 = *reinterpret_cast<const __nv_bfloat162 *>(&sb2);
-            uint4 v;
-            uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
+            const bool fused = e >= -126 && e <= 120;
+            const uint2 sc = exp_pair2(e, e);
+            const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const uint32_t pair = lut[(cw >> (8 * b)) & 0xFFu];
-                const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&pair), sc2);
-                vv[b] = *reinterpret_cast<const uint32_t *>(&r);
+            for (int k = 0; k < 4; ++k) {   // word k: dims 32 q + 8 k .. + 7, byte b = dims 2b (low), 2b + 1
+                const uint32_t lo = w[k] & 0x0F0F0F0Fu, hi = (w[k] >> 4) & 0x0F0F0F0Fu;
+                uint4 v;
+                uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const uint32_t pr = __byte_perm(lo, hi, b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12));
+                    vv[b] = conv_pair((pr & 0x000F000Fu) ^ 0x43084308u, sc, fused);
+                }
+                const int c = 4 * q + k;
+                *reinterpret_cast<uint4 *>(smem + C4::BF_OFF + kv * C::TILE_BYTES + tok * D * 2 + ((c ^ (tok & 7)) << 4)) = v;
             }
-            *reinterpret_cast<uint4 *>(smem + C4::BF_OFF + kv * C::TILE_BYTES + tok * D * 2 + ((ch ^ (tok & 7)) << 4)) = v;
         }
     };
 
@@ -753,14 +757,6 @@ __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kerne
     extern __shared__ __align__(128) unsigned char smem[];
     KvTile *s_tiles = reinterpret_cast<KvTile *>(smem + (KV4 ? KCfg4<D>::DESC_OFF : C::DESC_OFF));
     __shared__ int s_unit;
-    if constexpr (KV4) {
-        // byte -> its two signed 4-bit codes (low nibble first) as bf16
-        uint32_t *lut = reinterpret_cast<uint32_t *>(smem + KCfg4<D>::LUT_OFF);
-        for (int b = threadIdx.x; b < 256; b += kThreads) {
-            const int lo = (b & 7) - (b & 8), hi = ((b >> 4) & 7) - ((b >> 4) & 8);
-            lut[b] = pack_bf16x2((float)lo, (float)hi);
-        }
-    }
     // the plan (work items, tile descriptors, counters) was uploaded before
     // the kernel that may still be running; K/V, q and the tree masks are
     // read only after it has completed
