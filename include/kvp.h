@@ -398,7 +398,11 @@ int paged_decode_attention_pool(const kvp_pool *pool, const int32_t *seq_ids, in
  *   1. host-to-device copies h_k_new -> d_k_new, h_v_new -> d_v_new and
  *      h_q -> d_q (each skipped when its host pointer is NULL: the data is
  *      already on the device);
- *   2. seq_append_batch of ntok tokens to every sequence (skipped for ntok 0);
+ *   2. seq_append_batch of ntok tokens to every sequence (skipped for ntok 0):
+ *      its bookkeeping and the plan of step 3 are done on the host first, and
+ *      its write kernel is enqueued right before the attention kernels, which
+ *      are launched programmatically behind it (they start while it
+ *      finishes and wait for it before reading K/V);
  *   3. paged_decode_attention_pool over the sequences at their new lengths,
  *      d_q -> d_out, d_lse;
  *   4. device-to-host copies d_out -> h_out and d_lse -> h_lse (each skipped
@@ -420,11 +424,12 @@ int paged_decode_attention_pool(const kvp_pool *pool, const int32_t *seq_ids, in
  * NULL, then h_lse must be NULL too).  seq_ids: host, distinct live
  * sequences.  *ws_needed (may be NULL) receives the workspace bytes the
  * attention needed.
- * Errors: KVP_ERR_INVALID (bad arguments, descriptor not matching the pool)
- * and KVP_ERR_OOM (the appends do not fit) before anything is enqueued;
- * KVP_ERR_WORKSPACE when ws_bytes < *ws_needed: the copies and the append of
- * step 1-2 are enqueued and the pool holds the new tokens, nothing else ran;
- * grow the workspace and finish the step with paged_decode_attention_pool.
+ * Errors: KVP_ERR_INVALID (bad arguments, descriptor not matching the pool,
+ * unknown flags, misaligned mapped buffers) and KVP_ERR_OOM (the appends do
+ * not fit) before anything is enqueued; KVP_ERR_WORKSPACE when ws_bytes <
+ * *ws_needed: the copies and the append of steps 1-2 are enqueued and the
+ * pool holds the new tokens, nothing else ran; grow the workspace and finish
+ * the step with paged_decode_attention_pool.
  */
 typedef struct {
     const void *h_k_new, *h_v_new, *h_q; /* host inputs, or NULL */
