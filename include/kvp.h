@@ -447,6 +447,42 @@ int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, in
                     const kvp_step_io *io, const kvp_attn_desc *desc, void *workspace,
                     size_t ws_bytes, size_t *ws_needed, void *stream);
 
+/*
+ * kvp_decode_step in two halves, so that the host work of step i + 1 can run
+ * while the device runs step i (each sequence appending ntok tokens per step
+ * is known before the step's K/V and q are):
+ *
+ *   kvp_decode_step_plan: the checks of kvp_decode_step that involve the pool,
+ *     then the append's bookkeeping (the sequences grow by ntok tokens at once:
+ *     slots and copy-on-write copies are assigned) and the attention plan over
+ *     the grown sequences, packed into `plan`.  No device work.  *ws_needed
+ *     (may be NULL) receives the workspace bytes the run will need.
+ *   kvp_decode_step_run: steps 1-4 of kvp_decode_step for that plan, with the
+ *     plan's upload into `workspace` right before the append's write.
+ *
+ * A plan object (kvp_step_plan_create; kvp_step_plan_destroy frees it) holds
+ * one planned step at a time and is reused from step to step.  Planning a
+ * plan that is still waiting for its run is KVP_ERR_INVALID, since its
+ * tokens are already in the sequences.  Between plan and run no call may
+ * change the planned sequences or free blocks; appends and attention on other
+ * sequences may run.  `workspace` belongs to the run until the stream passes
+ * its kernels, as for every attention call.  The run takes its device
+ * buffers from io as kvp_decode_step does (num_seqs and ntok are the plan's).
+ * Errors: the plan call as kvp_decode_step's (KVP_ERR_INVALID, KVP_ERR_OOM;
+ * nothing changed); the run returns KVP_ERR_INVALID for a plan that is not
+ * waiting for its run or bad buffers (the plan then stays ready), and
+ * KVP_ERR_WORKSPACE when ws_bytes is short: the inputs' copies and the
+ * append's write are enqueued, nothing else; the plan is used up.
+ */
+typedef struct kvp_step_plan kvp_step_plan;
+
+kvp_step_plan *kvp_step_plan_create(void);
+void kvp_step_plan_destroy(kvp_step_plan *plan);
+int kvp_decode_step_plan(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, int32_t ntok,
+                         const kvp_attn_desc *desc, kvp_step_plan *plan, size_t *ws_needed);
+int kvp_decode_step_run(kvp_step_plan *plan, const kvp_step_io *io, void *workspace, size_t ws_bytes,
+                        void *stream);
+
 /* Reads (and clears) the device error word that the last attention call on
  * this workspace left; synchronises `stream`.  *err_out = 0 when clean. */
 int kvp_device_error(void *workspace, void *stream, int32_t *err_out);

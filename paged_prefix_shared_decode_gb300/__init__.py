@@ -25,7 +25,8 @@ __all__ = [
     "kvp_set_kernel_events", "kvp_kernel_launches", "paged_decode_attention_noalloc",
     "paged_decode_attention_kv4", "KVP_KV_BF16", "KVP_KV_4BIT",
     "kvp_pool_decode_workspace_size", "paged_decode_attention_pool", "StepIO", "step_io", "kvp_decode_step",
-    "DecodeStep", "KVP_STEP_HOST_MAPPED",
+    "DecodeStep", "KVP_STEP_HOST_MAPPED", "kvp_step_plan_create", "kvp_step_plan_destroy",
+    "kvp_decode_step_plan", "kvp_decode_step_run", "StepPlan",
     "KVP_STATIC_WORKSPACE_BYTES",
     "KVP_OK", "KVP_ERR_INVALID", "KVP_ERR_OOM", "KVP_ERR_STATE", "KVP_ERR_CUDA", "KVP_ERR_DEVICE",
     "KVP_ERR_WORKSPACE",
@@ -124,6 +125,11 @@ _SIGS = {
                                      _P], ctypes.c_int),
     "kvp_decode_step": ([_P, _P, _I32, _I32, ctypes.POINTER(StepIO), ctypes.POINTER(AttnDesc), _P,
                          ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t), _P], ctypes.c_int),
+    "kvp_step_plan_create": ([], _P),
+    "kvp_step_plan_destroy": ([_P], None),
+    "kvp_decode_step_plan": ([_P, _P, _I32, _I32, ctypes.POINTER(AttnDesc), _P, ctypes.POINTER(ctypes.c_size_t)],
+                             ctypes.c_int),
+    "kvp_decode_step_run": ([_P, ctypes.POINTER(StepIO), _P, ctypes.c_size_t, _P], ctypes.c_int),
     "seq_alloc_prefix": ([_P, _P, _I32, _I32P], ctypes.c_int),
     "seq_accept_draft": ([_P, _I32, _I32, _P, _I32, _I32, _P, _I32P, _P], ctypes.c_int),
     "kvp_radix_create": ([_P, ctypes.POINTER(_P)], ctypes.c_int),
@@ -447,6 +453,75 @@ class DecodeStep:
             e.ws_needed = self.ws_needed.value
             raise e
         return self.ws_needed.value
+
+
+def kvp_step_plan_create():
+    h = load().kvp_step_plan_create()
+    if not h:
+        raise KvpError(KVP_ERR_OOM, "kvp_step_plan_create")
+    return h
+
+
+def kvp_step_plan_destroy(plan) -> None:
+    load().kvp_step_plan_destroy(plan)
+
+
+def kvp_decode_step_plan(pool, seq_ids, ntok: int, desc: AttnDesc, plan) -> int:
+    """Host half of a decode step (the append's bookkeeping and the attention
+    plan over the grown sequences) into `plan`; returns the workspace bytes
+    its run needs."""
+    s, sp = _host_i32(seq_ids)
+    need = ctypes.c_size_t(0)
+    _check(load().kvp_decode_step_plan(pool, sp, len(s), ntok, ctypes.byref(desc), plan, ctypes.byref(need)),
+           "kvp_decode_step_plan")
+    return need.value
+
+
+def kvp_decode_step_run(plan, io: StepIO, workspace, ws_bytes=None, stream=None) -> None:
+    """Device half of a planned decode step on `stream`."""
+    _check(load().kvp_decode_step_run(plan, ctypes.byref(io), _dev(workspace), _ws_bytes(workspace, ws_bytes),
+                                      _stream(stream)), "kvp_decode_step_run")
+
+
+class StepPlan:
+    """kvp_decode_step_plan / kvp_decode_step_run on one plan object with
+    their arguments marshalled once: plan() is the host half of the next
+    step, run() its device half.  A loop can plan step i + 1 right after
+    running step i, while the device works.  Keep `io`'s tensors alive while
+    it is in use; close() frees the plan object."""
+
+    def __init__(self, pool, seq_ids, ntok: int, io: StepIO, desc: AttnDesc, workspace, ws_bytes=None,
+                 stream=None):
+        lib = load()
+        self._seqs = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        self._io, self._desc = io, desc
+        self._h = kvp_step_plan_create()
+        self.ws_needed = ctypes.c_size_t(0)
+        self._plan, self._run, self._destroy = lib.kvp_decode_step_plan, lib.kvp_decode_step_run, \
+            lib.kvp_step_plan_destroy
+        h = ctypes.c_void_p(self._h)
+        self._pargs = (ctypes.c_void_p(pool), ctypes.c_void_p(self._seqs.ctypes.data), _I32(len(self._seqs)),
+                       _I32(ntok), ctypes.byref(desc), h, ctypes.byref(self.ws_needed))
+        self._rargs = (h, ctypes.byref(io), ctypes.c_void_p(_dev(workspace)),
+                       ctypes.c_size_t(_ws_bytes(workspace, ws_bytes)), ctypes.c_void_p(_stream(stream)))
+
+    def plan(self) -> int:
+        _check(self._plan(*self._pargs), "kvp_decode_step_plan")
+        return self.ws_needed.value
+
+    def run(self) -> None:
+        _check(self._run(*self._rargs), "kvp_decode_step_run")
+
+    def close(self) -> None:
+        if self._h:
+            self._destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def kvp_verify_workspace_size(desc: AttnDesc, block_tables, ctx_lens, n_draft: int) -> int:

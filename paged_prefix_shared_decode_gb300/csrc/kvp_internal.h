@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -122,12 +123,20 @@ bool pool_drop_block(kvp_pool *p, int32_t b);
 int append_batch_check(kvp_pool *p, int32_t nseq, const int32_t *seqs, const int32_t *ntoks,
                        int64_t *total_out = nullptr);
 
-// seq_append_batch in two halves: the checks and the bookkeeping (the slots
-// and copy-on-write triples stay staged in the pool), then the device write
-// of the staged append.  Nothing else may touch the pool in between.
+// seq_append_batch's checks and bookkeeping, the slots and copy-on-write
+// triples staged in the pool for its device write.
 int append_batch_commit(kvp_pool *p, int32_t nseq, const int32_t *seqs, const int32_t *ntoks, const void *k,
                         const void *v, int32_t *total_out);
-int append_issue(kvp_pool *p, const void *k, const void *v, int32_t total, void *stream);
+
+// seq_append_batch in two halves: the checks and the bookkeeping, whose
+// token slots and copy-on-write triples go to the caller's lists (the
+// sequences grow at once), then the device write of those lists, with the
+// new tokens' K/V [L][slots.size()][Hkv][d].  No call that frees or
+// reallocates the lists' blocks may come in between.
+int append_batch_commit_lists(kvp_pool *p, int32_t nseq, const int32_t *seqs, const int32_t *ntoks,
+                              std::vector<int32_t> &slots, std::vector<int32_t> &cow, int32_t *total_out);
+int append_issue_lists(kvp_pool *p, const std::vector<int32_t> &slots, const std::vector<int32_t> &cow,
+                       const void *k, const void *v, void *stream);
 
 // A pool's shape and device storage (codes and exponents for 4-bit pages).
 struct PoolView {

@@ -573,38 +573,21 @@ WsLayout layout(const HostPlan &hp, const kvp_attn_desc &d) {
     return w;
 }
 
-// Host image of the plan region, reused across calls on the same thread.
-// It is pageable on purpose: a small pageable copy travels with the copy
-// command itself, which measured faster than a copy from page-locked memory.
-thread_local std::vector<unsigned char> t_image;
-thread_local cudaEvent_t t_ev_before = nullptr, t_ev_after = nullptr;
-std::atomic<long long> g_launches{0};
-
-// An append whose bookkeeping is done and whose device write is issued
-// between the plan upload and the attention launch, so that the attention
-// kernel follows the write kernel directly in the stream (and may start
-// while it finishes).
-struct StagedAppend {
-    kvp_pool *pool;
-    const void *k, *v;
-    int32_t total;
+// A plan packed for upload: the host image of the workspace's plan region
+// and what the launch takes from the plan.  The image is pageable on
+// purpose: a small pageable copy travels with the copy command itself, which
+// measured faster than a copy from page-locked memory.
+struct Packed {
+    std::vector<unsigned char> image;
+    WsLayout w{};
+    int32_t n_units = 0, n_tc_units = 0, n_partial_rows = 0;
 };
 
-int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k_pool,
-        const void *v_pool, int32_t nq, const int32_t *parent, int32_t n_draft, void *out,
-        float *lse, void *ws, size_t ws_bytes, cudaStream_t stream, const void *k_exp = nullptr,
-        const void *v_exp = nullptr, const StagedAppend *append = nullptr) {
-    if (!q || !k_pool || !v_pool || !out || !ws) return KVP_ERR_INVALID;
-    const bool kv4 = d.kv_format == KVP_KV_4BIT;
-    if (kv4 && (!k_exp || !v_exp || (((uintptr_t)k_exp | (uintptr_t)v_exp) & 15))) return KVP_ERR_INVALID;
-    if (((uintptr_t)ws & 255) != 0) return KVP_ERR_INVALID;
-    if (((uintptr_t)q | (uintptr_t)k_pool | (uintptr_t)v_pool | (uintptr_t)out) & 15)
-        return KVP_ERR_INVALID;
-    if ((uintptr_t)lse & 3) return KVP_ERR_INVALID;
-    WsLayout w = layout(hp, d);
-    if (ws_bytes < w.total) return KVP_ERR_INVALID;
-    t_image.assign(w.plan_bytes, 0);
-    unsigned char *img = t_image.data();
+void pack(const HostPlan &hp, const kvp_attn_desc &d, Packed &pk) {
+    pk.w = layout(hp, d);
+    const WsLayout &w = pk.w;
+    pk.image.assign(w.plan_bytes, 0);
+    unsigned char *img = pk.image.data();
     WsHeader h{};
     h.n_items = (int32_t)hp.items.size();
     h.n_tc_items = (int32_t)hp.tc_items.size();
@@ -620,11 +603,45 @@ int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k
     std::memcpy(img + w.members, hp.members.data(), sizeof(int32_t) * hp.members.size());
     std::memcpy(img + w.merge, hp.merge.data(), sizeof(MergeDesc) * hp.merge.size());
     std::memcpy(img + w.entries, hp.entries.data(), sizeof(int32_t) * hp.entries.size());
+    pk.n_units = hp.n_units;
+    pk.n_tc_units = hp.n_tc_units;
+    pk.n_partial_rows = hp.n_partial_rows;
+}
+
+thread_local Packed t_packed;
+thread_local cudaEvent_t t_ev_before = nullptr, t_ev_after = nullptr;
+std::atomic<long long> g_launches{0};
+
+// An append whose bookkeeping is done and whose device write is issued
+// between the plan upload and the attention launch, so that the attention
+// kernel follows the write kernel directly in the stream (and may start
+// while it finishes).
+struct StagedAppend {
+    kvp_pool *pool;
+    const std::vector<int32_t> *slots, *cow;
+    const void *k, *v;
+};
+
+// Uploads a packed plan into the workspace, issues a staged append, and
+// launches the attention kernels (and the merge).
+int launch_packed(const Packed &pk, const kvp_attn_desc &d, const void *q, const void *k_pool,
+                  const void *v_pool, int32_t nq, const int32_t *parent, int32_t n_draft, void *out,
+                  float *lse, void *ws, size_t ws_bytes, cudaStream_t stream, const void *k_exp = nullptr,
+                  const void *v_exp = nullptr, const StagedAppend *append = nullptr) {
+    if (!q || !k_pool || !v_pool || !out || !ws) return KVP_ERR_INVALID;
+    const bool kv4 = d.kv_format == KVP_KV_4BIT;
+    if (kv4 && (!k_exp || !v_exp || (((uintptr_t)k_exp | (uintptr_t)v_exp) & 15))) return KVP_ERR_INVALID;
+    if (((uintptr_t)ws & 255) != 0) return KVP_ERR_INVALID;
+    if (((uintptr_t)q | (uintptr_t)k_pool | (uintptr_t)v_pool | (uintptr_t)out) & 15)
+        return KVP_ERR_INVALID;
+    if ((uintptr_t)lse & 3) return KVP_ERR_INVALID;
+    const WsLayout &w = pk.w;
+    if (ws_bytes < w.total) return KVP_ERR_INVALID;
     // pageable source: the copy is staged before the call returns
-    if (cudaMemcpyAsync(ws, img, w.plan_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    if (cudaMemcpyAsync(ws, pk.image.data(), w.plan_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return KVP_ERR_CUDA;
     if (append) {
-        const int rc = append_issue(append->pool, append->k, append->v, append->total, stream);
+        const int rc = append_issue_lists(append->pool, *append->slots, *append->cow, append->k, append->v, stream);
         if (rc) return rc;
     }
     unsigned char *base = (unsigned char *)ws;
@@ -650,11 +667,20 @@ int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k
     a.part_o = (float *)(base + w.part_o);
     a.part_lse = (float *)(base + w.part_lse);
     a.tree_mask = parent ? (uint64_t *)(base + w.tree_mask) : nullptr;
-    a.n_units = hp.n_units;
-    a.n_tc_units = hp.n_tc_units;
-    a.n_merge_q = hp.n_partial_rows > 0 ? nq : 0;
-    a.P = hp.n_partial_rows;
+    a.n_units = pk.n_units;
+    a.n_tc_units = pk.n_tc_units;
+    a.n_merge_q = pk.n_partial_rows > 0 ? nq : 0;
+    a.P = pk.n_partial_rows;
     return launch_attention(a, stream, t_ev_before, t_ev_after) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k_pool,
+        const void *v_pool, int32_t nq, const int32_t *parent, int32_t n_draft, void *out,
+        float *lse, void *ws, size_t ws_bytes, cudaStream_t stream, const void *k_exp = nullptr,
+        const void *v_exp = nullptr) {
+    pack(hp, d, t_packed);
+    return launch_packed(t_packed, d, q, k_pool, v_pool, nq, parent, n_draft, out, lse, ws, ws_bytes, stream,
+                         k_exp, v_exp);
 }
 
 bool desc_matches_pool(const kvp_attn_desc &d, const PoolView &pv) {
@@ -673,10 +699,9 @@ int plan_pool(const kvp_pool *pool, const int32_t *seqs, int32_t n, const kvp_at
 }
 
 int run_pool(const HostPlan &hp, const kvp_attn_desc &d, const PoolView &pv, const void *q, int32_t n,
-             void *out, float *lse, void *ws, size_t ws_bytes, cudaStream_t stream,
-             const StagedAppend *append = nullptr) {
+             void *out, float *lse, void *ws, size_t ws_bytes, cudaStream_t stream) {
     return run(hp, d, q, pv.k, pv.v, n, nullptr, 0, out, lse, ws, ws_bytes, stream,
-               pv.kv4 ? pv.k_exp : nullptr, pv.kv4 ? pv.v_exp : nullptr, append);
+               pv.kv4 ? pv.k_exp : nullptr, pv.kv4 ? pv.v_exp : nullptr);
 }
 
 }  // namespace
@@ -770,84 +795,186 @@ int paged_decode_attention_pool(const kvp_pool *pool, const int32_t *seq_ids, in
     return run_pool(hp, *desc, pv, q, num_seqs, out, lse, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
-int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, int32_t ntok,
-                    const kvp_step_io *io, const kvp_attn_desc *desc, void *workspace,
-                    size_t ws_bytes, size_t *ws_needed, void *stream) {
-    if (!pool || !io || !desc_ok(desc) || num_seqs <= 0 || !seq_ids || ntok < 0 || !workspace)
-        return KVP_ERR_INVALID;
-    const PoolView pv = pool_view(pool);
-    if (!desc_matches_pool(*desc, pv)) return KVP_ERR_INVALID;
-    if (io->flags & ~(uint32_t)KVP_STEP_HOST_MAPPED) return KVP_ERR_INVALID;
-    if ((int64_t)num_seqs * ntok > INT32_MAX / 2) return KVP_ERR_INVALID;
-    // Inputs go to the device buffers (copy-engine transfers, or one copy
-    // kernel over all of them from mapped host memory); mapped host outputs
-    // are written straight by the attention kernels.
+}  // extern "C"
+
+// A decode step planned ahead of its launch: the append's bookkeeping is
+// done (the sequences hold the new tokens), its device write is staged as
+// slot and copy-on-write lists, and the attention plan over the grown
+// sequences is packed for upload.
+struct kvp_step_plan {
+    kvp_pool *pool = nullptr;
+    kvp_attn_desc desc{};
+    int32_t num_seqs = 0, ntok = 0;
+    bool ready = false;                // planned and not yet run
+    std::vector<int32_t> slots, cow;   // the append's device write
+    Packed pk;
+};
+
+namespace {
+
+bool a16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+struct StepBytes {
+    size_t kv, q, lse;
+};
+StepBytes step_bytes(const kvp_attn_desc &d, int32_t num_seqs, int32_t ntok) {
+    const size_t rows = (size_t)d.num_layers * num_seqs * d.num_q_heads;
+    return StepBytes{(size_t)d.num_layers * num_seqs * ntok * d.num_kv_heads * d.head_dim * 2,
+                     rows * d.head_dim * 2, rows * sizeof(float)};
+}
+
+// Everything about a step's buffers that the launch would reject.
+int check_io(const kvp_step_io *io, int32_t ntok) {
+    if (!io || (io->flags & ~(uint32_t)KVP_STEP_HOST_MAPPED)) return KVP_ERR_INVALID;
     const bool mapped = (io->flags & KVP_STEP_HOST_MAPPED) != 0;
-    const void *k_new = io->d_k_new, *v_new = io->d_v_new, *q = io->d_q;
-    void *out = mapped && io->h_out ? io->h_out : io->d_out;
-    float *lse = mapped && io->h_lse ? io->h_lse : io->d_lse;
-    // everything the attention launch would reject, checked before any work
-    auto a16 = [](const void *p) { return ((uintptr_t)p & 15) == 0; };
-    if (!q || !out || !a16(q) || !a16(out) || ((uintptr_t)lse & 3) || ((uintptr_t)workspace & 255))
-        return KVP_ERR_INVALID;
+    const void *out = mapped && io->h_out ? io->h_out : io->d_out;
+    const float *lse = mapped && io->h_lse ? io->h_lse : io->d_lse;
+    if (!io->d_q || !out || !a16(io->d_q) || !a16(out) || ((uintptr_t)lse & 3)) return KVP_ERR_INVALID;
     if (!mapped && ((io->h_out && !io->d_out) || (io->h_lse && !io->d_lse))) return KVP_ERR_INVALID;
     if (mapped && !(a16(io->h_k_new) && a16(io->h_v_new) && a16(io->h_q))) return KVP_ERR_INVALID;
-    const size_t kv_bytes = (size_t)pv.L * num_seqs * ntok * pv.Hkv * pv.d * 2;
-    const size_t rows = (size_t)desc->num_layers * num_seqs * desc->num_q_heads;
-    const size_t q_bytes = rows * desc->head_dim * 2, lse_bytes = rows * sizeof(float);
-    cudaStream_t st = (cudaStream_t)stream;
-    thread_local std::vector<int32_t> t_ntoks;
-    if (ntok > 0) {   // the appends must fit before anything is enqueued
-        if (!k_new || !v_new || !a16(k_new) || !a16(v_new)) return KVP_ERR_INVALID;
-        t_ntoks.assign(num_seqs, ntok);
-        int rc = append_batch_check(pool, num_seqs, seq_ids, t_ntoks.data());
-        if (rc) return rc;
-    }
-    if (mapped) {   // all inputs in one copy kernel
+    if (ntok > 0 && (!io->d_k_new || !io->d_v_new || !a16(io->d_k_new) || !a16(io->d_v_new)))
+        return KVP_ERR_INVALID;
+    return KVP_OK;
+}
+
+// Step 1: the inputs to the device buffers (copy-engine transfers, or one
+// copy kernel over all of them from mapped host memory).
+int step_inputs(const kvp_step_io *io, const StepBytes &b, int32_t ntok, cudaStream_t st) {
+    if (io->flags & KVP_STEP_HOST_MAPPED) {
         const void *src[3];
         void *dst[3];
         int64_t len[3];
         int n = 0;
         if (io->h_k_new && ntok > 0) {
-            src[n] = io->h_k_new, dst[n] = io->d_k_new, len[n++] = (int64_t)kv_bytes;
-            src[n] = io->h_v_new, dst[n] = io->d_v_new, len[n++] = (int64_t)kv_bytes;
+            src[n] = io->h_k_new, dst[n] = io->d_k_new, len[n++] = (int64_t)b.kv;
+            src[n] = io->h_v_new, dst[n] = io->d_v_new, len[n++] = (int64_t)b.kv;
         }
-        if (io->h_q) src[n] = io->h_q, dst[n] = io->d_q, len[n++] = (int64_t)q_bytes;
-        if (launch_copy_segments(src, dst, len, n, st) != cudaSuccess) return KVP_ERR_CUDA;
-    } else {
-        if (io->h_k_new && ntok > 0 &&
-            (cudaMemcpyAsync(io->d_k_new, io->h_k_new, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-             cudaMemcpyAsync(io->d_v_new, io->h_v_new, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess))
-            return KVP_ERR_CUDA;
-        if (io->h_q && cudaMemcpyAsync(io->d_q, io->h_q, q_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-            return KVP_ERR_CUDA;
+        if (io->h_q) src[n] = io->h_q, dst[n] = io->d_q, len[n++] = (int64_t)b.q;
+        return launch_copy_segments(src, dst, len, n, st) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
     }
-    // the append's bookkeeping now, its device write right before attention
-    StagedAppend staged{pool, k_new, v_new, 0};
+    if (io->h_k_new && ntok > 0 &&
+        (cudaMemcpyAsync(io->d_k_new, io->h_k_new, b.kv, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+         cudaMemcpyAsync(io->d_v_new, io->h_v_new, b.kv, cudaMemcpyHostToDevice, st) != cudaSuccess))
+        return KVP_ERR_CUDA;
+    if (io->h_q && cudaMemcpyAsync(io->d_q, io->h_q, b.q, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return KVP_ERR_CUDA;
+    return KVP_OK;
+}
+
+// The host half: the append's bookkeeping and the plan over the grown
+// sequences (the append was checked to fit).  For a pool whose tables are
+// consistent, planning after a committed append cannot fail.
+int plan_step(kvp_step_plan &sp, kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, int32_t ntok,
+              const kvp_attn_desc &d, const int32_t *ntoks) {
+    sp.pool = pool;
+    sp.desc = d;
+    sp.num_seqs = num_seqs;
+    sp.ntok = ntok;
+    sp.slots.clear();
+    sp.cow.clear();
     if (ntok > 0) {
-        int rc = append_batch_commit(pool, num_seqs, seq_ids, t_ntoks.data(), k_new, v_new, &staged.total);
+        int32_t total = 0;
+        const int rc = append_batch_commit_lists(pool, num_seqs, seq_ids, ntoks, sp.slots, sp.cow, &total);
         if (rc) return rc;
     }
     HostPlan &hp = t_plan;
     hp.clear();
-    int rc = plan_pool(pool, seq_ids, num_seqs, *desc, hp);
-    if (rc == KVP_OK) {
-        const size_t need = layout(hp, *desc).total;
-        if (ws_needed) *ws_needed = need;
-        if (ws_bytes < need) rc = KVP_ERR_WORKSPACE;
-    }
-    if (rc) {   // the pool already holds the new tokens: write them
-        if (ntok > 0 && append_issue(pool, staged.k, staged.v, staged.total, stream)) return KVP_ERR_CUDA;
-        return rc;
-    }
-    rc = run_pool(hp, *desc, pv, q, num_seqs, out, lse, workspace, ws_bytes, st, ntok > 0 ? &staged : nullptr);
+    const int rc = plan_pool(pool, seq_ids, num_seqs, d, hp);
     if (rc) return rc;
-    if (mapped) return KVP_OK;
-    if (io->h_out && cudaMemcpyAsync(io->h_out, io->d_out, q_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    pack(hp, d, sp.pk);
+    sp.ready = true;
+    return KVP_OK;
+}
+
+// The device half after the inputs: plan upload, the append's write,
+// attention, merge, then the outputs' copies.  With too small a workspace
+// only the append is written.
+int launch_step(kvp_step_plan &sp, const kvp_step_io *io, void *ws, size_t ws_bytes, cudaStream_t st) {
+    sp.ready = false;
+    const PoolView pv = pool_view(sp.pool);
+    const bool mapped = (io->flags & KVP_STEP_HOST_MAPPED) != 0;
+    void *out = mapped && io->h_out ? io->h_out : io->d_out;
+    float *lse = mapped && io->h_lse ? io->h_lse : io->d_lse;
+    if (ws_bytes < sp.pk.w.total) {   // the pool already holds the new tokens: write them
+        if (!sp.slots.empty() &&
+            append_issue_lists(sp.pool, sp.slots, sp.cow, io->d_k_new, io->d_v_new, st) != KVP_OK)
+            return KVP_ERR_CUDA;
+        return KVP_ERR_WORKSPACE;
+    }
+    const StagedAppend staged{sp.pool, &sp.slots, &sp.cow, io->d_k_new, io->d_v_new};
+    int rc = launch_packed(sp.pk, sp.desc, io->d_q, pv.k, pv.v, sp.num_seqs, nullptr, 0, out, lse, ws, ws_bytes,
+                           st, pv.kv4 ? pv.k_exp : nullptr, pv.kv4 ? pv.v_exp : nullptr,
+                           sp.slots.empty() ? nullptr : &staged);
+    if (rc || mapped) return rc;
+    const StepBytes b = step_bytes(sp.desc, sp.num_seqs, sp.ntok);
+    if (io->h_out && cudaMemcpyAsync(io->h_out, io->d_out, b.q, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return KVP_ERR_CUDA;
-    if (io->h_lse && cudaMemcpyAsync(io->h_lse, io->d_lse, lse_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (io->h_lse && cudaMemcpyAsync(io->h_lse, io->d_lse, b.lse, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return KVP_ERR_CUDA;
     return KVP_OK;
+}
+
+// The checks shared by kvp_decode_step and kvp_decode_step_plan; fills the
+// per-sequence token counts.
+int check_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, int32_t ntok, const kvp_attn_desc *desc,
+               std::vector<int32_t> &ntoks) {
+    if (!pool || !desc_ok(desc) || num_seqs <= 0 || !seq_ids || ntok < 0) return KVP_ERR_INVALID;
+    if (!desc_matches_pool(*desc, pool_view(pool))) return KVP_ERR_INVALID;
+    if ((int64_t)num_seqs * ntok > INT32_MAX / 2) return KVP_ERR_INVALID;
+    ntoks.assign(num_seqs, ntok);
+    if (ntok > 0) return append_batch_check(pool, num_seqs, seq_ids, ntoks.data());
+    return KVP_OK;
+}
+
+thread_local kvp_step_plan t_step;
+thread_local std::vector<int32_t> t_ntoks;
+
+}  // namespace
+
+extern "C" {
+
+int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, int32_t ntok,
+                    const kvp_step_io *io, const kvp_attn_desc *desc, void *workspace,
+                    size_t ws_bytes, size_t *ws_needed, void *stream) {
+    if (!workspace || ((uintptr_t)workspace & 255)) return KVP_ERR_INVALID;
+    int rc = check_io(io, ntok);
+    if (rc) return rc;
+    rc = check_step(pool, seq_ids, num_seqs, ntok, desc, t_ntoks);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    // the inputs' copies first, so that they run while the host plans
+    rc = step_inputs(io, step_bytes(*desc, num_seqs, ntok), ntok, st);
+    if (rc) return rc;
+    rc = plan_step(t_step, pool, seq_ids, num_seqs, ntok, *desc, t_ntoks.data());
+    if (rc) return rc;
+    if (ws_needed) *ws_needed = t_step.pk.w.total;
+    return launch_step(t_step, io, workspace, ws_bytes, st);
+}
+
+kvp_step_plan *kvp_step_plan_create(void) { return new (std::nothrow) kvp_step_plan(); }
+
+void kvp_step_plan_destroy(kvp_step_plan *plan) { delete plan; }
+
+int kvp_decode_step_plan(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, int32_t ntok,
+                         const kvp_attn_desc *desc, kvp_step_plan *plan, size_t *ws_needed) {
+    if (!plan || plan->ready) return KVP_ERR_INVALID;
+    int rc = check_step(pool, seq_ids, num_seqs, ntok, desc, t_ntoks);
+    if (rc) return rc;
+    rc = plan_step(*plan, pool, seq_ids, num_seqs, ntok, *desc, t_ntoks.data());
+    if (rc) return rc;
+    if (ws_needed) *ws_needed = plan->pk.w.total;
+    return KVP_OK;
+}
+
+int kvp_decode_step_run(kvp_step_plan *plan, const kvp_step_io *io, void *workspace, size_t ws_bytes,
+                        void *stream) {
+    if (!plan || !plan->ready || !workspace || ((uintptr_t)workspace & 255)) return KVP_ERR_INVALID;
+    int rc = check_io(io, plan->ntok);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    rc = step_inputs(io, step_bytes(plan->desc, plan->num_seqs, plan->ntok), plan->ntok, st);
+    if (rc) return rc;
+    return launch_step(*plan, io, workspace, ws_bytes, st);
 }
 
 size_t kvp_verify_workspace_size(const kvp_attn_desc *desc, const int32_t *block_tables,

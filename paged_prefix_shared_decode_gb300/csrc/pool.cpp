@@ -127,8 +127,11 @@ int check_append(const kvp_pool *p, int32_t s, int32_t ntok,
     return KVP_OK;
 }
 
-int issue_write(kvp_pool *p, const void *k, const void *v, int32_t ntok, void *stream) {
-    if (ntok == 0 && p->cow.empty()) return KVP_OK;
+// The device write of an append: the copy-on-write triples cow[0..3*ncow)
+// and the token scatter to slots[0..ntok).
+int issue_write_lists(kvp_pool *p, const int32_t *slots, const int32_t *cow, int32_t ncow, const void *k,
+                      const void *v, int32_t ntok, void *stream) {
+    if (ntok == 0 && ncow == 0) return KVP_OK;
     if (p->kv4) {
         kvp::Kv4Write w{};
         w.k_codes = p->k;
@@ -143,9 +146,9 @@ int issue_write(kvp_pool *p, const void *k, const void *v, int32_t ntok, void *s
         w.bs = p->desc.block_size;
         w.d = p->desc.head_dim;
         w.ntok = ntok;
-        w.slots = p->slots.data();
-        w.ncow = (int32_t)(p->cow.size() / 3);
-        w.cow = p->cow.data();
+        w.slots = slots;
+        w.ncow = ncow;
+        w.cow = cow;
         return kvp::launch_kv4_write(w, (cudaStream_t)stream) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
     }
     kvp::KvWrite w{};
@@ -159,11 +162,16 @@ int issue_write(kvp_pool *p, const void *k, const void *v, int32_t ntok, void *s
     w.bs = p->desc.block_size;
     w.d = p->desc.head_dim;
     w.ntok = ntok;
-    w.slots = p->slots.data();
-    w.ncow = (int32_t)(p->cow.size() / 3);
-    w.cow = p->cow.data();
+    w.slots = slots;
+    w.ncow = ncow;
+    w.cow = cow;
     cudaError_t e = kvp::launch_kv_write(w, (cudaStream_t)stream);
     return e == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+// The write of the append staged in the pool.
+int issue_write(kvp_pool *p, const void *k, const void *v, int32_t ntok, void *stream) {
+    return issue_write_lists(p, p->slots.data(), p->cow.data(), (int32_t)(p->cow.size() / 3), k, v, ntok, stream);
 }
 
 bool aligned16(const void *ptr) { return ((uintptr_t)ptr & 15) == 0; }
@@ -560,8 +568,22 @@ int append_batch_commit(kvp_pool *p, int32_t nseq, const int32_t *seqs, const in
     return KVP_OK;
 }
 
-int append_issue(kvp_pool *p, const void *k, const void *v, int32_t total, void *stream) {
-    return issue_write(p, k, v, total, stream);
+int append_batch_commit_lists(kvp_pool *p, int32_t nseq, const int32_t *seqs, const int32_t *ntoks,
+                              std::vector<int32_t> &slots, std::vector<int32_t> &cow, int32_t *total_out) {
+    int64_t total = 0;
+    int rc = append_batch_check(p, nseq, seqs, ntoks, &total);
+    if (rc) return rc;
+    slots.clear();
+    cow.clear();
+    for (int32_t i = 0; i < nseq; ++i) commit_append(p, seqs[i], ntoks[i], slots, cow);
+    *total_out = (int32_t)total;
+    return KVP_OK;
+}
+
+int append_issue_lists(kvp_pool *p, const std::vector<int32_t> &slots, const std::vector<int32_t> &cow,
+                       const void *k, const void *v, void *stream) {
+    return issue_write_lists(p, slots.data(), cow.data(), (int32_t)(cow.size() / 3), k, v, (int32_t)slots.size(),
+                             stream);
 }
 
 PoolView pool_view(const kvp_pool *p) {

@@ -11,7 +11,12 @@
   plan and kernels), for bf16 and 4-bit pages;
 - a too-small workspace returns KVP_ERR_WORKSPACE with the size needed after
   the append, and paged_decode_attention_pool finishes the step; an append
-  that does not fit returns KVP_ERR_OOM with the pool unchanged."""
+  that does not fit returns KVP_ERR_OOM with the pool unchanged;
+- the step in two halves (kvp_decode_step_plan, kvp_decode_step_run): a
+  planned-then-run step gives the same bits as the host-table entry point,
+  a loop that plans step i + 1 while the device runs step i follows the
+  oracle step after step, and the plan object's states (run before plan,
+  plan twice, a short workspace) give the documented errors."""
 import numpy as np
 import pytest
 
@@ -230,4 +235,110 @@ def test_small_workspace_and_full_pool():
     assert e.value.code == kvp.KVP_ERR_OOM
     assert [kvp.seq_len(p.pool, s) for s in seqs] == lens
     p.same(seqs + [filler])
+    p.close()
+
+
+def step_buffers(S, ntok=1):
+    d_k = torch.empty((L, S * ntok, HKV, D), dtype=torch.bfloat16, device="cuda")
+    d_q = torch.empty((L, S, HQ, D), dtype=torch.bfloat16, device="cuda")
+    return dict(d_k=d_k, d_v=torch.empty_like(d_k), d_q=d_q, d_out=torch.empty_like(d_q),
+                d_lse=torch.empty((L, S, HQ), dtype=torch.float32, device="cuda"),
+                h_k=torch.empty(d_k.shape, dtype=torch.bfloat16).pin_memory(),
+                h_v=torch.empty(d_k.shape, dtype=torch.bfloat16).pin_memory(),
+                h_q=torch.empty(d_q.shape, dtype=torch.bfloat16).pin_memory(),
+                h_out=torch.empty(d_q.shape, dtype=torch.bfloat16).pin_memory(),
+                h_lse=torch.empty((L, S, HQ), dtype=torch.float32).pin_memory())
+
+
+def bits_into(dst, bits):
+    dst.copy_(torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16))
+
+
+@pytest.mark.parametrize("mapped", [True, False])
+def test_planned_steps_overlap_the_device(mapped):
+    p = Pool()
+    seqs = p.forked_batch()
+    S = len(seqs)
+    b = step_buffers(S)
+    io = kvp.step_io(b["d_q"], b["d_out"], b["d_lse"], b["d_k"], b["d_v"], h_k_new=b["h_k"], h_v_new=b["h_v"],
+                     h_q=b["h_q"], h_out=b["h_out"], h_lse=b["h_lse"], host_mapped=mapped)
+    ws = torch.empty(4 << 20, dtype=torch.uint8, device="cuda")
+    sp = kvp.StepPlan(p.pool, seqs, 1, io, p.desc, ws)
+    need = sp.plan()                          # step 0's host half
+    assert 0 < need <= ws.numel()
+    # the sequences hold the planned token at once
+    assert [kvp.seq_len(p.pool, s) for s in seqs] == [p.m.length(s) + 1 for s in seqs]
+    steps = 4
+    for step in range(steps):
+        k, v = p.kv(S)
+        q = W.normal_bf16(66, step, (L, S, HQ, D))
+        bits_into(b["h_k"], k)
+        bits_into(b["h_v"], v)
+        bits_into(b["h_q"], q)
+        sp.run()
+        if step + 1 < steps:
+            sp.plan()                         # step + 1's host half, while the device runs this step
+        torch.cuda.synchronize()
+        assert kvp.kvp_device_error(ws) == 0
+        p.model_append(seqs, [1] * S, k, v)
+        want, want_lse = p.oracle(q, seqs)
+        check_close(to_f64(b["h_out"]), want)
+        check_lse(to_f64(b["h_lse"]), want_lse)
+    p.same(seqs)
+    sp.close()
+    p.close()
+
+
+def test_planned_step_matches_host_tables_and_errors():
+    p = Pool()
+    seqs = p.forked_batch()
+    S = len(seqs)
+    b = step_buffers(S)
+    io = kvp.step_io(b["d_q"], b["d_out"], b["d_lse"], b["d_k"], b["d_v"])
+    ws = torch.empty(4 << 20, dtype=torch.uint8, device="cuda")
+    plan = kvp.kvp_step_plan_create()
+    # a run with nothing planned
+    with pytest.raises(kvp.KvpError) as e:
+        kvp.kvp_decode_step_run(plan, io, ws)
+    assert e.value.code == kvp.KVP_ERR_INVALID
+    k, v = p.kv(S)
+    q = W.normal_bf16(67, 0, (L, S, HQ, D))
+    b["d_k"].copy_(bf16_tensor(k))
+    b["d_v"].copy_(bf16_tensor(v))
+    b["d_q"].copy_(bf16_tensor(q))
+    kvp.kvp_decode_step_plan(p.pool, seqs, 1, p.desc, plan)
+    # a second plan while the first waits for its run: its tokens are already in
+    with pytest.raises(kvp.KvpError) as e:
+        kvp.kvp_decode_step_plan(p.pool, seqs, 1, p.desc, plan)
+    assert e.value.code == kvp.KVP_ERR_INVALID
+    kvp.kvp_decode_step_run(plan, io, ws)
+    torch.cuda.synchronize()
+    p.model_append(seqs, [1] * S, k, v)
+    p.same(seqs)
+    ro, rl = p.reference_call(b["d_q"], seqs)
+    assert torch.equal(ro, b["d_out"]) and torch.equal(rl, b["d_lse"])
+    want, want_lse = p.oracle(q, seqs)
+    check_close(to_f64(b["d_out"]), want)
+    check_lse(to_f64(b["d_lse"]), want_lse)
+    # a short workspace: the append is written, the plan is used up
+    k, v = p.kv(S)
+    b["d_k"].copy_(bf16_tensor(k))
+    b["d_v"].copy_(bf16_tensor(v))
+    need = kvp.kvp_decode_step_plan(p.pool, seqs, 1, p.desc, plan)
+    small = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    assert need > small.numel()
+    with pytest.raises(kvp.KvpError) as e:
+        kvp.kvp_decode_step_run(plan, io, small)
+    assert e.value.code == kvp.KVP_ERR_WORKSPACE
+    with pytest.raises(kvp.KvpError) as e:
+        kvp.kvp_decode_step_run(plan, io, ws)
+    assert e.value.code == kvp.KVP_ERR_INVALID
+    p.model_append(seqs, [1] * S, k, v)
+    p.same(seqs)
+    kvp.paged_decode_attention_pool(p.pool, seqs, b["d_q"], b["d_out"], b["d_lse"], p.desc, ws)
+    torch.cuda.synchronize()
+    want, want_lse = p.oracle(q, seqs)
+    check_close(to_f64(b["d_out"]), want)
+    check_lse(to_f64(b["d_lse"]), want_lse)
+    kvp.kvp_step_plan_destroy(plan)
     p.close()
