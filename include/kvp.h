@@ -491,7 +491,10 @@ int kvp_device_error(void *workspace, void *stream, int32_t *err_out);
  * work items, row tiles, 64-token KV tiles and partial rows per (layer, kv
  * head), and the bytes of distinct (block, valid tokens) one call reads over
  * all layers, planned for a GPU with sm_count SMs.  Any out-pointer may be
- * NULL. */
+ * NULL.  The plan's internal invariants (tile ranges inside the tile list
+ * and within the kernels' descriptor stage, rows within each kernel's unit,
+ * member intervals inside their items) are checked: KVP_ERR_STATE if one
+ * fails, which would be a planner defect. */
 int kvp_decode_plan_stats(const kvp_attn_desc *desc, const int32_t *block_tables,
                           const int32_t *seq_lens, int32_t num_seqs, int32_t max_blocks,
                           int32_t sm_count, int32_t *n_items, int32_t *n_row_tiles,

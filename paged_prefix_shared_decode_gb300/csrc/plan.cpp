@@ -683,6 +683,30 @@ int run(const HostPlan &hp, const kvp_attn_desc &d, const void *q, const void *k
                          k_exp, v_exp);
 }
 
+// The plan's own invariants, for the host-side stats call: every item's
+// tiles lie inside the tile list and fit the kernels' descriptor stage, its
+// rows fit its kernel's unit, and every tile holds 1..64 tokens and a member
+// interval inside its item.
+bool plan_consistent(const HostPlan &hp, int32_t G) {
+    const int32_t nt = (int32_t)hp.tiles.size();
+    auto item_ok = [&](const WorkItem &it, int32_t max_rows) {
+        if (it.tile_begin < 0 || it.tile_end <= it.tile_begin || it.tile_end > nt) return false;
+        if (it.tile_end - it.tile_begin > kMaxItemTiles || it.n_members <= 0 || it.n_members * G > max_rows)
+            return false;
+        for (int32_t t = it.tile_begin; t < it.tile_end; ++t) {
+            const KvTile &k = hp.tiles[t];
+            const int32_t lo = k.members & 0xFFFF, hi = k.members >> 16, n = k.ntok_flags & 0xFFFF;
+            if (n < 1 || n > kTileTokens || hi <= lo || hi > it.n_members) return false;
+        }
+        return true;
+    };
+    for (const WorkItem &it : hp.items)
+        if (!item_ok(it, kMmaMaxRows)) return false;
+    for (const WorkItem &it : hp.tc_items)
+        if (!item_ok(it, kTcRows)) return false;
+    return true;
+}
+
 bool desc_matches_pool(const kvp_attn_desc &d, const PoolView &pv) {
     return d.num_layers == pv.L && d.num_kv_heads == pv.Hkv && d.head_dim == pv.d &&
            d.block_size == pv.bs && d.num_blocks == pv.NB &&
@@ -1027,6 +1051,7 @@ int kvp_decode_plan_stats(const kvp_attn_desc *desc, const int32_t *block_tables
     hp.clear();
     int rc = build_decode(*desc, block_tables, seq_lens, num_seqs, max_blocks, sm_count, hp);
     if (rc) return rc;
+    if (!plan_consistent(hp, desc->num_q_heads / desc->num_kv_heads)) return KVP_ERR_STATE;
     if (n_items) *n_items = (int32_t)(hp.items.size() + hp.tc_items.size());
     if (n_row_tiles) *n_row_tiles = hp.n_row_tiles;
     if (n_kv_tiles) *n_kv_tiles = (int32_t)hp.tiles.size();

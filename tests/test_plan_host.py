@@ -10,7 +10,10 @@ computed here from the block tables alone.
 - the plan's shape (items, KV tiles, partial rows) depends on which blocks
   are shared, not on their ids: the same batch built on a differently
   shuffled free list plans the same shape;
-- the pool-table and host-table entry points size the same workspace."""
+- the pool-table and host-table entry points size the same workspace;
+- the plan keeps its own invariants (checked inside kvp_decode_plan_stats)
+  on both kernels' shapes: head dim 64 (mma.sync only) and head dim 128 with
+  many-row items on the tcgen05 kernel."""
 import random
 
 import numpy as np
@@ -87,4 +90,26 @@ def test_plan_is_repeatable_and_rejects_bad_tables():
     empty[1] = 0                # an empty sequence
     with pytest.raises(kvp.KvpError):
         kvp.kvp_decode_plan_stats(d, t, empty)
+    kvp.kv_pool_destroy(p)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_plan_invariants_with_tcgen05_items(seed):
+    # head dim 128, GQA 4: items of more than 32 rows go to the tcgen05
+    # kernel, the rest to mma.sync; a wide fork gives both
+    rng = random.Random(seed)
+    bs, n = 16, 48
+    p = kvp.kv_pool_create(kvp.PoolDesc(2, 4096, bs, 8, 128, n + 1, 96, seed + 7))
+    root = kvp.seq_alloc(p)
+    kvp.seq_reserve(p, root, 700 + seed)
+    seqs = []
+    for i in range(n):
+        s = kvp.seq_fork(p, rng.choice([root] + seqs))
+        kvp.seq_reserve(p, s, rng.randrange(1, 3 * bs))
+        seqs.append(s)
+    t, ln = kvp.kvp_gather_tables(p, seqs, 96)
+    d = kvp.AttnDesc(2, 32, 8, 128, bs, 4096, 0.0, 1)
+    st = kvp.kvp_decode_plan_stats(d, t, ln)
+    assert st["unique_kv_bytes"] == unique_bytes(t, ln, bs, 2 * 8 * 128 * 2 * 2)
+    assert st["row_tiles"] == -(-n // (256 // 4))
     kvp.kv_pool_destroy(p)
