@@ -96,6 +96,17 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
+// non-blocking test of a phase
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -404,8 +415,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_after();
     const uint32_t tmem = *s_tmem;
 
-    // bounded wait; on a timeout the whole CTA aborts
+    // bounded wait; on a timeout the whole CTA aborts.  A phase that is
+    // already complete is seen by the non-blocking test first, which measured
+    // about half the latency of try_wait on the MMA thread's critical path.
     auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+        if (mbar_test_wait(b, parity)) return true;
         for (uint32_t i = 0; i < kWaitLimit; ++i) {
             if (mbar_try_wait(b, parity)) return true;
             if ((i & 1023) == 1023 && *s_abort) return false;
