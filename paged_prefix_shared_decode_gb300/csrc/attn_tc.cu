@@ -142,6 +142,10 @@ __device__ __forceinline__ bool soft_bar_or(bool v) {
 }
 
 // ---- tcgen05
+// (The start address is the low 14 bits, in 16-byte units; shared memory
+// addresses stay below 2^18, so a descriptor plus (bytes >> 4) describes the
+// operand that many bytes further on.  The MMA thread builds one descriptor
+// per operand and step and offsets it per instruction.)
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = (uint64_t)((addr >> 4) & 0x3FFF);
     d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
@@ -626,11 +630,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_after();
                     const uint32_t kst = k_smem + st * C::OPER;
                     const uint32_t d_tm = tmem + C::S_COL + (t & 1) * kStepTokens;
+                    const uint64_t qd = sdesc(q_smem, 16, 1024), kd = sdesc(kst, 16, 1024);
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t o = (uint32_t)(k >> 2) * C::SLAB + (uint32_t)(k & 3) * 32;
-                        umma_ss(d_tm, sdesc(q_smem + o, 16, 1024), sdesc(kst + o, 16, 1024), IDESC_S,
-                                k > 0 ? 1u : 0u);
+                        const uint32_t o = ((uint32_t)(k >> 2) * C::SLAB + (uint32_t)(k & 3) * 32) >> 4;
+                        umma_ss(d_tm, qd + o, kd + o, IDESC_S, k > 0 ? 1u : 0u);
                     }
                     umma_commit(bar(C::B_S_FULL + (t & 1)));
                     umma_commit(bar(C::B_K_EMPTY + st));
@@ -651,11 +655,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const uint32_t st = (gk + t) % C::NK;
                         const uint32_t kst = k_smem + st * C::OPER, qs = q_smem + tq * C::OPER;
                         const uint32_t d_tm = tmem + C::S_COL + tq * kStepTokens;
+                        const uint64_t qd = sdesc(qs, 16, 1024), kd = sdesc(kst, 16, 1024);
 #pragma unroll
                         for (int k = 0; k < D / 16; ++k) {
-                            const uint32_t o = (uint32_t)(k >> 2) * C::SLAB + (uint32_t)(k & 3) * 32;
-                            umma_ss(d_tm, sdesc(qs + o, 16, 1024), sdesc(kst + o, 16, 1024), IDESC_S,
-                                    k > 0 ? 1u : 0u);
+                            const uint32_t o = ((uint32_t)(k >> 2) * C::SLAB + (uint32_t)(k & 3) * 32) >> 4;
+                            umma_ss(d_tm, qd + o, kd + o, IDESC_S, k > 0 ? 1u : 0u);
                         }
                         umma_commit(bar(C::B_S_FULL + tq));
                         if (tq == 1) {
@@ -682,9 +686,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             if (tq == 0 && !wait(bar(C::B_V_FULL + st), (g / C::NV) & 1)) { ok = false; break; }
                             if (tq == 0) fence_async_smem();
                             tc_after();
-                            for (int k = 0; k < ksteps; ++k)
-                                umma_ts(tmem + C::O_COL + tq * D, tmem + C::S_COL + tq * kStepTokens + k * 8,
-                                        sdesc(vst + k * 2048, C::SLAB, 1024), IDESC_PV, (t > 0 || k > 0) ? 1u : 0u);
+                            const uint64_t vd = sdesc(vst, C::SLAB, 1024);
+                            const uint32_t o_tm = tmem + C::O_COL + tq * D, p_tm = tmem + C::S_COL + tq * kStepTokens;
+#pragma unroll
+                            for (int k = 0; k < kStepTokens / 16; ++k)
+                                if (k < ksteps)
+                                    umma_ts(o_tm, p_tm + k * 8, vd + k * (2048 >> 4), IDESC_PV,
+                                            (t > 0 || k > 0) ? 1u : 0u);
                             if (tq == 1) umma_commit(bar(C::B_V_EMPTY + st));
                             if (t + 1 < nsteps) {
                                 if (tq == 0 && !wait_k(t + 1)) { ok = false; break; }
@@ -709,9 +717,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t vst = v_smem + st * C::OPER;
                     // an odd last tile leaves rows 64..127 of V unwritten: skip them
                     const int ksteps = 2 * t + 1 < ntile ? kStepTokens / 16 : kTileTokens / 16;
-                    for (int k = 0; k < ksteps; ++k)
-                        umma_ts(tmem + C::O_COL + grp * D, tmem + C::S_COL + grp * kStepTokens + k * 8,
-                                sdesc(vst + k * 2048, C::SLAB, 1024), IDESC_PV, (t >= 2 || k > 0) ? 1u : 0u);
+                    const uint64_t vd = sdesc(vst, C::SLAB, 1024);
+                    const uint32_t o_tm = tmem + C::O_COL + grp * D, p_tm = tmem + C::S_COL + grp * kStepTokens;
+#pragma unroll
+                    for (int k = 0; k < kStepTokens / 16; ++k)
+                        if (k < ksteps)
+                            umma_ts(o_tm, p_tm + k * 8, vd + k * (2048 >> 4), IDESC_PV, (t >= 2 || k > 0) ? 1u : 0u);
                     umma_commit(bar(C::B_V_EMPTY + st));
                     if (t + 2 < nsteps && !issue_s(t + 2)) { ok = false; break; }
                 }
