@@ -875,18 +875,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             const bool write = has && nsteps > 0;
             for (int c0 = ca; !idle && c0 < cb; c0 += 32) {
-                uint32_t x[32], y[32];
-                tmem_ld32(o_tm + c0, x);
-                tmem_ld32(o_tm + D + c0, y);
-                tmem_wait_ld();
-                if (!write) continue;
-                // an O with weight 0 may never have been written (a group with
-                // no steps or no valid key): select, do not multiply
+                uint32_t x[32];
+                if (pair) {   // this group's own tile: its O alone
+                    tmem_ld32(o_tm + grp * D + c0, x);
+                    tmem_wait_ld();
+                    if (!write) continue;
+                    const float w = grp ? w1 : w0;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float v0 = w0 != 0.f ? __uint_as_float(x[j]) * w0 : 0.f;
-                    const float v1 = w1 != 0.f ? __uint_as_float(y[j]) * w1 : 0.f;
-                    x[j] = __float_as_uint(v0 + v1);
+                    for (int j = 0; j < 32; ++j)
+                        x[j] = __float_as_uint(w != 0.f ? __uint_as_float(x[j]) * w : 0.f);
+                } else {
+                    uint32_t y[32];
+                    tmem_ld32(o_tm + c0, x);
+                    tmem_ld32(o_tm + D + c0, y);
+                    tmem_wait_ld();
+                    if (!write) continue;
+                    // an O with weight 0 may never have been written (a group
+                    // with no steps or no valid key): select, do not multiply
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float v0 = w0 != 0.f ? __uint_as_float(x[j]) * w0 : 0.f;
+                        const float v1 = w1 != 0.f ? __uint_as_float(y[j]) * w1 : 0.f;
+                        x[j] = __float_as_uint(v0 + v1);
+                    }
                 }
                 if (it.out_base < 0) {
                     __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(a.out) +
@@ -901,12 +912,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         *reinterpret_cast<uint4 *>(dst + j) = v;
                     }
                 } else {
+                    // the workspace is 256-byte aligned: 32-byte stores
                     float *dst = a.part_o + (((size_t)l * a.Hkv + kvh) * a.P + it.out_base + rr) * D + c0;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(dst + j) =
-                            make_float4(__uint_as_float(x[j]), __uint_as_float(x[j + 1]),
-                                        __uint_as_float(x[j + 2]), __uint_as_float(x[j + 3]));
+                    for (int j = 0; j < 32; j += 8)
+                        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"l"(dst + j),
+                                     "r"(x[j]), "r"(x[j + 1]), "r"(x[j + 2]), "r"(x[j + 3]), "r"(x[j + 4]),
+                                     "r"(x[j + 5]), "r"(x[j + 6]), "r"(x[j + 7])
+                                     : "memory");
                 }
             }
             if (write && (pair || grp == 0)) {
