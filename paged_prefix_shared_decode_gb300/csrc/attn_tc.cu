@@ -638,7 +638,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     umma_commit(bar(C::B_S_FULL + (t & 1)));
                     umma_commit(bar(C::B_K_EMPTY + st));
-                    if (t == nsteps - 1) umma_commit(bar(C::B_Q_EMPTY));
                     return true;
                 };
                 if (pair) {
@@ -662,10 +661,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             umma_ss(d_tm, qd + o, kd + o, IDESC_S, k > 0 ? 1u : 0u);
                         }
                         umma_commit(bar(C::B_S_FULL + tq));
-                        if (tq == 1) {
-                            umma_commit(bar(C::B_K_EMPTY + st));
-                            if (t == nsteps - 1) umma_commit(bar(C::B_Q_EMPTY));
-                        }
+                        if (tq == 1) umma_commit(bar(C::B_K_EMPTY + st));
                     };
                     if (ok && nsteps > 0) {
                         ok = wait_k(0);
@@ -728,6 +724,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 }
                 if (!ok) break;
+                // (with steps, the softmax thread that sees the unit's last S
+                // releases Q)
                 if (nsteps == 0) umma_commit(bar(C::B_Q_EMPTY));
                 gk += nsteps;
                 gv += nsteps;
@@ -781,6 +779,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int t = pair ? 0 : grp; t < nsteps; t += pair ? 1 : 2) {
                 ok = wait(bar(C::B_S_FULL + grp), ns & 1) && ok;
                 ns += 1;
+                // the unit's last S is done with Q: one thread of the group
+                // that takes it releases Q for the next unit's load, as soon
+                // as that S is seen (measured slightly faster than releasing
+                // it with an MMA commit)
+                if (t == nsteps - 1 && grp == (pair ? 1 : (t & 1)) && quarter == 0 && lane == 0)
+                    mbar_arrive(bar(C::B_Q_EMPTY));
                 tc_after();
                 if (idle) {
                     tc_before();
