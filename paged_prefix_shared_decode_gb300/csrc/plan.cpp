@@ -293,10 +293,13 @@ void close_item(Protos &pr) {
 // member interval of the item it came from.  (A tile of one member leaves
 // the warps of the other members' rows idle, so packs stay small: 32 rows
 // measured 8% faster than 64 on Trellis phi = 0.9 and equal on MCTS; no
-// packing made MCTS 43% slower.)
+// packing made MCTS 43% slower.  With a GQA group of 8 or more, packs of 16
+// rows -- at most two members, whose tiles the four warps split four ways --
+// measured 2% faster on Dendrite and 3% on Trellis phi = 0.75, and 16 rows
+// for small groups made MCTS 3% slower.)
 void pack_small(Scratch &sc, int32_t G, int thr) {
     // stay on the mma.sync kernel: at most 32 rows and at most the threshold
-    const int kPackRows = thr < 32 ? thr : 32;
+    const int kPackRows = G >= 8 ? 16 : (thr < 32 ? thr : 32);
     constexpr int kPackTiles = 4, kPackMaxTiles = 64;
     const Protos &in = sc.protos;
     Protos &out = sc.packed;
