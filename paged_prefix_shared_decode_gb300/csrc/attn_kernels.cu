@@ -759,8 +759,13 @@ __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kerne
     __shared__ int s_unit;
     // the plan (work items, tile descriptors, counters) was uploaded before
     // the kernel that may still be running; K/V, q and the tree masks are
-    // read only after it has completed
+    // read only after it has completed (with a.wait_first that kernel wrote
+    // the plan as well: wait before anything)
     bool waited = false;
+    if (a.wait_first) {
+        griddep_wait();
+        waited = true;
+    }
     for (;;) {
         if (threadIdx.x == 0) s_unit = atomicAdd(a.counter, 1);
         __syncthreads();

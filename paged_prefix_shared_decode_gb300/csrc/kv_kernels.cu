@@ -14,6 +14,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstring>
 
 #include "kvp_internal.h"
 
@@ -44,46 +45,86 @@ struct KvWriteArgs {
     int32_t slots[NS];
 };
 
+// Chunk x of an append: x < 2 * cow_chunks copies a used slot of a
+// copy-on-write block, the rest scatter the new tokens (even x: K, odd: V).
+template <int NS, int NC>
+__device__ __forceinline__ void kv_write_chunk(const KvWriteArgs<NS, NC> &a, int64_t x) {
+    const int64_t tile = (int64_t)a.bs * a.CH;     // chunks per (block, head) tile
+    const bool is_v = x & 1;
+    int64_t y = x >> 1;
+    uint4 *pool = is_v ? a.v_pool : a.k_pool;
+    if (y < a.cow_chunks) {
+        // find the triple (few per launch)
+        int i = 0;
+        int64_t per = 0;
+        for (; i < a.ncow; ++i) {
+            per = (int64_t)a.L * a.Hkv * a.cow[3 * i + 2] * a.CH;
+            if (y < per) break;
+            y -= per;
+        }
+        const int64_t run = (int64_t)a.cow[3 * i + 2] * a.CH;   // chunks per (layer, head)
+        const int64_t lh = y / run, c = y % run;
+        const int64_t l = lh / a.Hkv, h = lh % a.Hkv;
+        const int64_t src = ((l * a.NB + a.cow[3 * i]) * a.Hkv + h) * tile + c;
+        const int64_t dst = ((l * a.NB + a.cow[3 * i + 1]) * a.Hkv + h) * tile + c;
+        pool[dst] = pool[src];
+    } else {
+        y -= a.cow_chunks;
+        const int64_t c = y % a.CH;
+        int64_t r = y / a.CH;
+        const int64_t h = r % a.Hkv;
+        r /= a.Hkv;
+        const int64_t t = r % a.ntok;
+        const int64_t l = r / a.ntok;
+        const int32_t slot = a.slots[t];
+        const int64_t blk = slot / a.bs, sl = slot % a.bs;
+        const uint4 *srcp = is_v ? a.v : a.k;
+        const int64_t src = ((l * a.ntok_total + a.tok_begin + t) * a.Hkv + h) * a.CH + c;
+        const int64_t dst = ((l * a.NB + blk) * a.Hkv + h) * tile + sl * a.CH + c;
+        pool[dst] = srcp[src];
+    }
+}
+
 template <int NS, int NC>
 __global__ void __launch_bounds__(256) kv_write_kernel(const __grid_constant__ KvWriteArgs<NS, NC> a) {
     const int64_t tok_chunks = (int64_t)a.L * a.ntok * a.Hkv * a.CH;
     const int64_t total = 2 * (a.cow_chunks + tok_chunks);
-    const int64_t tile = (int64_t)a.bs * a.CH;     // chunks per (block, head) tile
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
+         x += (int64_t)gridDim.x * blockDim.x)
+        kv_write_chunk(a, x);
+}
+
+// A decode step's inputs in one launch: the append (copy-on-write copies and
+// the new tokens' K/V, read straight from page-locked host memory or from
+// the device), q to its device buffer, and the attention plan, carried in
+// the kernel's parameters, into the workspace.  The attention kernels that
+// follow wait for this grid before they read anything, so it lets them
+// launch at once.
+template <int PB>
+struct StepWriteArgs {
+    KvWriteArgs<kSmallSlots, kSmallCow> w;
+    const uint4 *q_src;
+    uint4 *q_dst;
+    int64_t q_chunks;
+    uint4 *plan_dst;
+    int32_t plan_chunks;
+    uint4 plan[PB / 16];
+};
+
+template <int PB>
+__global__ void __launch_bounds__(256) step_write_kernel(const __grid_constant__ StepWriteArgs<PB> s) {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    const KvWriteArgs<kSmallSlots, kSmallCow> &a = s.w;
+    const int64_t kv_total = 2 * (a.cow_chunks + (int64_t)a.L * a.ntok * a.Hkv * a.CH);
+    const int64_t q_end = kv_total + s.q_chunks, total = q_end + s.plan_chunks;
     for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
          x += (int64_t)gridDim.x * blockDim.x) {
-        const bool is_v = x & 1;
-        int64_t y = x >> 1;
-        uint4 *pool = is_v ? a.v_pool : a.k_pool;
-        if (y < a.cow_chunks) {
-            // find the triple (few per launch)
-            int i = 0;
-            int64_t per = 0;
-            for (; i < a.ncow; ++i) {
-                per = (int64_t)a.L * a.Hkv * a.cow[3 * i + 2] * a.CH;
-                if (y < per) break;
-                y -= per;
-            }
-            const int64_t run = (int64_t)a.cow[3 * i + 2] * a.CH;   // chunks per (layer, head)
-            const int64_t lh = y / run, c = y % run;
-            const int64_t l = lh / a.Hkv, h = lh % a.Hkv;
-            const int64_t src = ((l * a.NB + a.cow[3 * i]) * a.Hkv + h) * tile + c;
-            const int64_t dst = ((l * a.NB + a.cow[3 * i + 1]) * a.Hkv + h) * tile + c;
-            pool[dst] = pool[src];
-        } else {
-            y -= a.cow_chunks;
-            const int64_t c = y % a.CH;
-            int64_t r = y / a.CH;
-            const int64_t h = r % a.Hkv;
-            r /= a.Hkv;
-            const int64_t t = r % a.ntok;
-            const int64_t l = r / a.ntok;
-            const int32_t slot = a.slots[t];
-            const int64_t blk = slot / a.bs, sl = slot % a.bs;
-            const uint4 *srcp = is_v ? a.v : a.k;
-            const int64_t src = ((l * a.ntok_total + a.tok_begin + t) * a.Hkv + h) * a.CH + c;
-            const int64_t dst = ((l * a.NB + blk) * a.Hkv + h) * tile + sl * a.CH + c;
-            pool[dst] = srcp[src];
-        }
+        if (x < kv_total)
+            kv_write_chunk(a, x);
+        else if (x < q_end)
+            s.q_dst[x - kv_total] = s.q_src[x - kv_total];
+        else
+            s.plan_dst[x - q_end] = s.plan[x - q_end];
     }
 }
 
@@ -227,6 +268,55 @@ cudaError_t launch_kv_move(const KvMove &m, cudaStream_t stream) {
     kv_move_kernel<<<blocks, 256, 0, stream>>>(a);
     count_launch();
     return cudaGetLastError();
+}
+
+template <int PB>
+cudaError_t launch_step_write_pb(const KvWrite &w, const void *q_src, void *q_dst, size_t q_bytes,
+                                 const void *plan, void *plan_dst, size_t plan_bytes, cudaStream_t stream) {
+    // on the stack: parameters are copied at launch
+    StepWriteArgs<PB> s;
+    KvWriteArgs<kSmallSlots, kSmallCow> &a = s.w;
+    a.k_pool = static_cast<uint4 *>(w.k_pool);
+    a.v_pool = static_cast<uint4 *>(w.v_pool);
+    a.k = static_cast<const uint4 *>(w.k);
+    a.v = static_cast<const uint4 *>(w.v);
+    a.L = w.L; a.NB = w.NB; a.Hkv = w.Hkv; a.bs = w.bs; a.CH = w.d / 8;
+    a.ntok_total = w.ntok;
+    a.ncow = w.ncow;
+    a.cow_chunks = 0;
+    for (int i = 0; i < w.ncow; ++i) {
+        a.cow[3 * i] = w.cow[3 * i];
+        a.cow[3 * i + 1] = w.cow[3 * i + 1];
+        a.cow[3 * i + 2] = w.cow[3 * i + 2];
+        a.cow_chunks += (int64_t)w.L * w.Hkv * a.cow[3 * i + 2] * a.CH;
+    }
+    a.tok_begin = 0;
+    a.ntok = w.ntok;
+    for (int i = 0; i < w.ntok; ++i) a.slots[i] = w.slots[i];
+    s.q_src = static_cast<const uint4 *>(q_src);
+    s.q_dst = static_cast<uint4 *>(q_dst);
+    s.q_chunks = q_src ? (int64_t)(q_bytes / 16) : 0;
+    s.plan_dst = static_cast<uint4 *>(plan_dst);
+    s.plan_chunks = (int32_t)(plan_bytes / 16);
+    std::memcpy(s.plan, plan, plan_bytes);
+    const int64_t total = 2 * (a.cow_chunks + (int64_t)w.L * w.ntok * w.Hkv * a.CH) + s.q_chunks + s.plan_chunks;
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)device_sm_count() * 4));
+    step_write_kernel<PB><<<blocks, 256, 0, stream>>>(s);
+    count_launch();
+    return cudaGetLastError();
+}
+
+bool step_write_fits(const KvWrite &w, size_t plan_bytes) {
+    return w.ntok <= kSmallSlots && w.ncow <= kSmallCow && plan_bytes <= kStepPlanMax && plan_bytes % 16 == 0 &&
+           w.d % 8 == 0;
+}
+
+cudaError_t launch_step_write(const KvWrite &w, const void *q_src, void *q_dst, size_t q_bytes, const void *plan,
+                              void *plan_dst, size_t plan_bytes, cudaStream_t stream) {
+    if (!step_write_fits(w, plan_bytes) || q_bytes % 16 != 0) return cudaErrorInvalidValue;
+    if (plan_bytes <= 8192)
+        return launch_step_write_pb<8192>(w, q_src, q_dst, q_bytes, plan, plan_dst, plan_bytes, stream);
+    return launch_step_write_pb<kStepPlanMax>(w, q_src, q_dst, q_bytes, plan, plan_dst, plan_bytes, stream);
 }
 
 cudaError_t launch_kv_write(const KvWrite &w, cudaStream_t stream) {

@@ -87,6 +87,7 @@ struct AttnLaunch {
     float *part_o;
     float *part_lse;
     int32_t n_units, n_tc_units, n_merge_q, P;
+    int32_t wait_first;   // 1: the kernel before wrote the plan too; wait before reading anything
 };
 
 // before/after: optional events recorded around the work-item kernel.
@@ -179,6 +180,17 @@ struct KvWrite {
 };
 
 cudaError_t launch_kv_write(const KvWrite &w, cudaStream_t stream);
+
+// A decode step's inputs in one launch (the append of w, q_bytes of q from
+// q_src to q_dst when q_src is given, and plan_bytes of a host plan image,
+// carried in the kernel parameters, to plan_dst), letting the kernel launched
+// behind it with programmatic serialisation start at once.  For appends of at
+// most 64 tokens and 16 copy-on-write blocks and plans of at most
+// kStepPlanMax bytes (step_write_fits); cudaErrorInvalidValue otherwise.
+constexpr size_t kStepPlanMax = 24576;
+bool step_write_fits(const KvWrite &w, size_t plan_bytes);
+cudaError_t launch_step_write(const KvWrite &w, const void *q_src, void *q_dst, size_t q_bytes, const void *plan,
+                              void *plan_dst, size_t plan_bytes, cudaStream_t stream);
 
 // Speculative accept on the device: copy-on-write block copies (all slots),
 // then kept draft tokens moved from src to dst slots in order.

@@ -627,10 +627,11 @@ struct StagedAppend {
 
 // Uploads a packed plan into the workspace, issues a staged append, and
 // launches the attention kernels (and the merge).
+// (uploaded: the kernel right before wrote the plan into the workspace.)
 int launch_packed(const Packed &pk, const kvp_attn_desc &d, const void *q, const void *k_pool,
                   const void *v_pool, int32_t nq, const int32_t *parent, int32_t n_draft, void *out,
                   float *lse, void *ws, size_t ws_bytes, cudaStream_t stream, const void *k_exp = nullptr,
-                  const void *v_exp = nullptr, const StagedAppend *append = nullptr) {
+                  const void *v_exp = nullptr, const StagedAppend *append = nullptr, bool uploaded = false) {
     if (!q || !k_pool || !v_pool || !out || !ws) return KVP_ERR_INVALID;
     const bool kv4 = d.kv_format == KVP_KV_4BIT;
     if (kv4 && (!k_exp || !v_exp || (((uintptr_t)k_exp | (uintptr_t)v_exp) & 15))) return KVP_ERR_INVALID;
@@ -641,7 +642,8 @@ int launch_packed(const Packed &pk, const kvp_attn_desc &d, const void *q, const
     const WsLayout &w = pk.w;
     if (ws_bytes < w.total) return KVP_ERR_INVALID;
     // pageable source: the copy is staged before the call returns
-    if (cudaMemcpyAsync(ws, pk.image.data(), w.plan_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    if (!uploaded &&
+        cudaMemcpyAsync(ws, pk.image.data(), w.plan_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return KVP_ERR_CUDA;
     if (append) {
         const int rc = append_issue_lists(append->pool, *append->slots, *append->cow, append->k, append->v, stream);
@@ -674,6 +676,7 @@ int launch_packed(const Packed &pk, const kvp_attn_desc &d, const void *q, const
     a.n_tc_units = pk.n_tc_units;
     a.n_merge_q = pk.n_partial_rows > 0 ? nq : 0;
     a.P = pk.n_partial_rows;
+    a.wait_first = uploaded ? 1 : 0;
     return launch_attention(a, stream, t_ev_before, t_ev_after) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
@@ -999,7 +1002,33 @@ int kvp_decode_step_run(kvp_step_plan *plan, const kvp_step_io *io, void *worksp
     int rc = check_io(io, plan->ntok);
     if (rc) return rc;
     cudaStream_t st = (cudaStream_t)stream;
-    rc = step_inputs(io, step_bytes(plan->desc, plan->num_seqs, plan->ntok), plan->ntok, st);
+    const StepBytes b = step_bytes(plan->desc, plan->num_seqs, plan->ntok);
+    // mapped host buffers on a bf16 pool, a small append and plan: the inputs,
+    // the append and the plan in one kernel, then attention and merge
+    if (io->flags & KVP_STEP_HOST_MAPPED) {
+        const PoolView pv = pool_view(plan->pool);
+        KvWrite w{};
+        w.k_pool = const_cast<void *>(pv.k);
+        w.v_pool = const_cast<void *>(pv.v);
+        w.k = io->h_k_new ? io->h_k_new : io->d_k_new;
+        w.v = io->h_v_new ? io->h_v_new : io->d_v_new;
+        w.L = pv.L; w.NB = pv.NB; w.Hkv = pv.Hkv; w.bs = pv.bs; w.d = pv.d;
+        w.ntok = (int32_t)plan->slots.size();
+        w.slots = plan->slots.data();
+        w.ncow = (int32_t)(plan->cow.size() / 3);
+        w.cow = plan->cow.data();
+        if (!pv.kv4 && ws_bytes >= plan->pk.w.total && step_write_fits(w, plan->pk.w.plan_bytes)) {
+            plan->ready = false;
+            if (launch_step_write(w, io->h_q, io->d_q, b.q, plan->pk.image.data(), workspace, plan->pk.w.plan_bytes,
+                                  st) != cudaSuccess)
+                return KVP_ERR_CUDA;
+            void *out = io->h_out ? io->h_out : io->d_out;
+            float *lse = io->h_lse ? io->h_lse : io->d_lse;
+            return launch_packed(plan->pk, plan->desc, io->d_q, pv.k, pv.v, plan->num_seqs, nullptr, 0, out, lse,
+                                 workspace, ws_bytes, st, nullptr, nullptr, nullptr, true);
+        }
+    }
+    rc = step_inputs(io, b, plan->ntok, st);
     if (rc) return rc;
     return launch_step(*plan, io, workspace, ws_bytes, st);
 }
