@@ -458,13 +458,16 @@ int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, in
  *     the grown sequences, packed into `plan`.  No device work.  *ws_needed
  *     (may be NULL) receives the workspace bytes the run will need.
  *   kvp_decode_step_run: steps 1-4 of kvp_decode_step for that plan, with the
- *     plan's upload into `workspace` right before the append's write.  With
- *     KVP_STEP_HOST_MAPPED on a bf16 pool, an append of at most 64 tokens and
- *     16 copy-on-write blocks and a plan of at most 24 KB, steps 1-2 and the
- *     plan upload are one kernel: the new K/V go from host memory straight
- *     into their pool slots (d_k_new / d_v_new are then left unwritten), q to
- *     d_q, and the plan, carried in the kernel's parameters, into the
- *     workspace; attention and merge follow.
+ *     plan's upload into `workspace` right before the append's write.
+ *
+ * Both kvp_decode_step and kvp_decode_step_run, when the step's inputs are
+ * already on the device or in mapped host memory (KVP_STEP_HOST_MAPPED), the
+ * pool holds bf16 pages, the append has at most 64 tokens and 16
+ * copy-on-write blocks and the plan at most 24 KB, make steps 1-2 and the
+ * plan upload one kernel: the new K/V go straight into their pool slots (from
+ * host memory when mapped; d_k_new / d_v_new are then left unwritten), q to
+ * d_q, and the plan, carried in the kernel's parameters, into the workspace;
+ * attention and merge follow.
  *
  * A plan object (kvp_step_plan_create; kvp_step_plan_destroy frees it) holds
  * one planned step at a time and is reused from step to step.  Planning a

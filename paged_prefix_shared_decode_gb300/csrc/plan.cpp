@@ -944,6 +944,48 @@ int launch_step(kvp_step_plan &sp, const kvp_step_io *io, void *ws, size_t ws_by
     return KVP_OK;
 }
 
+// The planned step with its inputs already on the device or in mapped host
+// memory, on a bf16 pool with a small append and plan: one kernel writes the
+// append (new K/V from d_k_new, or straight from h_k_new when mapped), q
+// (from h_q when mapped) and the plan image into the workspace; attention and
+// merge follow, then (unmapped) the outputs' copies.  *launched = false when
+// the step does not qualify (nothing enqueued).
+int launch_fused(kvp_step_plan &sp, const kvp_step_io *io, void *ws, size_t ws_bytes, cudaStream_t st,
+                 bool *launched) {
+    *launched = false;
+    const bool mapped = (io->flags & KVP_STEP_HOST_MAPPED) != 0;
+    if (!mapped && (io->h_k_new || io->h_v_new || io->h_q)) return KVP_OK;
+    const PoolView pv = pool_view(sp.pool);
+    if (pv.kv4 || ws_bytes < sp.pk.w.total) return KVP_OK;
+    KvWrite w{};
+    w.k_pool = const_cast<void *>(pv.k);
+    w.v_pool = const_cast<void *>(pv.v);
+    w.k = mapped && io->h_k_new ? io->h_k_new : io->d_k_new;
+    w.v = mapped && io->h_v_new ? io->h_v_new : io->d_v_new;
+    w.L = pv.L; w.NB = pv.NB; w.Hkv = pv.Hkv; w.bs = pv.bs; w.d = pv.d;
+    w.ntok = (int32_t)sp.slots.size();
+    w.slots = sp.slots.data();
+    w.ncow = (int32_t)(sp.cow.size() / 3);
+    w.cow = sp.cow.data();
+    if (!step_write_fits(w, sp.pk.w.plan_bytes)) return KVP_OK;
+    *launched = true;
+    sp.ready = false;
+    const StepBytes b = step_bytes(sp.desc, sp.num_seqs, sp.ntok);
+    if (launch_step_write(w, mapped ? io->h_q : nullptr, io->d_q, b.q, sp.pk.image.data(), ws, sp.pk.w.plan_bytes,
+                          st) != cudaSuccess)
+        return KVP_ERR_CUDA;
+    void *out = mapped && io->h_out ? io->h_out : io->d_out;
+    float *lse = mapped && io->h_lse ? io->h_lse : io->d_lse;
+    int rc = launch_packed(sp.pk, sp.desc, io->d_q, pv.k, pv.v, sp.num_seqs, nullptr, 0, out, lse, ws, ws_bytes, st,
+                           nullptr, nullptr, nullptr, true);
+    if (rc || mapped) return rc;
+    if (io->h_out && cudaMemcpyAsync(io->h_out, io->d_out, b.q, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return KVP_ERR_CUDA;
+    if (io->h_lse && cudaMemcpyAsync(io->h_lse, io->d_lse, b.lse, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return KVP_ERR_CUDA;
+    return KVP_OK;
+}
+
 // The checks shared by kvp_decode_step and kvp_decode_step_plan; fills the
 // per-sequence token counts.
 int check_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, int32_t ntok, const kvp_attn_desc *desc,
@@ -972,8 +1014,23 @@ int kvp_decode_step(kvp_pool *pool, const int32_t *seq_ids, int32_t num_seqs, in
     rc = check_step(pool, seq_ids, num_seqs, ntok, desc, t_ntoks);
     if (rc) return rc;
     cudaStream_t st = (cudaStream_t)stream;
-    // the inputs' copies first, so that they run while the host plans
-    rc = step_inputs(io, step_bytes(*desc, num_seqs, ntok), ntok, st);
+    const StepBytes b = step_bytes(*desc, num_seqs, ntok);
+    const bool mapped = (io->flags & KVP_STEP_HOST_MAPPED) != 0;
+    if (mapped || !(io->h_k_new || io->h_v_new || io->h_q)) {
+        // inputs on the device or mapped: plan first, then (when the step
+        // qualifies) inputs, append and plan in one kernel
+        rc = plan_step(t_step, pool, seq_ids, num_seqs, ntok, *desc, t_ntoks.data());
+        if (rc) return rc;
+        if (ws_needed) *ws_needed = t_step.pk.w.total;
+        bool launched = false;
+        rc = launch_fused(t_step, io, workspace, ws_bytes, st, &launched);
+        if (rc || launched) return rc;
+        rc = step_inputs(io, b, ntok, st);
+        if (rc) return rc;
+        return launch_step(t_step, io, workspace, ws_bytes, st);
+    }
+    // copy-engine inputs first, so that they run while the host plans
+    rc = step_inputs(io, b, ntok, st);
     if (rc) return rc;
     rc = plan_step(t_step, pool, seq_ids, num_seqs, ntok, *desc, t_ntoks.data());
     if (rc) return rc;
@@ -1003,31 +1060,9 @@ int kvp_decode_step_run(kvp_step_plan *plan, const kvp_step_io *io, void *worksp
     if (rc) return rc;
     cudaStream_t st = (cudaStream_t)stream;
     const StepBytes b = step_bytes(plan->desc, plan->num_seqs, plan->ntok);
-    // mapped host buffers on a bf16 pool, a small append and plan: the inputs,
-    // the append and the plan in one kernel, then attention and merge
-    if (io->flags & KVP_STEP_HOST_MAPPED) {
-        const PoolView pv = pool_view(plan->pool);
-        KvWrite w{};
-        w.k_pool = const_cast<void *>(pv.k);
-        w.v_pool = const_cast<void *>(pv.v);
-        w.k = io->h_k_new ? io->h_k_new : io->d_k_new;
-        w.v = io->h_v_new ? io->h_v_new : io->d_v_new;
-        w.L = pv.L; w.NB = pv.NB; w.Hkv = pv.Hkv; w.bs = pv.bs; w.d = pv.d;
-        w.ntok = (int32_t)plan->slots.size();
-        w.slots = plan->slots.data();
-        w.ncow = (int32_t)(plan->cow.size() / 3);
-        w.cow = plan->cow.data();
-        if (!pv.kv4 && ws_bytes >= plan->pk.w.total && step_write_fits(w, plan->pk.w.plan_bytes)) {
-            plan->ready = false;
-            if (launch_step_write(w, io->h_q, io->d_q, b.q, plan->pk.image.data(), workspace, plan->pk.w.plan_bytes,
-                                  st) != cudaSuccess)
-                return KVP_ERR_CUDA;
-            void *out = io->h_out ? io->h_out : io->d_out;
-            float *lse = io->h_lse ? io->h_lse : io->d_lse;
-            return launch_packed(plan->pk, plan->desc, io->d_q, pv.k, pv.v, plan->num_seqs, nullptr, 0, out, lse,
-                                 workspace, ws_bytes, st, nullptr, nullptr, nullptr, true);
-        }
-    }
+    bool launched = false;
+    rc = launch_fused(*plan, io, workspace, ws_bytes, st, &launched);
+    if (rc || launched) return rc;
     rc = step_inputs(io, b, plan->ntok, st);
     if (rc) return rc;
     return launch_step(*plan, io, workspace, ws_bytes, st);
