@@ -12,6 +12,9 @@
 - a too-small workspace returns KVP_ERR_WORKSPACE with the size needed after
   the append, and paged_decode_attention_pool finishes the step; an append
   that does not fit returns KVP_ERR_OOM with the pool unchanged;
+- a step too large for the one-kernel input path (more than 64 appended
+  tokens, or a plan image above 24 KB) takes the copy kernel, plan upload and
+  write kernel instead, with the same results;
 - the step in two halves (kvp_decode_step_plan, kvp_decode_step_run): a
   planned-then-run step gives the same bits as the host-table entry point,
   a loop that plans step i + 1 while the device runs step i follows the
@@ -341,4 +344,48 @@ def test_planned_step_matches_host_tables_and_errors():
     check_close(to_f64(b["d_out"]), want)
     check_lse(to_f64(b["d_lse"]), want_lse)
     kvp.kvp_step_plan_destroy(plan)
+    p.close()
+
+
+@pytest.mark.parametrize("case", ["many_tokens", "big_plan"])
+def test_planned_step_beyond_the_one_kernel_path(case):
+    # many_tokens: 4 sequences x 20 appended tokens (80 > 64 slots);
+    # big_plan: 160 forked sequences with their own tails, whose plan image
+    # is larger than the 24 KB the one-kernel path carries
+    if case == "many_tokens":
+        p, ntok = Pool(), 20
+        seqs = p.forked_batch()
+    else:
+        p, ntok = Pool(nb=4096, seqs=170, mb=32), 1
+        root = p.m.alloc()
+        assert kvp.seq_alloc(p.pool) == root
+        p.append([root], [100])
+        seqs = []
+        for i in range(160):
+            c = p.m.fork(root)
+            assert kvp.seq_fork(p.pool, root) == c
+            seqs.append(c)
+        # tails of up to 400 tokens: about 500 KV tiles, a plan image near 28 KB
+        p.append(seqs, [1 + (37 * i) % 400 for i in range(160)])
+    S = len(seqs)
+    b = step_buffers(S, ntok)
+    io = kvp.step_io(b["d_q"], b["d_out"], b["d_lse"], b["d_k"], b["d_v"], h_k_new=b["h_k"], h_v_new=b["h_v"],
+                     h_q=b["h_q"], h_out=b["h_out"], h_lse=b["h_lse"], host_mapped=True)
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    sp = kvp.StepPlan(p.pool, seqs, ntok, io, p.desc, ws)
+    sp.plan()
+    k, v = p.kv(S * ntok)
+    q = W.normal_bf16(68, 0, (L, S, HQ, D))
+    bits_into(b["h_k"], k)
+    bits_into(b["h_v"], v)
+    bits_into(b["h_q"], q)
+    sp.run()
+    torch.cuda.synchronize()
+    assert kvp.kvp_device_error(ws) == 0
+    p.model_append(seqs, [ntok] * S, k, v)
+    p.same(seqs)
+    want, want_lse = p.oracle(q, seqs)
+    check_close(to_f64(b["h_out"]), want)
+    check_lse(to_f64(b["h_lse"]), want_lse)
+    sp.close()
     p.close()
