@@ -217,7 +217,7 @@ struct KCfg4 {
 // holds 4-bit codes and row exponents (a.k_pool / a.v_pool are the codes).
 template <int D, int TS, bool KV4, bool TREE>
 __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it, int l, int kvh,
-                                         int ntile, unsigned char *smem, const KvTile *s_tiles) {
+                                         int ntile, unsigned char *smem, const KvTile *s_tiles, int *s_next) {
     using C = KCfg<D>;
     using C4 = KCfg4<D>;
     constexpr int NSTAGE = KV4 ? C4::NSTAGE : C::NSTAGE;
@@ -428,6 +428,9 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
     for (int t = 0; t < ntile; ++t) {
         cp_async_wait<NSTAGE - 2>();
         __syncthreads();
+        // claim the next unit while the last tile computes (every thread
+        // read the current one before the first barrier of the loop)
+        if (t == ntile - 1 && threadIdx.x == 0) *s_next = (a.n_tc_units > 0 ? 0 : gridDim.x) + atomicAdd(a.counter, 1);
         if (t + NSTAGE - 1 < ntile) issue(t + NSTAGE - 1);
         cp_async_commit();
         if constexpr (KV4 && !REG4) {
@@ -766,8 +769,13 @@ __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kerne
         griddep_wait();
         waited = true;
     }
+    // units: the first is the block's index, each next one is claimed from
+    // the counter during the last tile of the one before.  Beside the
+    // tcgen05 kernel, whose CTAs hold SMs when this grid starts, every unit
+    // is claimed (a block that starts late must not hold one of the longest
+    // units; measured 1% on MCTS)
+    if (threadIdx.x == 0) s_unit = a.n_tc_units > 0 ? atomicAdd(a.counter, 1) : (int)blockIdx.x;
     for (;;) {
-        if (threadIdx.x == 0) s_unit = atomicAdd(a.counter, 1);
         __syncthreads();
         const int unit = s_unit;
         if (unit >= a.n_units) {
@@ -796,9 +804,9 @@ __global__ void __launch_bounds__(kThreads, KCfg<D>::MIN_BLOCKS) attn_item_kerne
         // The two-way split pays at head dim 128 (two CTAs per SM leave few
         // warps to hide latency); at head dim 64 the extra copy of the tile
         // loop costs more in instruction fetch than the split gains.
-        if (rows <= 16) run_unit<D, 4, KV4, TREE>(a, it, l, kvh, ntile, smem, s_tiles);
-        else if (D == 128 && rows <= 32) run_unit<D, 2, KV4, TREE>(a, it, l, kvh, ntile, smem, s_tiles);
-        else run_unit<D, 1, KV4, TREE>(a, it, l, kvh, ntile, smem, s_tiles);
+        if (rows <= 16) run_unit<D, 4, KV4, TREE>(a, it, l, kvh, ntile, smem, s_tiles, &s_unit);
+        else if (D == 128 && rows <= 32) run_unit<D, 2, KV4, TREE>(a, it, l, kvh, ntile, smem, s_tiles, &s_unit);
+        else run_unit<D, 1, KV4, TREE>(a, it, l, kvh, ntile, smem, s_tiles, &s_unit);
         __syncthreads();
     }
 }
