@@ -429,8 +429,10 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
         cp_async_wait<NSTAGE - 2>();
         __syncthreads();
         // claim the next unit while the last tile computes (every thread
-        // read the current one before the first barrier of the loop)
-        if (t == ntile - 1 && threadIdx.x == 0) *s_next = (a.n_tc_units > 0 ? 0 : gridDim.x) + atomicAdd(a.counter, 1);
+        // read the current one before the first barrier of the loop); by the
+        // last warp, which a unit of 33-48 rows leaves without rows
+        if (t == ntile - 1 && threadIdx.x == kThreads - 32)
+            *s_next = (a.n_tc_units > 0 ? 0 : gridDim.x) + atomicAdd(a.counter, 1);
         if (t + NSTAGE - 1 < ntile) issue(t + NSTAGE - 1);
         cp_async_commit();
         if constexpr (KV4 && !REG4) {
