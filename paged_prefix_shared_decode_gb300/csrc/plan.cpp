@@ -339,7 +339,7 @@ void pack_small(Scratch &sc, int32_t G, int thr) {
 }
 
 void finish(HostPlan &hp, Scratch &sc, int32_t G, int32_t nq, int32_t layers_heads, int32_t sms,
-            int32_t mma_ctas, int thr) {
+            int32_t mma_ctas, int thr, bool kv4 = false) {
     pack_small(sc, G, thr);
     const Protos &pr = sc.packed;
     auto &cs = sc.cs;
@@ -358,7 +358,10 @@ void finish(HostPlan &hp, Scratch &sc, int32_t G, int32_t nq, int32_t layers_hea
         // queue balances them, and fewer, longer units pay fewer unit
         // start-ups and leave fewer partial rows to merge (two per CTA
         // measured 8% slower on Dendrite, 3/4 per CTA 11% slower)
-        const int64_t target_units = 1LL * sms * (tc ? 1 : mma_ctas);
+        // (4-bit pages: a quarter more, since their tiles cost more to expand
+        // than to load; measured 2.6% faster on Dendrite, and 0.75 / 1.25 /
+        // 1.5 per CTA slower on bf16 pages)
+        const int64_t target_units = tc ? 1LL * sms : (kv4 ? 5LL * sms * mma_ctas / 4 : 1LL * sms * mma_ctas);
         int64_t chunk = kMaxItemTiles;
         if (n_protos * layers_heads < target_units) {
             int64_t want = (total_tiles * layers_heads + target_units - 1) / target_units;
@@ -494,7 +497,7 @@ int build_decode(const kvp_attn_desc &d, const int32_t *tables, const int32_t *l
         }
     }
     finish(hp, sc, G, S, d.num_layers * d.num_kv_heads, sms, attention_ctas_per_sm(d.head_dim),
-           tc_usable(d) ? tc_row_threshold(d.head_dim) : INT32_MAX);
+           tc_usable(d) ? tc_row_threshold(d.head_dim) : INT32_MAX, d.kv_format == KVP_KV_4BIT);
     return KVP_OK;
 }
 
