@@ -42,6 +42,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/kvp.h"
@@ -212,6 +213,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3, %4}], [%5];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 template <int D>
 struct TcCfg {
     static constexpr int NSLAB = D / 64;               // 64-column slabs (128-byte rows)
@@ -368,7 +378,8 @@ __device__ __noinline__ float2 recompute_step(uint32_t s_tm, float m, float sc, 
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                   const AttnLaunch a, const int box_rows) {
+                   const __grid_constant__ CUtensorMap qmap, const AttnLaunch a, const int box_rows,
+                   const int q_tma) {
     using C = TcCfg<D>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -549,6 +560,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else if (warp == kUnitWarp) {
         // ------------------------------------------------------------ units and Q
+        if (q_tma && lane == 0)
+            asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&qmap)) : "memory");
+        int last_q = -1;   // last unit whose Q load was issued
         auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
             int ok = 1;
             if (lane == 0) ok = wait(b, parity) ? 1 : 0;
@@ -575,14 +589,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_UNIT_FULL + slot));
             if (done) break;
-            // Q of this unit, once the previous unit's S MMAs are done with
-            // it: rows lane + 32 i, whose member indices are loaded first
+            // Q of this unit, once the previous unit's S MMAs are done with it
             ok = wait_warp(bar(C::B_Q_EMPTY), (uc & 1) ^ 1);
+            if (!ok) break;
             const int lk = unit / n_items;
             const int kvh = lk % a.Hkv, l = lk / a.Hkv;
             // (one 128-row tile, or two for a pair unit)
             const int rows = it.n_members * G;
             const int ntq = rows > 128 ? 2 : 1;
+            last_q = uc;
+            // By TMA when every box's members are consecutive query tokens: a
+            // box is the kv head's G query heads of max(1, 8 / G) consecutive
+            // tokens, i.e. max(8, G) whole rows of one 64-column slab, so each
+            // lands on a 1024-byte boundary of the 128-byte swizzle; boxes
+            // past the unit's members are read out of range (zero fill).
+            // Otherwise lane j gathers rows j + 32 i by cp.async.
+            if (q_tma) {
+                const int tpb = G < 8 ? 8 / G : 1;       // tokens per box
+                const int nbox = ntq * (128 / (tpb * G)) * C::NSLAB;
+                const int z_oob = a.L * a.nq;
+                bool consec = true;
+                int zc[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int b = lane + 32 * j;
+                    const int m0 = (b / C::NSLAB) * tpb;   // first member of the box
+                    zc[j] = z_oob;
+                    if (b < nbox && m0 < it.n_members) {
+                        const int q0 = __ldg(a.members + it.member_off + m0);
+                        for (int k = 1; k < tpb && m0 + k < it.n_members; ++k)
+                            consec = consec && __ldg(a.members + it.member_off + m0 + k) == q0 + k;
+                        zc[j] = l * a.nq + q0;
+                    }
+                }
+                if (__all_sync(0xffffffffu, consec) && nbox <= 64) {
+                    if (lane == 0) mbar_expect_tx(bar(C::B_Q_FULL), (uint32_t)(ntq * C::OPER));
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int b = lane + 32 * j;
+                        if (b < nbox) {
+                            const int cb = b % C::NSLAB, row = (b / C::NSLAB) * tpb * G;   // unit row
+                            tma_load_3d(q_smem + (row >> 7) * C::OPER + cb * C::SLAB + (row & 127) * 128, &qmap,
+                                        cb * 64, kvh * G, zc[j], bar(C::B_Q_FULL));
+                        }
+                    }
+                    cp_async_arrive(bar(C::B_Q_FULL));
+                    continue;
+                }
+            }
             for (int tq = 0; tq < ntq; ++tq) {
                 int qt[4];
 #pragma unroll
@@ -601,8 +656,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             cp_async_arrive(bar(C::B_Q_FULL));
-            if (!ok) break;
         }
+        // the last Q load lands before the CTA ends (at once after a normal run)
+        if (lane == 0 && last_q >= 0) settle(bar(C::B_Q_FULL), last_q & 1);
+        __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -979,12 +1036,16 @@ cudaError_t launch_tc_d(const AttnLaunch &a, cudaStream_t stream) {
     const int bs = 1 << a.bs_log2;
     const int box_rows = bs < kTileTokens ? bs : kTileTokens;
     const long long rows = (long long)a.L * a.NB * a.Hkv * bs;
-    alignas(64) CUtensorMap km, vm;
+    alignas(64) CUtensorMap km, vm, qm;
     if (!make_pool_map(&km, a.k_pool, D, rows, box_rows) || !make_pool_map(&vm, a.v_pool, D, rows, box_rows))
         return cudaErrorInvalidValue;
+    // Q boxes of max(8, G) rows must tile the 128-row operand
+    const int G = a.G;
+    const bool q_tma = (G <= 8 ? 8 % G == 0 : (G <= 128 && 128 % G == 0)) && make_q_map(&qm, a.q, D, a.Hq, (long long)a.L * a.nq, G);
+    if (!q_tma) std::memset(&qm, 0, sizeof qm);
     // one CTA per SM (its shared memory and TMEM allow no more)
     const int grid = a.n_tc_units < occ.sms ? a.n_tc_units : occ.sms;
-    attn_tc_kernel<D><<<grid, kTcThreads, TcCfg<D>::SMEM, stream>>>(km, vm, a, box_rows);
+    attn_tc_kernel<D><<<grid, kTcThreads, TcCfg<D>::SMEM, stream>>>(km, vm, qm, a, box_rows, q_tma ? 1 : 0);
     count_launch();
     return cudaGetLastError();
 }
@@ -1039,6 +1100,41 @@ bool make_pool_map(CUtensorMap *m, const void *pool, int D, long long rows, int 
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     keys[next] = MapKey{pool, rows, D, box_rows};
+    maps[next] = *m;
+    next = (next + 1) % kCache;
+    return true;
+}
+
+// 3-D view of the queries [L * nq tokens][Hq heads][D]; box = 64 columns x
+// G heads x max(1, 8 / G) tokens, 128-byte swizzle.  Cached like the pool
+// maps (the query buffer is usually the same from call to call).
+bool make_q_map(CUtensorMap *m, const void *q, int D, int Hq, long long ntok, int G) {
+    struct QKey {
+        const void *q;
+        long long ntok;
+        int D, Hq, G;
+    };
+    constexpr int kCache = 4;
+    thread_local QKey keys[kCache] = {};
+    thread_local CUtensorMap maps[kCache];
+    thread_local int next = 0;
+    if (!q || (reinterpret_cast<uintptr_t>(q) & 15) != 0 || ntok >= (1LL << 31) || G > Hq) return false;
+    for (int i = 0; i < kCache; ++i)
+        if (keys[i].q == q && keys[i].ntok == ntok && keys[i].D == D && keys[i].Hq == Hq && keys[i].G == G) {
+            *m = maps[i];
+            return true;
+        }
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)ntok};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(G < 8 ? 8 / G : 1)};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    keys[next] = QKey{q, ntok, D, Hq, G};
     maps[next] = *m;
     next = (next + 1) % kCache;
     return true;

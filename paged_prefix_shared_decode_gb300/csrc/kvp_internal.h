@@ -103,6 +103,10 @@ bool tc_path_supported(int L, int NB, int Hkv, int bs);
 // per-thread cache.  False when the driver's encoder is unavailable or
 // rejects the view.
 bool make_pool_map(CUtensorMap *m, const void *pool, int D, long long rows, int box_rows);
+// TMA view of the queries [ntok][Hq][D] (box: 64 columns x G heads x
+// max(1, 8 / G) tokens, 128-byte swizzle), cached the same way.  False when
+// q is not 16-byte aligned, the view is too large or the encoder rejects it.
+bool make_q_map(CUtensorMap *m, const void *q, int D, int Hq, long long ntok, int G);
 // CTAs of the mma.sync work-item kernel that fit on one SM for head dim D.
 int attention_ctas_per_sm(int D);
 // Rows above which items of head dim D run on the tcgen05 kernel
