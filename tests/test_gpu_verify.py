@@ -127,3 +127,20 @@ def test_verify_growing_scores():
     check_close(to_f64(call.out), want_o, max_abs_tol=peaked_max_abs(want_o, bf16_absmax(rw.v_pool)))
     check_lse(to_f64(call.lse), want_l)
     assert kvp.kvp_device_error(call.ws) == 0
+
+
+def test_verify_output_16_byte_aligned():
+    # An output only 16-byte aligned (the documented minimum) takes the
+    # tcgen05 epilogue's 16-byte stores instead of its 32-byte ones: same bits.
+    w = W.verify_tree(2, layers=1)
+    r, call = run_verify(w)
+    ref_o, ref_l = call.out.clone(), call.lse.clone()
+    buf = torch.empty(call.out.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    assert buf.data_ptr() % 32 == 0
+    off = buf[8:].view(call.out.shape)   # 16 bytes past a 32-byte boundary
+    q = bf16_tensor(W.verify_q(w))
+    kvp.tree_verify_attention(q, call.parent, call.n, r.k_pool, r.v_pool, call.h_tables, call.ctx, call.desc,
+                              off, call.lse, call.ws)
+    torch.cuda.synchronize()
+    assert torch.equal(off.view(torch.int16), ref_o.view(torch.int16))
+    assert torch.equal(call.lse, ref_l)
