@@ -5,7 +5,8 @@
 //
 // One persistent CTA of 12 warps per SM.  A work unit is (item, layer, kv
 // head): up to 128 query rows (the item's members x the GQA group of the kv
-// head) against the item's 64-token KV tiles, taken two at a time as
+// head), or a pair unit of up to 256 rows as two 128-row tiles over one K/V
+// stream, against the item's 64-token KV tiles, taken two at a time as
 // 128-token steps.
 //   warp 0      K producer, warp 1 V producer.  Each fills its own ring, since
 //               K is released as soon as S = Q K^T is computed and V only once
@@ -18,16 +19,21 @@
 //               K=128) with P_g read from TMEM.
 //   warp 3      claims units from an atomic counter, stages their tile
 //               descriptors in shared memory (two slots), and loads each
-//               unit's Q as soon as the previous unit's last S is done.
+//               unit's Q as soon as the previous unit's last S is done: by
+//               TMA boxes of whole rows (the G heads of consecutive query
+//               tokens) when the unit's members are consecutive tokens, else
+//               by a cp.async gather.
 //   warps 4-7   softmax group 0 (even steps), warps 8-11 group 1 (odd
 //               steps), one thread per query row.  Each group keeps its own
 //               running max m_g, sum l_g and accumulator O_g, so while one
 //               group turns step t's scores into P the tensor cores run the
 //               other group's P V and next S.  The two groups' (m, l, O) are
-//               merged when the unit ends.
+//               merged when the unit ends.  In a pair unit group g takes
+//               every step for the rows of tile g and writes them alone.
 // P (bf16 pairs) overwrites the S columns it came from, so it never passes
-// through shared memory.  The running max is raised only when a step's max
-// exceeds it by more than 32, so p < 2^32; O_g is then rescaled in TMEM.
+// through shared memory.  The running max is raised only when a step's P
+// would sum to more than 2^32, so every p <= 2^32; O_g is then rescaled in
+// TMEM.
 // Every wait is bounded; on a timeout the CTA sets bit 4 of the workspace
 // error word and all roles leave their loops; before the CTA frees its TMEM
 // and ends, the producers let the copies they issued land and the MMA thread
