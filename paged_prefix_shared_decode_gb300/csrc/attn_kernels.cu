@@ -39,6 +39,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "kv4_codes.cuh"
 #include "kvp_internal.h"
 
 namespace kvp {
@@ -132,41 +133,6 @@ __global__ void tree_mask_kernel(const int32_t *parent, int32_t nq, int32_t n, u
     if (q < nq) mask[q] = ancestor_mask(parent, q / n, q % n, n, err);
 }
 
-// 4-bit codes to bf16 mma operands.  A code c in [-7, 7] stored as a
-// two's-complement nibble u becomes bf16(136 + c) by placing u ^ 8 in the
-// low mantissa bits of 128 (bits 0x4300); then fma(x, 2^e, -136 * 2^e) =
-// c * 2^e exactly (one rounding of an exact, representable result) when
-// 2^e and 136 * 2^e are normal bf16 numbers (-126 <= e <= 120); otherwise
-// x - 136 = c (exact) and a multiply by 2^e.
-__device__ __forceinline__ uint32_t bf16_exp2_bits(int e) {   // 2^e, e in [-127, 127]
-    return e >= -126 ? (uint32_t)(e + 127) << 7 : 0x40u;
-}
-__device__ __forceinline__ uint32_t bf16_neg136_bits(int e) {   // -136 * 2^e, e in [-126, 120]
-    return 0x8000u | ((uint32_t)(134 + e) << 7) | 0x08u;
-}
-// scale pair (2^ea, 2^eb) as bf16x2 with the -136 * 2^e pair packed above
-// it: .x = scales, .y = constants (callers check the fused range)
-__device__ __forceinline__ uint2 exp_pair2(int ea, int eb) {
-    const int ca = min(max(ea, -126), 120), cb = min(max(eb, -126), 120);
-    return make_uint2(bf16_exp2_bits(ea) | (bf16_exp2_bits(eb) << 16),
-                      bf16_neg136_bits(ca) | (bf16_neg136_bits(cb) << 16));
-}
-__device__ __forceinline__ uint32_t nib_pair(uint32_t w, int i) {   // nibbles i and i + 4 as bf16(136 + c)
-    return ((w >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
-}
-__device__ __forceinline__ uint32_t conv_pair(uint32_t x, uint2 sc, bool fused) {
-    __nv_bfloat162 xv = *reinterpret_cast<__nv_bfloat162 *>(&x);
-    const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&sc.x);
-    __nv_bfloat162 r;
-    if (fused) {
-        const __nv_bfloat162 c2 = *reinterpret_cast<const __nv_bfloat162 *>(&sc.y);
-        r = __hfma2(xv, s2, c2);
-    } else {
-        const uint32_t k136 = 0x43084308u;
-        r = __hmul2(__hsub2(xv, *reinterpret_cast<const __nv_bfloat162 *>(&k136)), s2);
-    }
-    return *reinterpret_cast<uint32_t *>(&r);
-}
 // K word (8 dims of one token with exponent e) -> b[0..3] = pairs 0..3
 __device__ __forceinline__ void code_pairs_k(uint32_t w, int e, bool fused, uint32_t (&b)[4]) {
     const uint2 sc = exp_pair2(e, e);
@@ -321,15 +287,9 @@ __device__ __forceinline__ void run_unit(const AttnLaunch &a, const WorkItem &it
             const uint2 sc = exp_pair2(e, e);
             const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {   // word k: dims 32 q + 8 k .. + 7, byte b = dims 2b (low), 2b + 1
-                const uint32_t lo = w[k] & 0x0F0F0F0Fu, hi = (w[k] >> 4) & 0x0F0F0F0Fu;
+            for (int k = 0; k < 4; ++k) {   // word k: dims 32 q + 8 k .. + 7
                 uint4 v;
-                uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const uint32_t pr = __byte_perm(lo, hi, b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12));
-                    vv[b] = conv_pair((pr & 0x000F000Fu) ^ 0x43084308u, sc, fused);
-                }
+                expand_word(w[k], sc, fused, *reinterpret_cast<uint32_t(*)[4]>(&v));
                 const int c = 4 * q + k;
                 *reinterpret_cast<uint4 *>(smem + C4::BF_OFF + kv * C::TILE_BYTES + tok * D * 2 + ((c ^ (tok & 7)) << 4)) = v;
             }

@@ -52,6 +52,7 @@
 #include <mutex>
 
 #include "../../include/kvp.h"
+#include "kv4_codes.cuh"
 #include "kvp_internal.h"
 
 namespace kvp {
@@ -76,6 +77,11 @@ __device__ __forceinline__ uint32_t saddr(const void *p) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                  "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 // arrives on the barrier once every earlier cp.async of this thread has landed
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
@@ -239,7 +245,12 @@ struct TcCfg {
     static constexpr int Q_OFF = 0;                    // two 128-row Q tiles
     static constexpr int K_OFF = Q_OFF + 2 * OPER;
     static constexpr int V_OFF = K_OFF + NK * OPER;
-    static constexpr int DESC_OFF = V_OFF + NV * OPER;                                // [2][kMaxItemTiles]
+    // 4-bit pages: each producer stages one 64-token tile of codes and row
+    // exponents per buffer, two buffers, and expands it into its ring
+    static constexpr int CODE4 = kTileTokens * D / 2;   // codes of one tile
+    static constexpr int STG4_BUF = CODE4 + kTileTokens;
+    static constexpr int STG4_OFF = V_OFF + NV * OPER;
+    static constexpr int DESC_OFF = STG4_OFF + 2 * 2 * STG4_BUF;                      // [2][kMaxItemTiles]
     static constexpr int ML_OFF = DESC_OFF + 2 * kMaxItemTiles * (int)sizeof(KvTile);  // [2][128] float2
     static constexpr int UNIT_OFF = ML_OFF + 2 * 128 * 8;                           // [2] ints
     static constexpr int BAR_OFF = UNIT_OFF + 16;
@@ -381,7 +392,7 @@ __device__ __noinline__ float2 recompute_step(uint32_t s_tm, float m, float sc, 
     return make_float2(m_new, ls);
 }
 
-template <int D>
+template <int D, bool KV4>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                    const __grid_constant__ CUtensorMap qmap, const AttnLaunch a, const int box_rows,
@@ -478,7 +489,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const size_t block_stride = (size_t)a.Hkv * head_stride;
         // (block, 64-column slab) boxes of one 64-token tile
         const int nbox = (kTileTokens / box_rows) * C::NSLAB;
-        if (lane == 0)
+        if (!KV4 && lane == 0)
             asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
         // lane 0 waits (acquire) and the warp follows it (__syncwarp orders memory)
         auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
@@ -503,12 +514,104 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const size_t layer_base = (size_t)l * a.NB * block_stride + (size_t)kvh * head_stride;
             const int row_base_lh = (l * a.NB) * a.Hkv + kvh;   // row of block b = (row_base_lh + b*Hkv) * bs
             const KvTile *tiles = s_desc + slot * kMaxItemTiles;
+            // 4-bit pages: tile j's codes and row exponents go to staging
+            // buffer j mod 2 by cp.async (the next tile's while this one is
+            // expanded); the expansion writes bf16 rows into the ring stage in
+            // the layout the MMAs read (64-column slabs, 128-byte swizzle)
+            const uint32_t stg4 = saddr(smem + C::STG4_OFF + (is_v ? 2 : 0) * C::STG4_BUF);
+            auto load4 = [&](int j) {
+                const KvTile &kt = tiles[j];
+                const int ntok = kt.ntok_flags & 0xFFFF;
+                const int jb = kt.tok0 >> bs_log2;
+                const uint8_t *codes = static_cast<const uint8_t *>(is_v ? a.v_pool : a.k_pool);
+                const int8_t *exps = static_cast<const int8_t *>(is_v ? a.v_exp : a.k_exp);
+                const size_t lrow = (size_t)l * a.NB * a.Hkv;   // + block * Hkv + kvh, times bs
+                const uint32_t sb = stg4 + (j & 1) * C::STG4_BUF;
+                for (int x = lane; x < kTileTokens * (D / 32); x += 32) {
+                    const int tok = x / (D / 32), c = x % (D / 32);
+                    const uint8_t *src = codes;
+                    int bytes = 0;
+                    if (tok < ntok) {
+                        const int pos = kt.tok0 + tok;
+                        const int blk = kt.blk[(pos >> bs_log2) - jb];
+                        if ((unsigned)blk < (unsigned)a.NB) {
+                            const size_t row = ((lrow + (size_t)blk * a.Hkv + kvh) << bs_log2) + (pos & (bs - 1));
+                            src = codes + row * (D / 2) + c * 16;
+                            bytes = 16;
+                        } else if (c == 0) {
+                            atomicOr(a.err, 1);
+                        }
+                    }
+                    cp_async16(sb + tok * (D / 2) + c * 16, src, bytes);
+                }
+                // exponents: four groups of 16 tokens, each inside one block
+                // (decode tiles start on block boundaries, blocks hold a
+                // multiple of 16 tokens)
+                if (lane < 4) {
+                    const int8_t *src = exps;
+                    int bytes = 0;
+                    if (16 * lane < ntok) {
+                        const int pos = kt.tok0 + 16 * lane;
+                        const int blk = kt.blk[(pos >> bs_log2) - jb];
+                        if ((unsigned)blk < (unsigned)a.NB) {
+                            src = exps + ((lrow + (size_t)blk * a.Hkv + kvh) << bs_log2) + (pos & (bs - 1));
+                            bytes = 16;
+                        }
+                    }
+                    cp_async16(sb + C::CODE4 + 16 * lane, src, bytes);
+                }
+                cp_async_commit();
+            };
+            // tile in buffer sb to rows 64 h .. 64 h + 63 of the stage at dst:
+            // each lane turns 16-byte chunks of codes (32 dims of one row)
+            // into four 16-byte chunks of bf16 (exact: code * 2^e)
+            const unsigned char *stg4p = smem + C::STG4_OFF + (is_v ? 2 : 0) * C::STG4_BUF;
+            auto expand4 = [&](const unsigned char *sb, uint32_t dst, int h) {
+                constexpr int CH4 = D / 32;
+                for (int x = lane; x < kTileTokens * CH4; x += 32) {
+                    const int tok = x / CH4, q = x % CH4;
+                    const uint4 cw = *reinterpret_cast<const uint4 *>(sb + tok * (D / 2) + q * 16);
+                    const int e = (int)reinterpret_cast<const int8_t *>(sb + C::CODE4)[tok];
+                    const bool fused = e >= -126 && e <= 120;
+                    const uint2 sc = exp_pair2(e, e);
+                    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {   // word k: dims 32 q + 8 k .. + 7, chunk 4 q + k
+                        uint32_t v[4];
+                        expand_word(w[k], sc, fused, v);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                                         dst + swz(h * kTileTokens + tok, 4 * q + k)),
+                                     "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                                     : "memory");
+                    }
+                }
+            };
+            if constexpr (KV4)
+                if (ntile > 0) load4(0);
             bool alive = true;
             for (int t = 0; alive && t < nsteps; ++t, ++g) {
                 const int st = g % nring;
                 if (!wait_warp(bar(b_empty + st), ((g / nring) & 1) ^ 1)) { alive = false; break; }
                 const uint32_t dst = ring + st * C::OPER;
                 const uint32_t fb = bar(b_full + st);
+                if constexpr (KV4) {
+                    for (int h = 0; h < 2 && 2 * t + h < ntile; ++h) {
+                        const int j = 2 * t + h;
+                        if (j + 1 < ntile) {
+                            load4(j + 1);
+                            cp_async_wait<1>();
+                        } else {
+                            cp_async_wait<0>();
+                        }
+                        __syncwarp();
+                        expand4(stg4p + (j & 1) * C::STG4_BUF, dst, h);
+                        __syncwarp();
+                    }
+                    // the bf16 rows were written through the generic proxy
+                    fence_async_smem();
+                    mbar_arrive(fb);
+                    continue;
+                }
                 // whole tiles by TMA, one box per lane; ragged ones by cp.async
                 // with zero fill past the tile's end
                 bool tma[2] = {false, false};
@@ -1036,7 +1139,7 @@ struct TcOcc {
 };
 
 // Per device: the shared-memory attribute is set once for each device.
-template <int D>
+template <int D, bool KV4>
 TcOcc &tc_occ() {
     static TcOcc occ[kMaxDevices];
     static std::once_flag once[kMaxDevices];
@@ -1044,7 +1147,7 @@ TcOcc &tc_occ() {
     const int dev = current_device();
     if (dev < 0) return none;
     std::call_once(once[dev], [dev] {
-        if (cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(attn_tc_kernel<D, KV4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  TcCfg<D>::SMEM) != cudaSuccess)
             return;
         occ[dev].sms = device_sm_count();
@@ -1053,15 +1156,18 @@ TcOcc &tc_occ() {
     return occ[dev];
 }
 
-template <int D>
+template <int D, bool KV4>
 cudaError_t launch_tc_d(const AttnLaunch &a, cudaStream_t stream) {
-    TcOcc &occ = tc_occ<D>();
+    TcOcc &occ = tc_occ<D, KV4>();
     if (!occ.ok) return cudaErrorInvalidDevice;
     const int bs = 1 << a.bs_log2;
     const int box_rows = bs < kTileTokens ? bs : kTileTokens;
     const long long rows = (long long)a.L * a.NB * a.Hkv * bs;
     alignas(64) CUtensorMap km, vm, qm;
-    if (!make_pool_map(&km, a.k_pool, D, rows, box_rows) || !make_pool_map(&vm, a.v_pool, D, rows, box_rows))
+    std::memset(&km, 0, sizeof km);
+    std::memset(&vm, 0, sizeof vm);
+    // (4-bit pages: the producers copy codes by cp.async, no pool maps)
+    if (!KV4 && (!make_pool_map(&km, a.k_pool, D, rows, box_rows) || !make_pool_map(&vm, a.v_pool, D, rows, box_rows)))
         return cudaErrorInvalidValue;
     // Q boxes of max(8, G) rows must tile the 128-row operand
     const int G = a.G;
@@ -1070,7 +1176,7 @@ cudaError_t launch_tc_d(const AttnLaunch &a, cudaStream_t stream) {
     // one CTA per SM (its shared memory and TMEM allow no more)
     const int grid = a.n_tc_units < occ.sms ? a.n_tc_units : occ.sms;
     const int out32 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0 ? 1 : 0;
-    attn_tc_kernel<D><<<grid, kTcThreads, TcCfg<D>::SMEM, stream>>>(km, vm, qm, a, box_rows, q_tma ? 1 : 0, out32);
+    attn_tc_kernel<D, KV4><<<grid, kTcThreads, TcCfg<D>::SMEM, stream>>>(km, vm, qm, a, box_rows, q_tma ? 1 : 0, out32);
     count_launch();
     return cudaGetLastError();
 }
@@ -1173,8 +1279,8 @@ bool tc_path_supported(int L, int NB, int Hkv, int bs) {
 cudaError_t launch_attention_tc(const AttnLaunch &a, cudaStream_t stream, int ctas_per_sm) {
     (void)ctas_per_sm;
     if (a.n_tc_units <= 0) return cudaSuccess;
-    if (a.D == 64) return launch_tc_d<64>(a, stream);
-    if (a.D == 128) return launch_tc_d<128>(a, stream);
+    if (a.D == 64) return a.kv4 ? launch_tc_d<64, true>(a, stream) : launch_tc_d<64, false>(a, stream);
+    if (a.D == 128) return a.kv4 ? launch_tc_d<128, true>(a, stream) : launch_tc_d<128, false>(a, stream);
     return cudaErrorInvalidValue;
 }
 

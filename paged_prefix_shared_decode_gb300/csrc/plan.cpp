@@ -225,8 +225,7 @@ int tc_row_threshold(int head_dim) {
 namespace {
 
 bool tc_usable(const kvp_attn_desc &d) {
-    // 4-bit pages run on the mma.sync kernel only
-    return d.kv_format == KVP_KV_BF16 && tc_row_threshold(d.head_dim) != INT32_MAX &&
+    return tc_row_threshold(d.head_dim) != INT32_MAX &&
            tc_path_supported(d.num_layers, d.num_blocks, d.num_kv_heads, d.block_size);
 }
 

@@ -18,14 +18,15 @@ if not torch.cuda.is_available():
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUBSET = ("tiny_fork or dendrite_full or trellis or mcts_tree or ragged or cow or gqa or "
-          "verify_B1 or verify_tree_shapes or short_draft or growing_scores")
+          "verify_B1 or verify_tree_shapes or short_draft or growing_scores or "
+          "quantise_on_append or tree_shaped_sharing or scaled_rows")
 
 
 @pytest.mark.parametrize("path", ["tc", "mma"])
 def test_forced_attention_path(path):
     env = dict(os.environ, KVP_ATTN_PATH=path)
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "-m", "gpu",
-                        "tests/test_gpu_decode.py", "tests/test_gpu_verify.py", "-k", SUBSET],
+                        "tests/test_gpu_decode.py", "tests/test_gpu_verify.py", "tests/test_gpu_kv4.py", "-k", SUBSET],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
 
