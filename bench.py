@@ -645,8 +645,7 @@ def sweep_kv4(name, dev):
     ht, hl = kvp.kvp_gather_tables(r.pool, seqs, w.max_blocks_per_seq)
     desc = r.attn_desc(True)
     st = kvp.kvp_decode_plan_stats(desc, ht, hl)
-    # the planner counts bf16 bytes: rescale to the 4-bit rows
-    ub4 = st["unique_kv_bytes"] * (s.d // 2 + 1) // (2 * s.d)
+    ub4 = st["unique_kv_bytes"]   # in the 4-bit rows' bytes
     q = torch.randn((s.L, S, s.Hq, s.d), generator=g, device=dev).to(torch.bfloat16)
     o = torch.empty((s.L, S, s.Hq, s.d), dtype=torch.bfloat16, device=dev)
     ls = torch.empty((s.L, S, s.Hq), dtype=torch.float32, device=dev)
@@ -660,7 +659,8 @@ def sweep_kv4(name, dev):
              "sequences": S, "unique_kv_bytes": ub4, "bits_per_value": 4 + 8 / s.d,
              "kernel_ms": kms, "ms_per_call": ms, "tokens_per_s": S / (ms / 1e3),
              "unique_gb_per_s": ub4 / (kms / 1e3) / 1e9, "frac": ub4 / (kms / 1e3) / 1e9 / peak,
-             "kernel": "attn_item_kernel<d, 4-bit>", "traffic": None}
+             "kernel": "attn_item_kernel<d, 4-bit> (and attn_tc_kernel<d, 4-bit> for items of more than "
+                       "32 rows at head dim 128)", "traffic": None}
     tr = traffic_for(name)
     if tr:
         entry["traffic"] = float(tr["dram_bytes_per_launch"])

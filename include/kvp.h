@@ -499,7 +499,8 @@ int kvp_device_error(void *workspace, void *stream, int32_t *err_out);
 /* Host-side view of the decode plan (no device work; for tests and tools):
  * work items, row tiles, 64-token KV tiles and partial rows per (layer, kv
  * head), and the bytes of distinct (block, valid tokens) one call reads over
- * all layers, planned for a GPU with sm_count SMs.  Any out-pointer may be
+ * all layers (K and V rows in the pool's format: d bf16 values, or d/2 code
+ * bytes and one exponent byte), planned for a GPU with sm_count SMs.  Any out-pointer may be
  * NULL.  The plan's internal invariants (tile ranges inside the tile list
  * and within the kernels' descriptor stage, rows within each kernel's unit,
  * member intervals inside their items) are checked: KVP_ERR_STATE if one

@@ -444,7 +444,10 @@ int build_decode(const kvp_attn_desc &d, const int32_t *tables, const int32_t *l
     TileSrc src{tables, MB, bs};
     Protos &pr = sc.protos;
     pr.clear();
-    const int64_t tok_bytes = 2LL * d.num_kv_heads * d.head_dim * 2 * d.num_layers;
+    // K and V rows in the pool's format: d bf16 values, or d / 2 code bytes and
+    // one exponent byte
+    const int64_t tok_bytes = 2LL * d.num_kv_heads * d.num_layers *
+                              (d.kv_format == KVP_KV_4BIT ? d.head_dim / 2 + 1 : d.head_dim * 2);
     if (d.use_sharing) {
         sc.order.clear();
         sc.segs.clear();

@@ -13,7 +13,7 @@ computed here from the block tables alone.
 - the pool-table and host-table entry points size the same workspace;
 - the plan keeps its own invariants (checked inside kvp_decode_plan_stats)
   on both kernels' shapes: head dim 64 (mma.sync only) and head dim 128 with
-  many-row items on the tcgen05 kernel."""
+  many-row items on the tcgen05 kernel, on bf16 and on 4-bit pages."""
 import random
 
 import numpy as np
@@ -93,10 +93,12 @@ def test_plan_is_repeatable_and_rejects_bad_tables():
     kvp.kv_pool_destroy(p)
 
 
+@pytest.mark.parametrize("kv4", [False, True])
 @pytest.mark.parametrize("seed", range(4))
-def test_plan_invariants_with_tcgen05_items(seed):
+def test_plan_invariants_with_tcgen05_items(seed, kv4):
     # head dim 128, GQA 4: items of more than 32 rows go to the tcgen05
-    # kernel, the rest to mma.sync; a wide fork gives both
+    # kernel, the rest to mma.sync; a wide fork gives both (on bf16 and on
+    # 4-bit pages alike)
     rng = random.Random(seed)
     bs, n = 16, 48
     p = kvp.kv_pool_create(kvp.PoolDesc(2, 4096, bs, 8, 128, n + 1, 96, seed + 7))
@@ -108,8 +110,10 @@ def test_plan_invariants_with_tcgen05_items(seed):
         kvp.seq_reserve(p, s, rng.randrange(1, 3 * bs))
         seqs.append(s)
     t, ln = kvp.kvp_gather_tables(p, seqs, 96)
-    d = kvp.AttnDesc(2, 32, 8, 128, bs, 4096, 0.0, 1)
+    fmt = kvp.KVP_KV_4BIT if kv4 else kvp.KVP_KV_BF16
+    d = kvp.AttnDesc(2, 32, 8, 128, bs, 4096, 0.0, 1, fmt)
     st = kvp.kvp_decode_plan_stats(d, t, ln)
-    assert st["unique_kv_bytes"] == unique_bytes(t, ln, bs, 2 * 8 * 128 * 2 * 2)
+    per_tok = 2 * 8 * (128 // 2 + 1) * 2 if kv4 else 2 * 8 * 128 * 2 * 2
+    assert st["unique_kv_bytes"] == unique_bytes(t, ln, bs, per_tok)
     assert st["row_tiles"] == -(-n // (256 // 4))
     kvp.kv_pool_destroy(p)
