@@ -544,6 +544,14 @@ def _timed_calls(call, flush, stream, reps=5, warm=3):
             float(np.mean([e[2].elapsed_time(e[3]) for e in ev])))
 
 
+def max_sm_mhz():
+    """Maximum SM clock (MEASURED_PEAKS.json, else GB300's 2070 MHz)."""
+    try:
+        return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["sm_max_mhz"])
+    except (OSError, KeyError, ValueError):
+        return 2070.0
+
+
 def tensor_peak():
     try:
         return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"]), "measured"
@@ -551,9 +559,10 @@ def tensor_peak():
         return 1900.0, "fallback"
 
 
-def sweep_decode(name, dev):
+def sweep_decode(name, dev, alloc_seed=1):
     """One decode workload of the sweep: sharing on (the planned call) and off
-    (every sequence reads its own blocks), and one layer alone."""
+    (every sequence reads its own blocks), and one layer alone.  alloc_seed 0:
+    the pool hands out blocks in id order (the contiguous control)."""
     import torch
     import paged_prefix_shared_decode_gb300 as kvp
     from paged_prefix_shared_decode_gb300.runner import PoolRunner
@@ -569,7 +578,7 @@ def sweep_decode(name, dev):
         return (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16),
                 torch.randn(shape, generator=g, device=dev).to(torch.bfloat16))
 
-    r = PoolRunner(w, alloc_seed=1)
+    r = PoolRunner(w, alloc_seed=alloc_seed)
     r.run_ops(kv_dev_fn=kv_dev)
     S = len(w.batch)
     seqs = np.array([r.ids[n] for n in w.batch], np.int32)
@@ -584,8 +593,9 @@ def sweep_decode(name, dev):
     st = kvp.kvp_decode_plan_stats(r.attn_desc(True), ht, hl)
     ub = st["unique_kv_bytes"]
     flops = 4 * s.d * s.Hq * int(hl.sum()) * s.L
-    entry = {"workload": name, "config": describe(w), "sequences": S, "unique_kv_bytes": ub,
-             "items": st["items"], "partial_rows": st["partial_rows"]}
+    entry = {"workload": name + ("_contig" if alloc_seed == 0 else ""),
+             "config": describe(w) + ("; blocks handed out in id order (alloc_seed 0)" if alloc_seed == 0 else ""),
+             "sequences": S, "unique_kv_bytes": ub, "items": st["items"], "partial_rows": st["partial_rows"]}
     for sharing in (True, False):
         desc = r.attn_desc(use_sharing=sharing)
         wsb = kvp.kvp_decode_workspace_size(desc, ht, hl)
@@ -608,7 +618,7 @@ def sweep_decode(name, dev):
             entry["sharing_off"] = {"kernel_ms": kms, "ms_per_call": ms,
                                     "unique_gb_per_s": ub / (kms / 1e3) / 1e9, "frac": ub / (kms / 1e3) / 1e9 / peak}
         del ws
-    tr = traffic_for(w.name)
+    tr = traffic_for(w.name) if alloc_seed == 1 else None
     entry["traffic"] = float(tr["dram_bytes_per_launch"]) if tr else None
     r.close()
     del flush
@@ -670,6 +680,63 @@ def sweep_kv4(name, dev):
     return entry
 
 
+def sweep_trellis_loop(phi, dev, steps=64):
+    """The Trellis benchmark's whole decode loop: from the sessions' prompts
+    (length 512) through `steps` decode steps, each appending one token per
+    session and attending over all layers (kvp_decode_step on device-resident
+    inputs), timed as one block of steps with CUDA events."""
+    import torch
+    import paged_prefix_shared_decode_gb300 as kvp
+    from paged_prefix_shared_decode_gb300.runner import PoolRunner
+    w = W.trellis(phi, decode=1)   # the prompts only
+    s = w.shapes
+    g = torch.Generator(device=dev).manual_seed(1)
+
+    def kv_dev(w_, i):
+        n = w_.ops[i][2]
+        shape = (s.L, n, s.Hkv, s.d)
+        return (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16),
+                torch.randn(shape, generator=g, device=dev).to(torch.bfloat16))
+
+    r = PoolRunner(w, alloc_seed=1)
+    r.run_ops(kv_dev_fn=kv_dev)
+    S = len(w.batch)
+    seqs = np.array([r.ids[n] for n in w.batch], np.int32)
+    desc = r.attn_desc(True)
+    kd = torch.randn((steps, s.L, S, s.Hkv, s.d), generator=g, device=dev).to(torch.bfloat16)
+    vd = torch.randn((steps, s.L, S, s.Hkv, s.d), generator=g, device=dev).to(torch.bfloat16)
+    qd = torch.randn((steps, s.L, S, s.Hq, s.d), generator=g, device=dev).to(torch.bfloat16)
+    out = torch.empty((s.L, S, s.Hq, s.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((s.L, S, s.Hq), dtype=torch.float32, device=dev)
+    t0, l0 = kvp.kvp_gather_tables(r.pool, seqs, w.max_blocks_per_seq)
+    ws_bytes = 2 * kvp.kvp_decode_workspace_size(desc, t0, l0) + (8 << 20)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ios = [kvp.step_io(qd[i], out, lse, kd[i], vd[i]) for i in range(steps)]
+    calls = [kvp.DecodeStep(r.pool, seqs, 1, io, desc, ws, ws_bytes, stream=stream) for io in ios]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for c in calls:
+        c()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    _, ln = kvp.kvp_gather_tables(r.pool, seqs, w.max_blocks_per_seq)
+    entry = {"workload": f"trellis{phi}_loop",
+             "config": (f"Trellis-shaped decode loop: {s.L} layers, {s.Hq}q/{s.Hkv}kv heads, d {s.d}, block {s.bs}, "
+                        f"bf16; 64 sessions from length 512 (phi={phi}, prefixBlocks={w.info['prefix_blocks']}) "
+                        f"through {steps} decode steps (append one token per session, attention over all layers)"),
+             "sequences": S, "steps": steps, "ms": ms, "ms_per_step": ms / steps,
+             "tokens_per_s": S * steps / (ms / 1e3), "final_length": int(ln.max()),
+             "how": "CUDA events around the block of steps (kvp_decode_step on device buffers: append, plan "
+                    "from the pool's tables, attention, merge); no L2 flush between steps"}
+    r.close()
+    del ws, kd, vd, qd
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_sweep(a, dev):
     """The rest of the metric beside the headline: the phi sweep, MCTS and
     verify on the device, the radix prefix cache on the host."""
@@ -678,7 +745,7 @@ def run_sweep(a, dev):
     out = []
     names = ["trellis0.0", "trellis0.25", "trellis0.5", "trellis0.75", "trellis0.9", "mcts",
              "verify1", "verify8", "verify32", "dendrite_kv4", "trellis0.0_kv4", "mcts_kv4",
-             "radix0.5", "radix0.9"]
+             "radix0.5", "radix0.9", "dendrite_contig", "trellis0.0_loop", "trellis0.9_loop"]
     if a.sweep_set:
         names = [n for n in a.sweep_set.split(",") if n]
     for name in names:
@@ -688,16 +755,30 @@ def run_sweep(a, dev):
         if name.endswith("_kv4"):
             out.append(sweep_kv4(name, dev))
             continue
+        if name.endswith("_contig"):
+            out.append(sweep_decode(name[:-len("_contig")], dev, alloc_seed=0))
+            continue
+        if name.endswith("_loop"):
+            out.append(sweep_trellis_loop(float(name[len("trellis"):-len("_loop")]), dev))
+            continue
         if name.startswith("verify"):
             sub = argparse.Namespace(**vars(a))
             sub.steps, sub.warmup = 5, 3
             res, w = run_verify_bench(sub, workload(name, 0), 0, 1, dev, single_layer=True)
             rf = res["roofline"]
+            # third bound: one exp per (query row, key attended), at the
+            # ex2.approx.ftz.f32 rate a probe measured on this GPU (about 60
+            # results per clock per SM), at the maximum SM clock
+            exps = rf["tensor_tflops"] * 1e12 * rf["kernel_ms"] / 1e3 / (4 * w.shapes.d)
+            props = torch.cuda.get_device_properties(dev)
+            exp_ms = exps / (60.0 * props.multi_processor_count * max_sm_mhz() * 1e6) * 1e3
             out.append({"workload": name, "config": describe(w), "query_tokens": res["config"]["query_tokens_per_step"],
                         "unique_kv_bytes": rf["algorithmic_bytes_per_launch"], "kernel_ms": rf["kernel_ms"],
                         "ms_per_call": res["ms_per_step"], "tokens_per_s": res["value"],
                         "unique_gb_per_s": rf["achieved"], "frac": rf["frac"],
                         "tensor_tflops": rf["tensor_tflops"], "tensor_frac": rf["tensor_frac"],
+                        "exp_bound": {"exps": exps, "ms": exp_ms, "frac": exp_ms / rf["kernel_ms"],
+                                      "rate": "60 ex2 results per clock per SM (probe on this GPU), max SM clock"},
                         "single_layer": res["single_layer"], "traffic": None})
             torch.cuda.empty_cache()
             continue
