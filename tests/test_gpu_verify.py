@@ -144,3 +144,11 @@ def test_verify_output_16_byte_aligned():
     torch.cuda.synchronize()
     assert torch.equal(off.view(torch.int16), ref_o.view(torch.int16))
     assert torch.equal(call.lse, ref_l)
+
+
+def test_verify_partly_filled_pair_unit():
+    # 40 draft nodes x G 4 = 160 query rows: a pair unit whose second 128-row
+    # tile holds 32 rows (its Q boxes past the members read zeros; that
+    # tile's output rows are written row by row), over a context that ends
+    # inside a block
+    run_verify(W.verify_tree(2, layers=1, ctx=1000, n_draft=40))
